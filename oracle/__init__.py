@@ -1,0 +1,159 @@
+"""CPU fp64 oracle for exact scaled dot-product attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product path (the CUDA
+library in ``exact_io_aware_04_gb300``) never imports this package, and this
+package imports nothing from it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, one row at a time, the
+definition written out); this module only compiles it and marshals arrays.
+
+Parity status of each function (what pins it, see ``tests/test_oracle.py``):
+  prefill_rows -- pinned: the two-tile worked example and the normaliser
+                  example (printed values), keep matrices for both causal
+                  corners, the GQA head map, torch SDPA fp64 MATH backend with
+                  an explicit bottom-right keep mask, shift invariance, the
+                  log-sum-exp merge identity, rows summing to one.
+  decode_rows  -- pinned: equals prefill_rows on the keys gathered through the
+                  block table as the paged-gather example describes, and the
+                  example's gathered shape.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_long
+            D = ctypes.c_double
+            lib.oracle_prefill_rows.argtypes = [P, P, P, I, I, I, I, I, I, D, I, P, P, P, L, P, P, I]
+            lib.oracle_prefill_rows.restype = I
+            lib.oracle_decode_rows.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, L, P, P, I]
+            lib.oracle_decode_rows.restype = I
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    """CPUs this process may run on (sched_getaffinity)."""
+    return int(_load().oracle_num_threads())
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype != torch.bfloat16:
+        raise TypeError("oracle inputs are bf16 tensors")
+    return np.ascontiguousarray(t.detach().to("cpu").contiguous().view(torch.int16).numpy())
+
+
+def _i32(t) -> np.ndarray:
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        t = t.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(t, dtype=np.int32))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def prefill_rows(q, k, v, *, B, Hq, Hkv, Nq, Nk, scale, causal, rows,
+                 cu_q=None, cu_k=None, threads: int = 0):
+    """Rows (b, h, i) of softmax(QK^T*scale + mask) V and their lse, fp64.
+
+    q [T_q, Hq, d], k/v [T_k, Hkv, d] bf16; rows int [n, 3].
+    Returns (out [n, d] float64, lse [n] float64)."""
+    d = int(q.shape[-1])
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    r = _i32(rows).reshape(-1, 3)
+    n = r.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    cq, ck = _i32(cu_q), _i32(cu_k)
+    rc = _load().oracle_prefill_rows(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d,
+                                     float(scale), int(bool(causal)), _ptr(cq), _ptr(ck),
+                                     _ptr(r), n, _ptr(out), _ptr(lse),
+                                     threads if threads > 0 else num_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_prefill_rows rejected its arguments (status {rc})")
+    return out, lse
+
+
+def decode_rows(q, k_cache, v_cache, block_table, seq_lens, *, scale, rows, threads: int = 0):
+    """Rows (b, h) of paged single-query attention, fp64.
+
+    q [B, Hq, d]; caches [num_pages, page, Hkv, d]; block_table int [B, max_pages];
+    seq_lens int [B]; rows int [n, 2].  Returns (out [n, d], lse [n])."""
+    B, Hq, d = (int(x) for x in q.shape)
+    page, Hkv = int(k_cache.shape[1]), int(k_cache.shape[2])
+    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    r = _i32(rows).reshape(-1, 2)
+    n = r.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = _load().oracle_decode_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), int(bt.shape[1]),
+                                    _ptr(sl), B, Hq, Hkv, d, page, float(scale), _ptr(r), n,
+                                    _ptr(out), _ptr(lse), threads if threads > 0 else num_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_decode_rows rejected its arguments (status {rc})")
+    return out, lse
+
+
+def all_rows(p) -> np.ndarray:
+    """Every (b, h, i) row of a prefill problem (small problems only)."""
+    out = []
+    for b, (nq, _) in enumerate(p.seq_lens()):
+        for h in range(p.Hq):
+            for i in range(nq):
+                out.append((b, h, i))
+    return np.asarray(out, dtype=np.int32).reshape(-1, 3)
+
+
+def prefill(p, rows=None, threads: int = 0):
+    """prefill_rows over a workloads.Prefill problem (all rows by default)."""
+    if rows is None:
+        rows = all_rows(p)
+    return prefill_rows(p.q, p.k, p.v, B=p.B, Hq=p.Hq, Hkv=p.Hkv, Nq=p.Nq, Nk=p.Nk,
+                        scale=p.scale, causal=p.causal, rows=rows, cu_q=p.cu_q, cu_k=p.cu_k,
+                        threads=threads)
+
+
+def decode(p, rows=None, threads: int = 0):
+    """decode_rows over a workloads.Decode problem (all (b, h) by default)."""
+    if rows is None:
+        rows = np.asarray([(b, h) for b in range(p.B) for h in range(p.Hq)], dtype=np.int32)
+    return decode_rows(p.q, p.k_cache, p.v_cache, p.block_table, p.seq_lens, scale=p.scale,
+                       rows=rows, threads=threads)

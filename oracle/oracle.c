@@ -1,0 +1,339 @@
+/*
+ * oracle.c -- plain, slow, obviously correct fp64 CPU reference for exact
+ * scaled dot-product attention: dense and packed (varlen) prefill with a
+ * bottom-right causal mask and grouped-query heads, and paged decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The CUDA library never
+ * calls it, and the two share no code, header or table.
+ *
+ * What one output row is (the definition, written out; no tiling and no online
+ * recurrence -- two plain passes over the allowed keys):
+ *
+ *   A_i   = { j : 0 <= j < Nk_b  and  (not causal  or  j <= i + Nk_b - Nq_b) }
+ *   s_j   = scale * sum_c q[i,c] * k[j,c]                 for j in A_i
+ *   m     = max_{j in A_i} s_j
+ *   l     = sum_{j in A_i} exp(s_j - m)
+ *   O_i,c = sum_{j in A_i} exp(s_j - m) * v[j,c] / l
+ *   lse_i = m + ln(l)
+ *   A_i empty  ->  O_i = 0 and lse_i = -inf.
+ *
+ * Passages followed:
+ *  - the operator: softmax(Q K^T * scale) V, "Deep Dive - FlashAttention",
+ *    opening section; "FlashAttention: Part 1", sections 1.2 and 3.2;
+ *  - max subtraction before the exponentials: "Flash Attention: A Complete
+ *    Architectural Autopsy", part 2, "The Online Softmax Recurrence" (the
+ *    plain softmax formula for row i);
+ *  - lse = m + log l, defined for a nonempty row: "Deep Dive - FlashAttention",
+ *    section "Exact attention without an n x n workspace";
+ *  - an entirely masked row returns zero: same page, section "Online softmax
+ *    is what makes the tiles exact"; its lse is read as log 0 = -inf (the page
+ *    defines lse only for nonempty rows; -inf is the value that leaves a
+ *    log-sum-exp merge unchanged);
+ *  - keep rule j <= i + Nk - Nq (bottom-right corner): same page, section
+ *    "Causal 2.1 is the decode gotcha";
+ *  - query head h reads K/V head h / (Hq / Hkv) (consecutive groups): same
+ *    page, section "The public interface is several kernels";
+ *  - packed sequences: sequence b owns tokens [cu[b], cu[b+1]), section
+ *    "Paged KV is a lookup, not a cache manager";
+ *  - paged keys: logical token t of sequence b sits in physical page
+ *    block_table[b][t / page] at slot t % page: "FlashAttention-3 and
+ *    PagedAttention", sections "Block tables and what the kernel does" and
+ *    "Runnable Example: Measuring the IO Gap" (the block-table gather).
+ *
+ * Inputs are bf16 bit patterns (uint16); each is widened exactly to double.
+ * Threads: POSIX threads over output rows; each row is computed by one thread
+ * in the order written above, so results do not depend on the thread count.
+ */
+#define _GNU_SOURCE
+#include <math.h>
+#include <pthread.h>
+#include <sched.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ---- bf16 -> double (exact: bf16 is the top half of an IEEE binary32) ---- */
+static double bf16_value(uint16_t bits)
+{
+    uint32_t word = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &word, sizeof f);
+    return (double)f;
+}
+
+/* ---- the mask: is key j allowed for query row i of a (nq, nk) sequence? ---- */
+static int key_allowed(long i, long j, long nq, long nk, int causal)
+{
+    if (j < 0 || j >= nk)
+        return 0;
+    if (causal && j > i + nk - nq) /* bottom-right aligned corner */
+        return 0;
+    return 1;
+}
+
+/* ---- where the key/value rows of one sequence live ---- */
+typedef struct {
+    const uint16_t *k, *v;    /* K and V base pointers */
+    long first_token;         /* contiguous: token row of key 0 */
+    const int32_t *pages;     /* paged: this sequence's block-table row, else NULL */
+    int page_size;
+    int hkv, d;
+} key_store;
+
+static long token_of_key(const key_store *ks, long j)
+{
+    if (ks->pages) {
+        long page = ks->pages[j / ks->page_size];
+        return page * ks->page_size + j % ks->page_size;
+    }
+    return ks->first_token + j;
+}
+
+static const uint16_t *key_row(const key_store *ks, const uint16_t *base, long j, int g)
+{
+    return base + (token_of_key(ks, j) * ks->hkv + g) * (long)ks->d;
+}
+
+/* ---- one output row, by the definition ---- */
+static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
+                       long i, long nq, long nk, int causal, double scale,
+                       double *s, double *out, double *lse)
+{
+    const int d = ks->d;
+    double m = -INFINITY;
+    long n_allowed = 0;
+
+    /* pass 1: scores of the allowed keys and their maximum */
+    for (long j = 0; j < nk; ++j) {
+        if (!key_allowed(i, j, nq, nk, causal))
+            continue;
+        const uint16_t *k_row = key_row(ks, ks->k, j, g);
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += bf16_value(q_row[c]) * bf16_value(k_row[c]);
+        s[j] = scale * dot;
+        if (n_allowed == 0 || s[j] > m)
+            m = s[j];
+        ++n_allowed;
+    }
+
+    for (int c = 0; c < d; ++c)
+        out[c] = 0.0;
+    if (n_allowed == 0) {
+        *lse = -INFINITY;
+        return;
+    }
+
+    /* pass 2: normaliser and value-weighted sum, relative to the maximum */
+    double l = 0.0;
+    for (long j = 0; j < nk; ++j) {
+        if (!key_allowed(i, j, nq, nk, causal))
+            continue;
+        double w = exp(s[j] - m);
+        l += w;
+        const uint16_t *v_row = key_row(ks, ks->v, j, g);
+        for (int c = 0; c < d; ++c)
+            out[c] += w * bf16_value(v_row[c]);
+    }
+    for (int c = 0; c < d; ++c)
+        out[c] /= l;
+    *lse = m + log(l);
+}
+
+/* ---- row jobs ---- */
+typedef struct {
+    /* shared inputs */
+    const uint16_t *q, *k, *v;
+    int B, Hq, Hkv, Nq, Nk, d, causal, paged, page_size, max_pages;
+    double scale;
+    const int32_t *cu_q, *cu_k, *block_table, *seq_lens;
+    const int32_t *rows;   /* prefill: (b, h, i) triples; decode: (b, h) pairs */
+    long n_rows;
+    double *out, *lse;
+    long max_keys;
+    /* work distribution */
+    long next;
+    int status;
+} job;
+
+static void run_row(job *jb, long r, double *s)
+{
+    double *out = jb->out + r * (long)jb->d;
+    double *lse = jb->lse + r;
+    const int group = jb->Hq / jb->Hkv;
+    key_store ks;
+    memset(&ks, 0, sizeof ks);
+    ks.k = jb->k;
+    ks.v = jb->v;
+    ks.hkv = jb->Hkv;
+    ks.d = jb->d;
+
+    if (!jb->paged) {
+        int b = jb->rows[3 * r], h = jb->rows[3 * r + 1], i = jb->rows[3 * r + 2];
+        long q_first, nq, nk;
+        if (jb->cu_q) {
+            q_first = jb->cu_q[b];
+            nq = jb->cu_q[b + 1] - jb->cu_q[b];
+            ks.first_token = jb->cu_k[b];
+            nk = jb->cu_k[b + 1] - jb->cu_k[b];
+        } else {
+            q_first = (long)b * jb->Nq;
+            nq = jb->Nq;
+            ks.first_token = (long)b * jb->Nk;
+            nk = jb->Nk;
+        }
+        const uint16_t *q_row = jb->q + ((q_first + i) * jb->Hq + h) * (long)jb->d;
+        attend_row(q_row, &ks, h / group, i, nq, nk, jb->causal, jb->scale, s, out, lse);
+    } else {
+        int b = jb->rows[2 * r], h = jb->rows[2 * r + 1];
+        long len = jb->seq_lens[b];
+        ks.pages = jb->block_table + (long)b * jb->max_pages;
+        ks.page_size = jb->page_size;
+        const uint16_t *q_row = jb->q + ((long)b * jb->Hq + h) * (long)jb->d;
+        /* one query per sequence: it is the last position, so under the
+         * bottom-right rule it sees every cached key (i = 0, nq = 1). */
+        attend_row(q_row, &ks, h / group, 0, 1, len, 0, jb->scale, s, out, lse);
+    }
+}
+
+static void *worker(void *arg)
+{
+    job *jb = (job *)arg;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->max_keys > 0 ? jb->max_keys : 1));
+    if (!s) {
+        __atomic_store_n(&jb->status, -2, __ATOMIC_SEQ_CST);
+        return NULL;
+    }
+    for (;;) {
+        long r = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (r >= jb->n_rows)
+            break;
+        run_row(jb, r, s);
+    }
+    free(s);
+    return NULL;
+}
+
+static int run_job(job *jb, int n_threads)
+{
+    if (n_threads <= 0)
+        n_threads = 1;
+    if (n_threads > 1024)
+        n_threads = 1024;
+    if ((long)n_threads > jb->n_rows)
+        n_threads = jb->n_rows > 0 ? (int)jb->n_rows : 1;
+    jb->next = 0;
+    jb->status = 0;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    if (!th)
+        return -2;
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t) {
+        if (pthread_create(&th[t], NULL, worker, jb) != 0)
+            break;
+        ++started;
+    }
+    if (started == 0)
+        worker(jb);
+    for (int t = 0; t < started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    return jb->status;
+}
+
+/* ---- exported API ---- */
+
+/* Number of CPUs this process may run on. */
+int oracle_num_threads(void)
+{
+    cpu_set_t set;
+    CPU_ZERO(&set);
+    if (sched_getaffinity(0, sizeof set, &set) == 0) {
+        int n = CPU_COUNT(&set);
+        if (n > 0)
+            return n;
+    }
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/*
+ * Prefill rows.  q [T_q, Hq, d], k/v [T_k, Hkv, d] bf16 bits, token-major.
+ * Dense when cu_q == cu_k == NULL (sequence b = tokens [b*Nq, (b+1)*Nq) and
+ * [b*Nk, (b+1)*Nk)); packed otherwise.  rows: n_rows triples (b, h, i) with i
+ * local to sequence b.  out [n_rows, d] and lse [n_rows] in fp64.
+ * Returns 0, or -1 for invalid arguments, -2 when out of memory.
+ */
+int oracle_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        double scale, int causal,
+                        const int32_t *cu_q, const int32_t *cu_k,
+                        const int32_t *rows, long n_rows,
+                        double *out, double *lse, int n_threads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || n_rows < 0)
+        return -1;
+    if ((cu_q == NULL) != (cu_k == NULL))
+        return -1;
+    long max_keys = Nk;
+    for (long r = 0; r < n_rows; ++r) {
+        int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0)
+            return -1;
+        long nq = cu_q ? cu_q[b + 1] - cu_q[b] : Nq;
+        long nk = cu_k ? cu_k[b + 1] - cu_k[b] : Nk;
+        if (i >= nq || nk < 0)
+            return -1;
+        if (nk > max_keys)
+            max_keys = nk;
+    }
+    job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k; jb.v = v;
+    jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.Nq = Nq; jb.Nk = Nk; jb.d = d;
+    jb.causal = causal; jb.scale = scale;
+    jb.cu_q = cu_q; jb.cu_k = cu_k;
+    jb.rows = rows; jb.n_rows = n_rows;
+    jb.out = out; jb.lse = lse;
+    jb.max_keys = max_keys;
+    return run_job(&jb, n_threads);
+}
+
+/*
+ * Paged decode rows: one query per sequence, q [B, Hq, d]; caches
+ * [num_pages, page_size, Hkv, d]; block_table [B, max_pages]; seq_lens [B].
+ * rows: n_rows pairs (b, h).  out [n_rows, d], lse [n_rows] in fp64.
+ */
+int oracle_decode_rows(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                       const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                       int B, int Hq, int Hkv, int d, int page_size, double scale,
+                       const int32_t *rows, long n_rows,
+                       double *out, double *lse, int n_threads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || page_size <= 0 || n_rows < 0)
+        return -1;
+    long max_keys = 1;
+    for (long r = 0; r < n_rows; ++r) {
+        int b = rows[2 * r], h = rows[2 * r + 1];
+        if (b < 0 || b >= B || h < 0 || h >= Hq)
+            return -1;
+        long len = seq_lens[b];
+        if (len < 0 || len > (long)max_pages * page_size)
+            return -1;
+        if (len > max_keys)
+            max_keys = len;
+    }
+    job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k_cache; jb.v = v_cache;
+    jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.d = d;
+    jb.paged = 1; jb.page_size = page_size; jb.max_pages = max_pages;
+    jb.scale = scale;
+    jb.block_table = block_table; jb.seq_lens = seq_lens;
+    jb.rows = rows; jb.n_rows = n_rows;
+    jb.out = out; jb.lse = lse;
+    jb.max_keys = max_keys;
+    return run_job(&jb, n_threads);
+}

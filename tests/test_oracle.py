@@ -1,0 +1,375 @@
+"""Pins for the fp64 oracle: checked against what the pages print and what the
+mathematics fixes, never against itself.
+
+Each pin is chosen so that a plausible mistake in the oracle fails it: a wrong
+mask corner (keep matrices), a wrong head map (GQA lists), a missing max shift
+(shift by +-1000), a wrong normaliser or lse (printed l values), a wrong
+sequence offset (varlen vs per-sequence), a wrong page gather (paged vs
+gathered-dense), a transposed operand or dropped term (SDPA comparison).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bf16(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+def one_row_problem(scores, values):
+    """q = [1, 0], k_j = [s_j, 0] so that q.k_j = s_j exactly (scale 1)."""
+    n = len(scores)
+    dv = len(values[0])
+    d = max(2, dv)
+    q = torch.zeros(1, 1, d)
+    q[0, 0, 0] = 1.0
+    k = torch.zeros(n, 1, d)
+    k[:, 0, 0] = torch.tensor(scores)
+    v = torch.zeros(n, 1, d)
+    v[:, 0, :dv] = torch.tensor(values)
+    return bf16(q), bf16(k), bf16(v), d
+
+
+def run_one_row(scores, values, causal=False):
+    q, k, v, d = one_row_problem(scores, values)
+    out, lse = oracle.prefill_rows(q, k, v, B=1, Hq=1, Hkv=1, Nq=1, Nk=len(scores), scale=1.0,
+                                   causal=causal, rows=[[0, 0, 0]])
+    return out[0, : len(values[0])], lse[0]
+
+
+# ---------------------------------------------------------------------------
+# printed worked examples
+# ---------------------------------------------------------------------------
+def test_two_tile_example_printed_output():
+    g = golden("two_tile_example.json")
+    out, lse = run_one_row(g["scores"], g["values"])
+    tol = 0.5 * 10 ** -g["printed_output_decimals"]
+    assert np.abs(out - np.array(g["printed_output"])).max() <= tol
+
+
+def test_two_tile_example_tile_one_state():
+    g = golden("two_tile_example.json")
+    t1 = g["tile_one"]
+    keys = t1["keys"]
+    out, lse = run_one_row([g["scores"][j] for j in keys], [g["values"][j] for j in keys])
+    tol = 0.5 * 10 ** -t1["decimals"]
+    l1 = math.exp(lse - t1["m"])            # normaliser relative to the tile max
+    assert abs(l1 - t1["l"]) <= tol
+    u1 = out * l1                           # unnormalised numerator
+    assert np.abs(u1 - np.array(t1["u"])).max() <= tol
+
+
+def test_two_tile_example_merge_of_tiles_equals_full():
+    """Merging the two tiles' (O, lse) states reproduces the full row; the
+    old state's weight relative to the new max is the printed 0.3679."""
+    g = golden("two_tile_example.json")
+    o1, l1 = run_one_row(g["scores"][:2], g["values"][:2])
+    o2, l2 = run_one_row(g["scores"][2:], g["values"][2:])
+    of, lf = run_one_row(g["scores"], g["values"])
+    lse = np.logaddexp(l1, l2)
+    merged = math.exp(l1 - lse) * o1 + math.exp(l2 - lse) * o2
+    assert np.abs(merged - of).max() < 1e-12
+    assert abs(lse - lf) < 1e-12
+    # tile-one normaliser carried to the new max 3: e^(2-3) * 1.3679
+    carried = math.exp(l1 - 3.0)
+    assert abs(carried - g["rescale_factor_tile_two"] * g["tile_one"]["l"]) < 1e-4
+
+
+def test_normaliser_example_lse():
+    g = golden("normaliser_example.json")
+    out, lse = run_one_row(g["scores"], [[1.0]] * 4)
+    tol = 0.5 * 10 ** -g["decimals"]
+    assert abs(math.exp(lse - g["final_max"]) - g["l_final"]) <= tol
+    _, lse1 = run_one_row(g["blocks"][0], [[1.0]] * 2)
+    assert abs(math.exp(lse1 - max(g["blocks"][0])) - g["l_block_one"]) <= tol
+    assert abs(math.exp(lse1 - g["final_max"]) - g["l_block_one_rescaled"]) <= tol
+    _, lse2 = run_one_row(g["blocks"][1], [[1.0]] * 2)
+    assert abs(math.exp(lse2 - g["final_max"]) - g["block_two_contribution"]) <= tol
+
+
+def test_shift_invariance_large_offsets():
+    """Adding the same constant to every score leaves O unchanged and moves
+    lse by that constant (+-1000 would overflow exp without the max shift)."""
+    g = golden("two_tile_example.json")
+    base_out, base_lse = run_one_row(g["scores"], g["values"])
+    for shift in (-1000.0, 1000.0):
+        n = len(g["scores"])
+        q = torch.zeros(1, 1, 3)
+        q[0, 0, 0] = 1.0
+        q[0, 0, 2] = shift
+        k = torch.zeros(n, 1, 3)
+        k[:, 0, 0] = torch.tensor(g["scores"])
+        k[:, 0, 2] = 1.0
+        v = torch.zeros(n, 1, 3)
+        v[:, 0, :2] = torch.tensor(g["values"])
+        out, lse = oracle.prefill_rows(bf16(q), bf16(k), bf16(v), B=1, Hq=1, Hkv=1, Nq=1, Nk=n,
+                                       scale=1.0, causal=False, rows=[[0, 0, 0]])
+        assert np.isfinite(out).all()
+        assert np.abs(out[0, :2] - base_out).max() < 1e-12
+        assert abs(lse[0] - (base_lse + shift)) < 1e-9
+
+
+def test_empty_rows_and_single_key_rows():
+    """Nq > Nk under the bottom-right corner: early rows have no key (zero
+    output, lse -inf); the first non-empty row sees key 0 only and returns v_0."""
+    q = bf16(torch.randn(5, 1, 4))
+    k = bf16(torch.randn(2, 1, 4))
+    v = bf16(torch.randn(2, 1, 4))
+    rows = [[0, 0, i] for i in range(5)]
+    out, lse = oracle.prefill_rows(q, k, v, B=1, Hq=1, Hkv=1, Nq=5, Nk=2, scale=0.5,
+                                   causal=True, rows=rows)
+    assert (out[:3] == 0).all()
+    assert np.isneginf(lse[:3]).all()
+    assert np.array_equal(out[3], v[0, 0].double().numpy())
+    assert lse[3] == pytest.approx(0.5 * float((q[3, 0].double() * k[0, 0].double()).sum()), abs=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# mask corner and head map, read off the oracle's outputs
+# ---------------------------------------------------------------------------
+def keep_matrix(nq, nk, causal):
+    """Q = 0, V = identity on keys: O[i, c] > 0 exactly when key c is allowed."""
+    d = max(nk, 2)
+    q = torch.zeros(nq, 1, d)
+    k = torch.zeros(nk, 1, d)
+    v = torch.zeros(nk, 1, d)
+    for j in range(nk):
+        v[j, 0, j] = 1.0
+    out, lse = oracle.prefill_rows(bf16(q), bf16(k), bf16(v), B=1, Hq=1, Hkv=1, Nq=nq, Nk=nk,
+                                   scale=1.0, causal=causal, rows=[[0, 0, i] for i in range(nq)])
+    keep = (out[:, :nk] > 0).astype(int)
+    # each allowed key carries weight 1/|A_i| exactly; lse = ln|A_i|
+    for i in range(nq):
+        cnt = keep[i].sum()
+        if cnt:
+            assert np.allclose(out[i, :nk][keep[i] == 1], 1.0 / cnt, atol=1e-15)
+            assert lse[i] == pytest.approx(math.log(cnt), abs=1e-12)
+        else:
+            assert np.isneginf(lse[i])
+    return keep.tolist()
+
+
+def test_bottom_right_keep_matrices():
+    g = golden("causal_keep.json")
+    for case in g["bottom_right"]:
+        assert keep_matrix(case["q"], case["k"], causal=True) == case["keep"]
+    # the oracle does not use the top-left corner
+    for case in g["top_left"]:
+        assert keep_matrix(case["q"], case["k"], causal=True) != case["keep"]
+    assert keep_matrix(2, 5, causal=False) == [[1] * 5] * 2
+
+
+def test_gqa_head_map():
+    g = golden("gqa_map.json")
+    for case in g["cases"]:
+        hq, hkv = case["q_heads"], case["kv_heads"]
+        nk, d = 3, 2
+        q = torch.zeros(1, hq, d)
+        k = torch.zeros(nk, hkv, d)
+        v = torch.zeros(nk, hkv, d)
+        for gh in range(hkv):
+            v[:, gh, :] = float(gh + 1)
+        out, _ = oracle.prefill_rows(bf16(q), bf16(k), bf16(v), B=1, Hq=hq, Hkv=hkv, Nq=1, Nk=nk,
+                                     scale=1.0, causal=False, rows=[[0, h, 0] for h in range(hq)])
+        got = [int(round(x)) - 1 for x in out[:, 0]]
+        assert got == case["map"]
+    for hq, hkv in g["rejected"]:
+        with pytest.raises(ValueError):
+            oracle.prefill_rows(bf16(torch.zeros(1, max(hq, 1), 2)), bf16(torch.zeros(1, hkv, 2)),
+                                bf16(torch.zeros(1, hkv, 2)), B=1, Hq=hq, Hkv=hkv, Nq=1, Nk=1,
+                                scale=1.0, causal=False, rows=[[0, 0, 0]])
+
+
+# ---------------------------------------------------------------------------
+# against a library routine: torch SDPA, fp64 MATH backend, explicit mask
+# ---------------------------------------------------------------------------
+def sdpa_reference(q, k, v, nq, nk, hq, hkv, scale, causal):
+    """q [nq, hq, d], k/v [nk, hkv, d] -> (out [hq, nq, d], lse [hq, nq]) in fp64."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    import torch.nn.functional as F
+    qd = q.double().permute(1, 0, 2)[None]
+    kd = k.double().permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)[None]
+    vd = v.double().permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)[None]
+    keep = torch.ones(nq, nk, dtype=torch.bool)
+    if causal:
+        keep = torch.arange(nk)[None, :] <= torch.arange(nq)[:, None] + nk - nq
+    with sdpa_kernel(SDPBackend.MATH):
+        out = F.scaled_dot_product_attention(qd, kd, vd, attn_mask=keep, is_causal=False,
+                                             dropout_p=0.0, scale=scale)[0]
+    scores = (qd @ kd.transpose(-2, -1))[0] * scale
+    lse = torch.logsumexp(scores.masked_fill(~keep, -math.inf), dim=-1)
+    return out, lse, keep
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,causal", [
+    (2, 5, 2, 2, 3, True), (5, 2, 2, 2, 3, True), (4, 4, 2, 2, 3, True),
+    (7, 13, 6, 2, 8, True), (13, 7, 4, 1, 8, True), (9, 9, 4, 4, 16, False),
+    (33, 70, 8, 2, 32, True),
+])
+def test_matches_sdpa_fp64(nq, nk, hq, hkv, d, causal):
+    torch.manual_seed(nq * 100 + nk)
+    q, k, v = bf16(torch.randn(nq, hq, d)), bf16(torch.randn(nk, hkv, d)), bf16(torch.randn(nk, hkv, d))
+    scale = 1.0 / math.sqrt(d)
+    rows = [[0, h, i] for h in range(hq) for i in range(nq)]
+    out, lse = oracle.prefill_rows(q, k, v, B=1, Hq=hq, Hkv=hkv, Nq=nq, Nk=nk, scale=scale,
+                                   causal=causal, rows=rows)
+    ref, ref_lse, keep = sdpa_reference(q, k, v, nq, nk, hq, hkv, scale, causal)
+    has_key = keep.any(dim=-1)
+    for r, (_, h, i) in enumerate(rows):
+        if has_key[i]:
+            assert np.abs(out[r] - ref[h, i].numpy()).max() <= 1e-12
+            assert abs(lse[r] - float(ref_lse[h, i])) <= 1e-12
+        else:
+            assert (out[r] == 0).all() and np.isneginf(lse[r])
+
+
+# ---------------------------------------------------------------------------
+# invariants and independent algorithms
+# ---------------------------------------------------------------------------
+def tiled_online_softmax(q, k, v, scale, block):
+    """Independent fp64 tiled forward with the running (m, l, acc) state and
+    the exp(m_old - m_new) rescale, written from the recurrence the pages
+    describe (no masks; one query block)."""
+    m = np.full(q.shape[0], -np.inf)
+    l = np.zeros(q.shape[0])
+    acc = np.zeros((q.shape[0], v.shape[1]))
+    for s0 in range(0, k.shape[0], block):
+        s = (q @ k[s0:s0 + block].T) * scale
+        m_new = np.maximum(m, s.max(axis=1))
+        alpha = np.exp(m - m_new)
+        p = np.exp(s - m_new[:, None])
+        l = alpha * l + p.sum(axis=1)
+        acc = alpha[:, None] * acc + p @ v[s0:s0 + block]
+        m = m_new
+    return acc / l[:, None], m + np.log(l)
+
+
+def test_matches_independent_tiled_recurrence_256x64():
+    g = golden("paged_gather.json")
+    n, d = g["tiled_problem_shape"]
+    torch.manual_seed(0)
+    q, k, v = bf16(torch.randn(n, 1, d)), bf16(torch.randn(n, 1, d)), bf16(torch.randn(n, 1, d))
+    scale = 1.0 / math.sqrt(d)
+    out, lse = oracle.prefill_rows(q, k, v, B=1, Hq=1, Hkv=1, Nq=n, Nk=n, scale=scale, causal=False,
+                                   rows=[[0, 0, i] for i in range(n)])
+    for block in (64, 100, 256):
+        t_out, t_lse = tiled_online_softmax(q[:, 0].double().numpy(), k[:, 0].double().numpy(),
+                                            v[:, 0].double().numpy(), scale, block)
+        # the page reports ~6e-16 between its tiled and dense fp64 versions
+        assert np.abs(out - t_out).max() < 100 * g["tiled_vs_reference_max_abs_diff_fp64"]
+        assert np.abs(lse - t_lse).max() < 1e-12
+
+
+def test_lse_merge_of_disjoint_key_sets():
+    """Split a row's keys into two disjoint sets: logaddexp of the two lse and
+    the exp(lse_s - lse)-weighted outputs equal the full row (the split-KV
+    combine identity)."""
+    torch.manual_seed(3)
+    nq, nk, d = 6, 50, 16
+    q, k, v = bf16(torch.randn(nq, 2, d)), bf16(torch.randn(nk, 1, d)), bf16(torch.randn(nk, 1, d))
+    rows = [[0, h, i] for h in range(2) for i in range(nq)]
+    kw = dict(B=1, Hq=2, Hkv=1, Nq=nq, scale=0.3, causal=False, rows=rows)
+    full_o, full_l = oracle.prefill_rows(q, k, v, Nk=nk, **kw)
+    for s in (1, 17, 49):
+        o1, l1 = oracle.prefill_rows(q, k[:s], v[:s], Nk=s, **kw)
+        o2, l2 = oracle.prefill_rows(q, k[s:], v[s:], Nk=nk - s, **kw)
+        lse = np.logaddexp(l1, l2)
+        merged = np.exp(l1 - lse)[:, None] * o1 + np.exp(l2 - lse)[:, None] * o2
+        assert np.abs(merged - full_o).max() < 1e-12
+        assert np.abs(lse - full_l).max() < 1e-12
+
+
+def test_rows_sum_to_one():
+    """With V = 1 every nonempty row returns exactly 1 (probabilities sum to 1)."""
+    p = workloads.make_varlen([3, 40, 0, 17], [9, 40, 5, 3], 4, 2, 16, causal=True, seed=5)
+    v1 = torch.ones_like(p.v)
+    rows = oracle.all_rows(p)
+    out, lse = oracle.prefill_rows(p.q, p.k, v1, B=p.B, Hq=p.Hq, Hkv=p.Hkv, Nq=p.Nq, Nk=p.Nk,
+                                   scale=p.scale, causal=True, rows=rows, cu_q=p.cu_q, cu_k=p.cu_k)
+    nonempty = np.isfinite(lse)
+    assert nonempty.sum() > 0 and (~nonempty).sum() > 0   # sequence 4 has Nq > Nk
+    assert np.abs(out[nonempty] - 1.0).max() < 1e-12
+    assert (out[~nonempty] == 0).all()
+
+
+def test_varlen_offsets_equal_per_sequence_dense():
+    """A packed problem gives, row for row, the dense result of each sequence
+    alone: a wrong cu_seqlens offset would read another sequence's tokens."""
+    ql, kl = [5, 1, 33, 0, 12], [5, 9, 20, 4, 40]
+    p = workloads.make_varlen(ql, kl, 4, 2, 8, causal=True, seed=11)
+    rows = oracle.all_rows(p)
+    out, lse = oracle.prefill(p, rows)
+    cq = p.cu_q.tolist()
+    ck = p.cu_k.tolist()
+    r = 0
+    for b in range(p.B):
+        nq, nk = ql[b], kl[b]
+        if nq == 0:
+            continue
+        rr = [[0, h, i] for h in range(p.Hq) for i in range(nq)]
+        o, l = oracle.prefill_rows(p.q[cq[b]:cq[b + 1]], p.k[ck[b]:ck[b + 1]], p.v[ck[b]:ck[b + 1]],
+                                   B=1, Hq=p.Hq, Hkv=p.Hkv, Nq=nq, Nk=nk, scale=p.scale,
+                                   causal=True, rows=rr)
+        assert np.array_equal(out[r:r + len(rr)], o)
+        assert np.array_equal(lse[r:r + len(rr)], l)
+        r += len(rr)
+    assert r == len(rows)
+
+
+# ---------------------------------------------------------------------------
+# paged decode
+# ---------------------------------------------------------------------------
+def paged_gather(pool, table, length):
+    """Concatenate the listed physical pages and keep the first `length`
+    tokens (the toy block-table gather the paged-attention page runs)."""
+    return torch.cat([pool[int(b)] for b in table], dim=0)[:length]
+
+
+def test_paged_gather_example_shape():
+    g = golden("paged_gather.json")
+    pool = torch.randn(*g["pool_shape"])
+    assert list(paged_gather(pool, g["table"], g["length"]).shape) == g["gathered_shape"]
+
+
+def test_decode_equals_dense_on_gathered_keys():
+    p = workloads.make_decode([40, 17, 1, 0, 33], 4, 2, 16, num_pages=14, seed=7,
+                              nan_fill_unused=True, max_pages=4)
+    out, lse = oracle.decode(p)
+    assert np.isfinite(out).all()
+    r = 0
+    for b in range(p.B):
+        L = int(p.seq_lens[b])
+        n_pages = -(-L // p.page_size)
+        table = p.block_table[b, :n_pages].tolist()
+        for h in range(p.Hq):
+            if L == 0:
+                assert (out[r] == 0).all() and np.isneginf(lse[r])
+            else:
+                kk = paged_gather(p.k_cache, table, L)  # [L, Hkv, d]
+                vv = paged_gather(p.v_cache, table, L)
+                o, l = oracle.prefill_rows(p.q[b:b + 1], kk, vv, B=1, Hq=p.Hq, Hkv=p.Hkv, Nq=1, Nk=L,
+                                           scale=p.scale, causal=True, rows=[[0, h, 0]])
+                assert np.array_equal(out[r], o[0])
+                assert lse[r] == l[0]
+            r += 1
+
+
+def test_thread_count_does_not_change_results():
+    p = workloads.make_prefill(2, 4, 2, 37, 70, 16, causal=True, seed=9)
+    a = oracle.prefill(p, threads=1)
+    b = oracle.prefill(p, threads=7)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])

@@ -1,0 +1,46 @@
+"""The oracle's pins must fail when a plausible mistake is planted in it.
+
+Each case copies the oracle package to a temporary directory, applies one
+textual mistake to oracle.c, and runs tests/test_oracle.py against the
+mutated copy in a child process: the run has to fail.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "top-left corner": ("j > i + nk - nq", "j > i"),
+    "no max shift in the weights": ("double w = exp(s[j] - m);", "double w = exp(s[j]);"),
+    "alternating head map": ("h / group, i, nq", "h % jb->Hkv, i, nq"),
+    "lse off by a little": ("*lse = m + log(l);", "*lse = m + log(l) + 1e-9;"),
+    "varlen key offset": ("return ks->first_token + j;", "return ks->first_token + j + (ks->first_token > 0);"),
+    "page slot off by one": ("return page * ks->page_size + j % ks->page_size;",
+                             "return page * ks->page_size + (j + 1) % ks->page_size;"),
+    "normaliser perturbed": ("out[c] /= l;", "out[c] /= (l + 1e-13);"),
+    "scale dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "empty row lse zero": ("*lse = -INFINITY;\n        return;", "*lse = 0.0;\n        return;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTATIONS[name]
+    dst = tmp_path / "oracle"
+    shutil.copytree(os.path.join(ROOT, "oracle"), dst,
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
+    src = (dst / "oracle.c").read_text()
+    assert old in src, f"mutation anchor not found: {old!r}"
+    (dst / "oracle.c").write_text(src.replace(old, new, 1))
+    env = dict(os.environ)
+    env["PYTHONPATH"] = os.pathsep.join([str(tmp_path), ROOT])
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch: {name}\n{r.stdout[-2000:]}"
+    # make sure the mutated copy (not the tree's oracle) was the one under test
+    assert (dst / "liboracle.so").exists()
