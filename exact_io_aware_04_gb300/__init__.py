@@ -1,0 +1,30 @@
+"""libattn: exact scaled dot-product attention on one GB300 (sm_103a).
+
+This package is a thin binding over the C ABI declared in include/attn.h: it
+marshals torch tensors (device memory, streams) into pointers and sizes and
+calls the shared library; every step of the computation runs in the library's
+CUDA kernels.  There is no CPU path: without the built library, or without a
+CUDA device, the calls raise.
+
+    out, lse = attn_fwd(q, k, v, causal=True)                       # dense THD/BSHD
+    out, lse = attn_fwd(q, k, v, causal=True, cu_seqlens_q=cq, cu_seqlens_k=ck)
+    out, lse = attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens)
+"""
+from ._binding import (  # noqa: F401
+    ATTN_ERR_BAD_INDEX,
+    ATTN_ERR_CUDA,
+    ATTN_ERR_INVALID_ARG,
+    ATTN_ERR_TIMEOUT,
+    ATTN_ERR_UNSUPPORTED,
+    ATTN_OK,
+    AttnError,
+    attn_decode_paged,
+    attn_decode_workspace_size,
+    attn_fwd,
+    attn_get_device_status,
+    attn_set_validation,
+    attn_status_string,
+    build,
+    lib,
+    lib_path,
+)

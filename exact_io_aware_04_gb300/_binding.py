@@ -1,0 +1,211 @@
+"""ctypes binding of libattn (include/attn.h): argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_CUDA = -3
+ATTN_ERR_TIMEOUT = -4
+ATTN_ERR_BAD_INDEX = -5
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class AttnError(RuntimeError):
+    """A libattn call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile libattn.so in-tree (nvcc, sm_103a)."""
+    return _build.build(force=force)
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"libattn is not built ({path} missing); call "
+                                   "exact_io_aware_04_gb300.build() first")
+            L = ctypes.CDLL(path)
+            P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P]
+            L.attn_fwd.restype = I
+            L.attn_decode_paged.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
+            L.attn_decode_paged.restype = I
+            L.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            L.attn_decode_workspace_size.restype = Z
+            L.attn_get_device_status.argtypes = [P]
+            L.attn_get_device_status.restype = I
+            L.attn_set_validation.argtypes = [I]
+            L.attn_set_validation.restype = I
+            L.attn_status_string.argtypes = [I]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_last_error_message.argtypes = []
+            L.attn_last_error_message.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return lib().attn_status_string(status).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _check(status: int):
+    if status != ATTN_OK:
+        raise AttnError(status, lib().attn_last_error_message().decode())
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libattn has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
+             scale: Optional[float] = None,
+             cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+    """Prefill forward.  Returns (out, lse).
+
+    Dense: q [B, Nq, Hq, d] and k/v [B, Nk, Hkv, d] (or the flattened
+    [B*N, H, d] with B given by a 4-D tensor only).  Packed: q [T_q, Hq, d],
+    k/v [T_k, Hkv, d] with int32 cu_seqlens_q/k of B+1 entries.
+    lse is [B, Hq, Nq] (dense) or [Hq, T_q] (packed), fp32."""
+    _need(q, "q", torch.bfloat16)
+    _need(k, "k", torch.bfloat16)
+    _need(v, "v", torch.bfloat16)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    d = int(q.shape[-1])
+    Hq, Hkv = int(q.shape[-2]), int(k.shape[-2])
+    if cu_seqlens_q is not None or cu_seqlens_k is not None:
+        if cu_seqlens_q is None or cu_seqlens_k is None:
+            raise ValueError("give both cu_seqlens or neither")
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("packed mode takes q [T_q, Hq, d] and k/v [T_k, Hkv, d]")
+        B = int(cu_seqlens_q.numel()) - 1
+        if int(cu_seqlens_k.numel()) != B + 1:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B+1 entries")
+        Nq, Nk = int(q.shape[0]), int(k.shape[0])
+        lse_shape = (Hq, Nq)
+    else:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense mode takes q [B, Nq, Hq, d] and k/v [B, Nk, Hkv, d]")
+        B, Nq, Nk = int(q.shape[0]), int(q.shape[1]), int(k.shape[1])
+        if int(k.shape[0]) != B:
+            raise ValueError("q and k must have the same batch size")
+        lse_shape = (B, Hq, Nq)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    if out.shape != q.shape or tuple(lse.shape) != tuple(lse_shape):
+        raise ValueError("out/lse have the wrong shape")
+    _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                          float(scale), 1 if causal else 0, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                          _stream_handle(stream)))
+    return out, lse
+
+
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, d: int, page_size: int,
+                               max_pages_per_seq: int, num_splits: int = 0) -> int:
+    return int(lib().attn_decode_workspace_size(B, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits))
+
+
+def attn_decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_table: torch.Tensor, seq_lens: torch.Tensor, *,
+                      scale: Optional[float] = None, num_splits: int = 0,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """Paged split-KV decode.  q [B, Hq, d]; caches [num_pages, page, Hkv, d];
+    block_table int32 [B, max_pages]; seq_lens int32 [B].  Returns (out, lse)
+    with out [B, Hq, d] bf16 and lse [B, Hq] fp32.  The workspace (device
+    scratch for the per-chunk partials) is allocated here when not given."""
+    _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache", torch.bfloat16)
+    _need(v_cache, "v_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4 or q.dim() != 3:
+        raise ValueError("q [B, Hq, d]; caches [num_pages, page, Hkv, d]")
+    B, Hq, d = (int(x) for x in q.shape)
+    num_pages, page, Hkv = int(k_cache.shape[0]), int(k_cache.shape[1]), int(k_cache.shape[2])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != B or int(seq_lens.numel()) != B:
+        raise ValueError("block_table [B, max_pages] and seq_lens [B] required")
+    max_pages = int(block_table.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_bytes = attn_decode_workspace_size(B, Hq, Hkv, d, page, max_pages, num_splits)
+    if ws_bytes == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "no decode plan for these sizes")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(lib().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), max_pages,
+                                   _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, d, page, num_pages,
+                                   float(scale), int(num_splits), _ptr(workspace),
+                                   int(workspace.numel() * workspace.element_size()),
+                                   _stream_handle(stream)))
+    return out, lse
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    return int(lib().attn_get_device_status(_stream_handle(stream)))
+
+
+def attn_set_validation(enabled: bool) -> bool:
+    return bool(lib().attn_set_validation(1 if enabled else 0))

@@ -1,0 +1,246 @@
+// api.cu -- the C ABI of libattn: argument checks, per-device state, tensor
+// map encoding, and dispatch to the kernels in fwd.cu and decode.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace attn {
+
+// One error word per device (each device that loads the library gets its own
+// copy of this variable).
+__device__ int g_device_error = 0;
+
+namespace {
+
+thread_local char t_message[512] = "";
+std::atomic<int> g_validation{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+bool g_dev_ready[kMaxDevices] = {};
+DeviceInfo g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status fail(attn_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_message, sizeof(t_message), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+}  // namespace
+
+void set_error_message(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_message, sizeof(t_message), fmt, ap);
+    va_end(ap);
+}
+
+bool validation_enabled() { return g_validation.load(std::memory_order_relaxed) != 0; }
+
+attn_status current_device_info(DeviceInfo* info) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d;
+        d.device = dev;
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "multiProcessorCount: %s", cudaGetErrorString(e));
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d; libattn is built for sm_103a only", dev, major,
+                        minor);
+        void* addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_device_error);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        d.err_word = static_cast<int*>(addr);
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    *info = g_dev[dev];
+    return ATTN_OK;
+}
+
+attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    if (!g_encode) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t gdim[5];
+    cuuint64_t gstride[4];
+    cuuint32_t bdim[5];
+    cuuint32_t estride[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estride[i] = 1;
+        if (i + 1 < rank) gstride[i] = strides_bytes[i];
+    }
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                          gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d, rank %d)", (int)r, rank);
+    return ATTN_OK;
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, void* stream) {
+    if (!q || !k || !v || !out || !lse) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: NULL tensor pointer");
+    if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: give both cu_seqlens or neither");
+    if (B < 0 || Nq < 0 || Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: negative size");
+    if (Hq <= 0 || Hkv <= 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: head counts must be positive");
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
+    if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: scale must be finite and > 0");
+    if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: tensor pointers must be 16-byte aligned");
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd: head_dim %d (built: 64, 128)", d);
+    const bool varlen = cu_seqlens_q != nullptr;
+    if (!varlen && (static_cast<long long>(B) * Nq > INT32_MAX || static_cast<long long>(B) * Nk > INT32_MAX))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd: more than 2^31 tokens");
+    if (B == 0 || Nq == 0) return ATTN_OK;
+    FwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    return launch_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size, int max_pages_per_seq,
+                                  int num_splits) {
+    DecodePlan plan;
+    if (!make_decode_plan(B, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan)) return 0;
+    return plan.total_bytes;
+}
+
+attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                              int max_pages_per_seq, const int* seq_lens, void* out, float* lse, int B, int Hq,
+                              int Hkv, int d, int page_size, int num_pages, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse || !workspace)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: NULL pointer");
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: bad size");
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
+    if (!isfinite(scale) || !(scale > 0.f))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: scale must be finite and > 0");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: misaligned pointer");
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: head_dim %d (built: 64, 128)", d);
+    if (page_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: page_size %d (built: 16)", page_size);
+    if (static_cast<long long>(max_pages_per_seq) * page_size > INT32_MAX)
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: sequences longer than 2^31 tokens");
+    DecodePlan plan;
+    if (!make_decode_plan(B, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: no plan for Hq/Hkv = %d", Hq / Hkv);
+    if (workspace_bytes < plan.total_bytes)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: workspace %zu bytes < %zu needed", workspace_bytes,
+                    plan.total_bytes);
+    if (B == 0) return ATTN_OK;
+    DecodeArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.max_pages = max_pages_per_seq;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    a.scale = scale;
+    a.num_splits = num_splits;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    return launch_decode(a, plan, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_get_device_status(void* stream) {
+    DeviceInfo dev;
+    attn_status st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    int word = 0;
+    e = cudaMemcpy(&word, dev.err_word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpy(dev.err_word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "clearing the device error word: %s", cudaGetErrorString(e));
+    }
+    return static_cast<attn_status>(word);
+}
+
+int attn_set_validation(int enabled) { return g_validation.exchange(enabled ? 1 : 0); }
+
+const char* attn_status_string(attn_status status) {
+    switch (status) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+        case ATTN_ERR_BAD_INDEX: return "ATTN_ERR_BAD_INDEX";
+    }
+    return "ATTN_UNKNOWN_STATUS";
+}
+
+const char* attn_last_error_message(void) { return t_message; }
+
+}  // extern "C"

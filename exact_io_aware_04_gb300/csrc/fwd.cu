@@ -1,0 +1,766 @@
+// fwd.cu -- prefill forward of exact attention on sm_103a.
+//
+// One persistent CTA per SM walks a longest-first list of work items.  An item
+// is (sequence b, query head h, pair of 128-row query tiles).  Inside a CTA
+// the warps specialise:
+//   warps 0-3  softmax group 0: owns query tile 0 (one thread per row)
+//   warps 4-7  softmax group 1: owns query tile 1
+//   warp  8    producer: TMA loads of Q tiles and a ring of K and V tiles
+//   warp  9    MMA issuer (one thread) and tensor-memory owner
+//   warps 10-11 idle (they complete the third warpgroup)
+// The softmax warpgroups raise their register budget to kSoftmaxRegs and the
+// third warpgroup lowers its own to kControlRegs (setmaxnreg).
+// Tensor memory (512 columns x 128 lanes x 32 bit):
+//   [0,128)       S0 = Q0 K^T (fp32); P0 (bf16) overwrites its first 64 columns
+//   [128,256)     S1, P1
+//   [256,256+d)   O0 accumulator (fp32)
+//   [256+d,256+2d) O1
+// Per K/V tile j the tensor core runs S = Q K_j^T for both query tiles, the
+// softmax groups turn S into P in place, and the tensor core runs O += P V_j
+// with P read straight from tensor memory.  The issue order
+//     PV0(j), S0(j+1), PV1(j), S1(j+1)
+// lets softmax group 0 work while the tensor core serves tile 1 and the other
+// way round.  Nothing quadratic ever leaves the SM.
+//
+// The recurrence is the blockwise merge of "Flash Attention: A Complete
+// Architectural Autopsy", part 2 ("The Online Softmax Recurrence"): running
+// max m, normaliser l, accumulator O, the old state scaled by exp(m_old-m_new)
+// when the max rises, and one division by l at the end ("FlashAttention: Part
+// 1", section 3.1).  The rescale is conditional ("FlashAttention-3 and
+// PagedAttention", FA4 paragraph): the reference max of a row is only moved
+// when the tile max exceeds it by more than 2^8 in the exponent, which keeps O
+// and l on one common reference (exact in real arithmetic) while skipping
+// almost every rescale.  Causal tiles wholly above the bottom-right boundary
+// are never loaded; only tiles that cross it or a sequence edge are masked
+// ("FlashAttention: Part 1", section 3.5).
+#include <cuda_bf16.h>
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;                     // query rows per tile
+constexpr int kBN = 128;                     // keys per K/V tile
+constexpr int kPairRows = 2 * kBM;           // query rows per work item
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
+constexpr int kSoftmaxRegs = 208;    // warpgroups 0 and 1
+constexpr int kControlRegs = 88;     // warpgroup 2
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr int kMaxSortedPairs = 1024;        // packed mode: (seq, pair) entries sorted per CTA
+constexpr int kChunks = kThreads;            // packed mode: sequences scanned in this many chunks
+
+template <int HD>
+struct Cfg {
+    static constexpr int kPanels = HD / 64;          // 64-element (128-byte) column panels
+    static constexpr int kPanelBytes = kBM * 128;    // 128 rows x 128 bytes
+    static constexpr int kTileBytes = kPanels * kPanelBytes;
+    static constexpr int kStages = HD == 128 ? 2 : 4;  // K ring depth == V ring depth
+    static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+    static constexpr uint32_t kTmemCols = 512;
+    // tensor-memory column of S_t / P_t and of O_t
+    __device__ static constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+    __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * HD; }
+};
+
+struct FwdParams {
+    CUtensorMap tm_q;   // [T_q rows, Hq*d] bf16, box 64 x 128, 128B swizzle
+    CUtensorMap tm_k;   // [T_k rows, Hkv*d]
+    CUtensorMap tm_v;
+    __nv_bfloat16* out;
+    float* lse;
+    const int* cu_q;
+    const int* cu_k;
+    int B, Hq, Hkv, group;
+    int Nq, Nk;         // dense: per-sequence lengths; packed: total rows
+    int causal, varlen;
+    float scale_log2;   // scale * log2(e)
+    int* err;
+};
+
+struct Seq {
+    int q_base, k_base, nq, nk;
+};
+
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+__device__ __forceinline__ Seq seq_of(const FwdParams& p, int b) {
+    Seq s;
+    if (p.varlen) {
+        const int q0 = clampi(__ldg(p.cu_q + b), 0, p.Nq);
+        const int q1 = clampi(__ldg(p.cu_q + b + 1), q0, p.Nq);
+        const int k0 = clampi(__ldg(p.cu_k + b), 0, p.Nk);
+        const int k1 = clampi(__ldg(p.cu_k + b + 1), k0, p.Nk);
+        s.q_base = q0;
+        s.nq = q1 - q0;
+        s.k_base = k0;
+        s.nk = k1 - k0;
+    } else {
+        s.q_base = b * p.Nq;
+        s.nq = p.Nq;
+        s.k_base = b * p.Nk;
+        s.nk = p.Nk;
+    }
+    return s;
+}
+
+// Number of K/V tiles a query tile starting at local row q_start needs.
+__device__ __forceinline__ int kv_tiles(int q_start, int nq, int nk, int causal) {
+    const int rows = min(nq - q_start, kBM);
+    if (rows <= 0 || nk <= 0) return 0;
+    const int all = (nk + kBN - 1) / kBN;
+    if (!causal) return all;
+    const int last_key = q_start + rows - 1 + (nk - nq);  // last row's last allowed key
+    if (last_key < 0) return 0;
+    return min(last_key / kBN + 1, all);
+}
+
+struct Item {
+    int b, pair, h;
+    Seq s;
+    int n[2];       // K/V tiles per query tile
+    int rows[2];    // valid query rows per tile
+};
+
+__device__ __forceinline__ void fill_item(const FwdParams& p, Item& it) {
+    it.s = seq_of(p, it.b);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int q_start = it.pair * kPairRows + t * kBM;
+        it.rows[t] = clampi(it.s.nq - q_start, 0, kBM);
+        it.n[t] = kv_tiles(q_start, it.s.nq, it.s.nk, p.causal);
+    }
+}
+
+// Work list shared by all roles of a CTA (packed mode only).
+struct Schedule {
+    int n_pairs;                    // total (sequence, pair) entries
+    int sorted;                     // 1 if the lists below are valid
+    int chunk_prefix[kChunks + 1];  // pairs before each chunk of sequences
+    int sb[kMaxSortedPairs];        // sorted: sequence of entry
+    int sp[kMaxSortedPairs];        // sorted: pair of entry
+    int tmp_b[kMaxSortedPairs];
+    int tmp_p[kMaxSortedPairs];
+    int tmp_c[kMaxSortedPairs];
+};
+
+// Longest-first order of (sequence, pair) entries, built by every CTA from
+// cu_seqlens (no host round trip, no global scratch).
+__device__ void build_schedule(const FwdParams& p, Schedule& sc) {
+    const int tid = threadIdx.x;
+    const int per = (p.B + kChunks - 1) / kChunks;
+    const int b0 = min(tid * per, p.B), b1 = min(b0 + per, p.B);
+    int cnt = 0;
+    for (int b = b0; b < b1; ++b) cnt += (seq_of(p, b).nq + kPairRows - 1) / kPairRows;
+    sc.chunk_prefix[tid + 1] = cnt;
+    __syncthreads();
+    if (tid == 0) {
+        sc.chunk_prefix[0] = 0;
+        for (int c = 0; c < kChunks; ++c) sc.chunk_prefix[c + 1] += sc.chunk_prefix[c];
+        sc.n_pairs = sc.chunk_prefix[kChunks];
+        sc.sorted = sc.n_pairs <= kMaxSortedPairs;
+    }
+    __syncthreads();
+    if (!sc.sorted) return;
+    int pos = sc.chunk_prefix[tid];
+    for (int b = b0; b < b1; ++b) {
+        const Seq s = seq_of(p, b);
+        const int np = (s.nq + kPairRows - 1) / kPairRows;
+        for (int pr = 0; pr < np; ++pr, ++pos) {
+            sc.tmp_b[pos] = b;
+            sc.tmp_p[pos] = pr;
+            const int c0 = kv_tiles(pr * kPairRows, s.nq, s.nk, p.causal);
+            const int c1 = kv_tiles(pr * kPairRows + kBM, s.nq, s.nk, p.causal);
+            sc.tmp_c[pos] = max(c0, c1);
+        }
+    }
+    __syncthreads();
+    const int n = sc.n_pairs;
+    for (int i = tid; i < n; i += kThreads) {
+        const int ci = sc.tmp_c[i];
+        int rank = 0;
+        for (int j = 0; j < n; ++j) {
+            const int cj = sc.tmp_c[j];
+            rank += (cj > ci) || (cj == ci && j < i);
+        }
+        sc.sb[rank] = sc.tmp_b[i];
+        sc.sp[rank] = sc.tmp_p[i];
+    }
+    __syncthreads();
+}
+
+// Item k of the CTA-independent longest-first order.
+__device__ __forceinline__ void item_at(const FwdParams& p, const Schedule& sc, int k, Item& it) {
+    if (!p.varlen) {
+        const int per = p.B * p.Hq;
+        const int pairs = (p.Nq + kPairRows - 1) / kPairRows;
+        const int pi = k / per;
+        it.pair = p.causal ? pairs - 1 - pi : pi;
+        const int rem = k - pi * per;
+        it.b = rem / p.Hq;
+        it.h = rem - it.b * p.Hq;
+    } else {
+        const int e = k / p.Hq;
+        it.h = k - e * p.Hq;
+        if (sc.sorted) {
+            it.b = sc.sb[e];
+            it.pair = sc.sp[e];
+        } else {
+            // natural order: find the chunk, then the sequence inside it
+            int lo = 0, hi = kChunks;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sc.chunk_prefix[mid] <= e) lo = mid; else hi = mid;
+            }
+            const int per = (p.B + kChunks - 1) / kChunks;
+            int rem = e - sc.chunk_prefix[lo];
+            int b = lo * per;
+            for (;; ++b) {
+                const int np = (seq_of(p, b).nq + kPairRows - 1) / kPairRows;
+                if (rem < np) break;
+                rem -= np;
+            }
+            it.b = b;
+            it.pair = rem;
+        }
+    }
+    fill_item(p, it);
+}
+
+__device__ __forceinline__ int total_items(const FwdParams& p, const Schedule& sc) {
+    if (!p.varlen) return ((p.Nq + kPairRows - 1) / kPairRows) * p.B * p.Hq;
+    return sc.n_pairs * p.Hq;
+}
+
+// Snake order over the grid: round r visits items r*G + c (r even) or
+// r*G + G-1-c (r odd), so the heaviest items are spread across CTAs.
+__device__ __forceinline__ int snake(int round, int cta, int grid) {
+    return round * grid + ((round & 1) ? grid - 1 - cta : cta);
+}
+
+// Shared-memory barrier indices (each barrier is 8 bytes at bar0 + 8*index).
+template <int S>
+struct BarIdx {
+    static constexpr int q_full = 0, q_empty = 1;
+    static constexpr int k_full = 2, k_empty = 2 + S, v_full = 2 + 2 * S, v_empty = 2 + 3 * S;
+    static constexpr int s_full = 2 + 4 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
+    static constexpr int mma_done = o_empty + 2;
+    static constexpr int count = mma_done + 1;
+};
+
+__device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); }
+
+// ---------------------------------------------------------------- producer warp (one thread)
+template <int HD>
+__device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
+                                           int n_items) {
+    using C = Cfg<HD>;
+    using BI = BarIdx<C::kStages>;
+    constexpr int S = C::kStages;
+    const uint32_t sm_k0 = smem0 + 2 * C::kTileBytes;
+    const uint32_t sm_v0 = sm_k0 + S * C::kTileBytes;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t kc = 0, vc = 0, qc = 0;
+    bool ok = true;
+    Item it;
+    for (int r = 0; ok && r * grid < n_items; ++r) {
+        const int k = snake(r, cta, grid);
+        if (k >= n_items) continue;
+        item_at(p, sc, k, it);
+        const int n = max(it.n[0], it.n[1]);
+        if (n == 0) continue;
+        const int g = it.h / p.group;
+        if (qc > 0) ok = mbar_wait(bar_at(bar0, BI::q_empty), (qc - 1) & 1, p.err);
+        if (!ok) break;
+        const uint32_t qbytes = (it.n[0] > 0 ? C::kTileBytes : 0) + (it.n[1] > 0 ? C::kTileBytes : 0);
+        mbar_arrive_expect_tx(bar_at(bar0, BI::q_full), qbytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (it.n[t] == 0) continue;
+            const int y = it.s.q_base + it.pair * kPairRows + t * kBM;
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_2d(smem0 + t * C::kTileBytes + pn * C::kPanelBytes, &p.tm_q, bar_at(bar0, BI::q_full),
+                            it.h * HD + pn * 64, y);
+        }
+        ++qc;
+        for (int j = 0; j < n && ok; ++j) {
+            const int y = it.s.k_base + j * kBN;
+            {
+                const uint32_t st = kc % S;
+                if (kc >= S) ok = mbar_wait(bar_at(bar0, BI::k_empty + st), ((kc / S) - 1) & 1, p.err);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_at(bar0, BI::k_full + st), C::kTileBytes);
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_2d(sm_k0 + st * C::kTileBytes + pn * C::kPanelBytes, &p.tm_k,
+                                bar_at(bar0, BI::k_full + st), g * HD + pn * 64, y);
+                ++kc;
+            }
+            {
+                const uint32_t st = vc % S;
+                if (vc >= S) ok = mbar_wait(bar_at(bar0, BI::v_empty + st), ((vc / S) - 1) & 1, p.err);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_at(bar0, BI::v_full + st), C::kTileBytes);
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_2d(sm_v0 + st * C::kTileBytes + pn * C::kPanelBytes, &p.tm_v,
+                                bar_at(bar0, BI::v_full + st), g * HD + pn * 64, y);
+                ++vc;
+            }
+        }
+    }
+    // Drain: every load issued must have landed before the CTA exits.
+    for (uint32_t i = (kc > S ? kc - S : 0); i < kc; ++i)
+        mbar_wait(bar_at(bar0, BI::k_full + i % S), (i / S) & 1, p.err);
+    for (uint32_t i = (vc > S ? vc - S : 0); i < vc; ++i)
+        mbar_wait(bar_at(bar0, BI::v_full + i % S), (i / S) & 1, p.err);
+    if (qc > 0) mbar_wait(bar_at(bar0, BI::q_full), (qc - 1) & 1, p.err);
+}
+
+// ---------------------------------------------------------------- MMA warp (one thread)
+template <int HD>
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_tile, uint32_t k_tile) {
+    using C = Cfg<HD>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
+        mma_smem_smem(tmem_d, smem_desc_sw128(q_tile + off, 16, 1024), smem_desc_sw128(k_tile + off, 16, 1024), idesc,
+                      kk > 0);
+    }
+}
+
+template <int HD>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_tile, bool first) {
+    using C = Cfg<HD>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, HD, true);
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_tmem_smem(tmem_o, tmem_p + kk * 8, smem_desc_sw128(v_tile + kk * 2048, C::kPanelBytes, 1024), idesc,
+                      (!first || kk > 0) ? 1u : 0u);
+}
+
+template <int HD>
+__device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
+                                      uint32_t tmem, int n_items) {
+    using C = Cfg<HD>;
+    using BI = BarIdx<C::kStages>;
+    constexpr int S = C::kStages;
+    const uint32_t sm_k0 = smem0 + 2 * C::kTileBytes;
+    const uint32_t sm_v0 = sm_k0 + S * C::kTileBytes;
+    const uint32_t q0 = smem0, q1 = smem0 + C::kTileBytes;
+    const uint32_t ts0 = tmem + C::col_s(0), ts1 = tmem + C::col_s(1);
+    const uint32_t to0 = tmem + C::col_o(0), to1 = tmem + C::col_o(1);
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0, oc0 = 0, oc1 = 0;
+    bool ok = true;
+    Item it;
+    for (int r = 0; ok && r * grid < n_items; ++r) {
+        const int k = snake(r, cta, grid);
+        if (k >= n_items) continue;
+        item_at(p, sc, k, it);
+        const int n0 = it.n[0], n1 = it.n[1];
+        const int n = max(n0, n1);
+        if (n == 0) continue;
+        ok = mbar_wait(bar_at(bar0, BI::q_full), qc & 1, p.err);
+        ++qc;
+        if (!ok) break;
+        // K_0 -> S0(0), S1(0)
+        ok = mbar_wait(bar_at(bar0, BI::k_full + kc % S), (kc / S) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after_sync();
+        {
+            const uint32_t kt = sm_k0 + (kc % S) * C::kTileBytes;
+            if (n0 > 0) {
+                issue_s<HD>(ts0, q0, kt);
+                tc_commit(bar_at(bar0, BI::s_full + 0));
+            }
+            if (n1 > 0) {
+                issue_s<HD>(ts1, q1, kt);
+                tc_commit(bar_at(bar0, BI::s_full + 1));
+            }
+        }
+        tc_commit(bar_at(bar0, BI::k_empty + kc % S));
+        ++kc;
+        if (n == 1) tc_commit(bar_at(bar0, BI::q_empty));
+        for (int j = 0; j < n && ok; ++j) {
+            const uint32_t vst = vc % S;
+            const uint32_t vt = sm_v0 + vst * C::kTileBytes;
+            ok = mbar_wait(bar_at(bar0, BI::v_full + vst), (vc / S) & 1, p.err);
+            if (!ok) break;
+            const bool next = j + 1 < n;
+            // ---- tile 0: PV0(j), then S0(j+1)
+            if (j < n0) {
+                ok = mbar_wait(bar_at(bar0, BI::p_ready + 0), pc0 & 1, p.err);
+                ++pc0;
+                if (ok && j == 0 && oc0 > 0) ok = mbar_wait(bar_at(bar0, BI::o_empty + 0), (oc0 - 1) & 1, p.err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                issue_pv<HD>(to0, ts0, vt, j == 0);
+                if (j == n0 - 1) {
+                    tc_commit(bar_at(bar0, BI::o_final + 0));
+                    ++oc0;
+                }
+            }
+            const uint32_t kst = kc % S;
+            const uint32_t kt = sm_k0 + kst * C::kTileBytes;
+            if (next) {
+                ok = mbar_wait(bar_at(bar0, BI::k_full + kst), (kc / S) & 1, p.err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (j + 1 < n0) {
+                    issue_s<HD>(ts0, q0, kt);
+                    tc_commit(bar_at(bar0, BI::s_full + 0));
+                }
+            }
+            // ---- tile 1: PV1(j), then S1(j+1)
+            if (j < n1) {
+                ok = mbar_wait(bar_at(bar0, BI::p_ready + 1), pc1 & 1, p.err);
+                ++pc1;
+                if (ok && j == 0 && oc1 > 0) ok = mbar_wait(bar_at(bar0, BI::o_empty + 1), (oc1 - 1) & 1, p.err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                issue_pv<HD>(to1, ts1, vt, j == 0);
+                if (j == n1 - 1) {
+                    tc_commit(bar_at(bar0, BI::o_final + 1));
+                    ++oc1;
+                }
+            }
+            tc_commit(bar_at(bar0, BI::v_empty + vst));
+            ++vc;
+            if (next) {
+                if (j + 1 < n1) {
+                    issue_s<HD>(ts1, q1, kt);
+                    tc_commit(bar_at(bar0, BI::s_full + 1));
+                }
+                tc_commit(bar_at(bar0, BI::k_empty + kst));
+                ++kc;
+                if (j + 2 == n) tc_commit(bar_at(bar0, BI::q_empty));
+            }
+        }
+    }
+    // Drain: all issued tensor-core work must finish before TMEM is freed.
+    tc_commit(bar_at(bar0, BI::mma_done));
+    mbar_wait(bar_at(bar0, BI::mma_done), 0, p.err);
+}
+
+// ---------------------------------------------------------------- softmax warpgroups
+template <int HD>
+__device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc, uint32_t bar0, uint32_t tmem,
+                                          int n_items, int t) {
+    using C = Cfg<HD>;
+    using BI = BarIdx<C::kStages>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int wq = warp & 3;                 // lane quarter of tensor memory
+    const int row_in_tile = wq * 32 + lane;  // == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::col_s(t);
+    const uint32_t t_o = tmem + lane_off + C::col_o(t);
+    const uint32_t b_s_full = bar_at(bar0, BI::s_full + t), b_p_ready = bar_at(bar0, BI::p_ready + t);
+    const uint32_t b_o_final = bar_at(bar0, BI::o_final + t), b_o_empty = bar_at(bar0, BI::o_empty + t);
+    const float sl2 = p.scale_log2;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t scnt = 0, ocnt = 0;
+    bool ok = true;
+    Item it;
+    for (int r = 0; ok && r * grid < n_items; ++r) {
+        const int k = snake(r, cta, grid);
+        if (k >= n_items) continue;
+        item_at(p, sc, k, it);
+        const int rows_t = t == 0 ? it.rows[0] : it.rows[1];
+        if (rows_t == 0) continue;
+        const int nt = t == 0 ? it.n[0] : it.n[1];
+        const int q_tile0 = it.pair * kPairRows + t * kBM;
+        const int q_local = q_tile0 + row_in_tile;
+        const bool row_valid = row_in_tile < rows_t;
+        const int off = it.s.nk - it.s.nq;
+        // last allowed key of this row, and of the tile's first row (inclusive)
+        const int kmax_row = p.causal ? min(q_local + off, it.s.nk - 1) : it.s.nk - 1;
+        const int kmax_first = p.causal ? min(q_tile0 + off, it.s.nk - 1) : it.s.nk - 1;
+        float m_ref = -INFINITY;
+        float l = 0.f;
+        for (int j = 0; j < nt; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, scnt & 1, p.err));
+            ++scnt;
+            if (!ok) break;
+            tc_fence_after_sync();
+            float x[128];
+            tmem_ld_32cols_f(t_s + 0, x);
+            tmem_ld_32cols_f(t_s + 32, x + 32);
+            tmem_ld_32cols_f(t_s + 64, x + 64);
+            tmem_ld_32cols_f(t_s + 96, x + 96);
+            tmem_ld_wait_f(x);
+            tmem_ld_wait_f(x + 32);
+            tmem_ld_wait_f(x + 64);
+            tmem_ld_wait_f(x + 96);
+            const int k0 = j * kBN;
+            if (k0 + kBN - 1 > kmax_first) {
+                const int lim = kmax_row - k0;  // columns > lim are masked
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > lim) x[c] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            const float mx2 = mx * sl2;
+            if (j == 0) {
+                m_ref = mx2;
+            } else {
+                const bool need = mx2 > m_ref + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = fmaxf(m_ref, mx2);
+                    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_ref - m_new);
+                    l *= alpha;
+                    m_ref = m_new;
+#pragma unroll 1
+                    for (int cc = 0; cc < HD; cc += 32) {
+                        float o[32];
+                        tmem_ld_32cols_f(t_o + cc, o);
+                        tmem_ld_wait_f(o);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                        tmem_st_32cols(t_o + cc, reinterpret_cast<const uint32_t(&)[32]>(o));
+                    }
+                }
+            }
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float lsum = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const float a = fast_exp2(fmaf(x[h * 64 + c], sl2, -m_use));
+                    const float b = fast_exp2(fmaf(x[h * 64 + c + 1], sl2, -m_use));
+                    lsum += a + b;
+                    pk[c >> 1] = pack_bf16x2(a, b);
+                }
+                tmem_st_32cols(t_s + h * 32, pk);
+            }
+            l += lsum;
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p_ready);
+        }
+        if (!ok) break;
+        // ---- epilogue: O / l -> bf16, lse
+        const size_t out_row = static_cast<size_t>(it.s.q_base + q_local) * p.Hq + it.h;
+        __nv_bfloat16* dst = p.out + out_row * HD;
+        if (nt > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(b_o_final, ocnt & 1, p.err));
+            ++ocnt;
+            if (!ok) break;
+            tc_fence_after_sync();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int cc = 0; cc < HD; cc += 32) {
+                float o[32];
+                tmem_ld_32cols_f(t_o + cc, o);
+                tmem_ld_wait_f(o);
+                if (row_valid) {
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(o[c + 0] * inv_l, o[c + 1] * inv_l);
+                        w.y = pack_bf16x2(o[c + 2] * inv_l, o[c + 3] * inv_l);
+                        w.z = pack_bf16x2(o[c + 4] * inv_l, o[c + 5] * inv_l);
+                        w.w = pack_bf16x2(o[c + 6] * inv_l, o[c + 7] * inv_l);
+                        d4[c >> 3] = w;
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_o_empty);
+        } else if (row_valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            for (int c = 0; c < HD / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
+        }
+        if (row_valid) {
+            float lse_v = -INFINITY;
+            if (l > 0.f) {
+                float lg;
+                asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l));
+                lse_v = (m_ref + lg) * 0.69314718055994531f;
+            }
+            const size_t li = p.varlen ? static_cast<size_t>(it.h) * p.Nq + it.s.q_base + q_local
+                                       : (static_cast<size_t>(it.b) * p.Hq + it.h) * p.Nq + q_local;
+            p.lse[li] = lse_v;
+        }
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using C = Cfg<HD>;
+    using BI = BarIdx<C::kStages>;
+    extern __shared__ __align__(1024) uint8_t smem_dyn[];
+    __shared__ __align__(8) uint64_t bars[BI::count];
+    __shared__ uint32_t tmem_base_slot;
+    __shared__ Schedule sched;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t smem0 = (smem_addr(smem_dyn) + 1023u) & ~1023u;
+    const uint32_t bar0 = smem_addr(bars);
+
+    if (p.varlen) build_schedule(p, sched);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < BI::count; ++i) {
+            uint32_t cnt = 1;
+            if ((i >= BI::p_ready && i < BI::p_ready + 2) || (i >= BI::o_empty && i < BI::o_empty + 2)) cnt = 4;
+            mbar_init(bar_at(bar0, i), cnt);
+        }
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(&tmem_base_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_base_slot;
+    const int n_items = total_items(p, sched);
+
+    if (warp >= 8) {
+        regs_decrease<kControlRegs>();
+        if (warp == kProducerWarp && lane == 0) role_producer<HD>(p, sched, smem0, bar0, n_items);
+        if (warp == kMmaWarp && lane == 0) role_mma<HD>(p, sched, smem0, bar0, tmem, n_items);
+        __syncwarp();
+    } else {
+        regs_increase<kSoftmaxRegs>();
+        role_softmax<HD>(p, sched, bar0, tmem, n_items, warp >> 2);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// Optional check of cu_seqlens: start 0, nondecreasing, end == total.
+__global__ void check_cu_seqlens_kernel(const int* cu, int B, int total, int* err) {
+    for (int i = threadIdx.x; i <= B; i += blockDim.x) {
+        const int v = cu[i];
+        bool bad = (i == 0 && v != 0) || (i == B && v != total) || v < 0 || v > total;
+        if (i > 0 && v < cu[i - 1]) bad = true;
+        if (bad) record_error(err, ATTN_ERR_BAD_INDEX);
+    }
+}
+
+template <int HD>
+attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+    using C = Cfg<HD>;
+    FwdParams p;
+    memset(&p, 0, sizeof(p));
+    const bool varlen = a.cu_q != nullptr;
+    const uint64_t t_q = varlen ? static_cast<uint64_t>(a.Nq) : static_cast<uint64_t>(a.B) * a.Nq;
+    // With no keys at all the K/V maps are never used; a zero extent is not
+    // encodable, so they get one row.
+    uint64_t t_k = varlen ? static_cast<uint64_t>(a.Nk) : static_cast<uint64_t>(a.B) * a.Nk;
+    if (t_k == 0) t_k = 1;
+    const uint32_t box[2] = {64, kBM};
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hq) * HD, t_q};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hq) * HD * 2};
+        attn_status st = encode_tma_bf16(&p.tm_q, a.q, 2, dims, strides, box, true);
+        if (st != ATTN_OK) return st;
+    }
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, t_k};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
+        attn_status st = encode_tma_bf16(&p.tm_k, a.k, 2, dims, strides, box, true);
+        if (st != ATTN_OK) return st;
+        st = encode_tma_bf16(&p.tm_v, a.v, 2, dims, strides, box, true);
+        if (st != ATTN_OK) return st;
+    }
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.lse = a.lse;
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = a.Hq / a.Hkv;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.causal = a.causal ? 1 : 0;
+    p.varlen = varlen ? 1 : 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.err = dev.err_word;
+
+    long long items;
+    if (varlen)  // upper bound on (sequence, pair) entries times heads
+        items = (static_cast<long long>(a.Nq) / kPairRows + a.B) * a.Hq;
+    else
+        items = static_cast<long long>((a.Nq + kPairRows - 1) / kPairRows) * a.B * a.Hq;
+    if (items <= 0) return ATTN_OK;
+    const int grid = static_cast<int>(items < dev.sm_count ? items : dev.sm_count);
+
+    if (varlen && validation_enabled()) {
+        check_cu_seqlens_kernel<<<1, 256, 0, stream>>>(a.cu_q, a.B, a.Nq, dev.err_word);
+        check_cu_seqlens_kernel<<<1, 256, 0, stream>>>(a.cu_k, a.B, a.Nk, dev.err_word);
+    }
+    static bool attr_set[2] = {false, false};  // per instantiation, all devices
+    if (!attr_set[HD == 128]) {
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) {
+            set_error_message("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<HD>);
+        if (e != cudaSuccess) {
+            set_error_message("cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+        // setmaxnreg.inc can only draw on what the launch allocated
+        if (fa.numRegs * kThreads < 2 * 128 * kSoftmaxRegs + 128 * kControlRegs) {
+            set_error_message("attn_fwd kernel built with %d registers/thread; the warpgroup split needs %d",
+                              fa.numRegs, kLaunchRegs);
+            return ATTN_ERR_UNSUPPORTED;
+        }
+        attr_set[HD == 128] = true;
+    }
+    attn_fwd_kernel<HD><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error_message("attn_fwd launch: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+    DeviceInfo dev;
+    attn_status st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    if (a.d == 128) return launch_typed<128>(a, dev, stream);
+    if (a.d == 64) return launch_typed<64>(a, dev, stream);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace attn

@@ -1,0 +1,72 @@
+// internal.h -- host-side plumbing shared by the libattn translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "status.h"
+
+namespace attn {
+
+// Per-device facts the launchers need; cached after the first query.
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int* err_word;  // device address of this device's error word
+};
+
+// Fills `info` for the current device.  ATTN_ERR_CUDA on failure.
+attn_status current_device_info(DeviceInfo* info);
+
+// Records a printf-style detail message for attn_last_error_message().
+void set_error_message(const char* fmt, ...);
+
+// Encodes a tiled TMA descriptor for a bf16 tensor.  dims[0] is the
+// contiguous dimension; strides_bytes[i] is the byte stride of dims[i+1].
+attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+
+bool validation_enabled();
+
+// ---- launchers (one per translation unit) ----
+struct FwdArgs {
+    const void *q, *k, *v;
+    void* out;
+    float* lse;
+    int B, Hq, Hkv, Nq, Nk, d;
+    float scale;
+    int causal;
+    const int *cu_q, *cu_k;
+};
+attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+    const void* q;
+    const void *k_cache, *v_cache;
+    const int* block_table;
+    int max_pages;
+    const int* seq_lens;
+    void* out;
+    float* lse;
+    int B, Hq, Hkv, d, page_size, num_pages;
+    float scale;
+    int num_splits;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+// How attn_decode_paged cuts sequences into chunks.
+struct DecodePlan {
+    int pages_per_chunk;  // chunk length in pages
+    int max_chunks;       // chunks of the longest possible sequence
+    int heads_per_cta;    // K/V heads gathered by one CTA
+    int head_groups;      // Hkv / heads_per_cta
+    size_t partial_o_bytes, partial_lse_bytes, total_bytes;
+};
+bool make_decode_plan(int B, int Hq, int Hkv, int d, int page_size, int max_pages, int num_splits,
+                      DecodePlan* plan);
+attn_status launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+}  // namespace attn

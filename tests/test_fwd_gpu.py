@@ -1,0 +1,149 @@
+"""GPU parity of attn_fwd against the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import assert_close, gather_prefill, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    import exact_io_aware_04_gb300 as m
+    m.build()
+    torch.cuda.set_device(0)
+    yield m
+    assert m.attn_get_device_status() == 0
+
+
+def check_all_rows(la, p):
+    out, lse = run_prefill(la, p)
+    torch.cuda.synchronize()
+    rows = oracle.all_rows(p)
+    ref_o, ref_lse = oracle.prefill(p, rows)
+    go, gl = gather_prefill(p, out, lse, rows)
+    return assert_close(p.name, go, gl, ref_o, ref_lse)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_workload_all_rows(la, causal):
+    check_all_rows(la, workloads.tiny(causal))
+
+
+# (B, Hq, Hkv, Nq, Nk, d, causal): several tiles, ragged tails, both corners
+SMALL = [
+    (2, 4, 4, 300, 300, 128, True),
+    (2, 4, 4, 300, 300, 128, False),
+    (1, 2, 2, 200, 517, 128, True),     # Nq < Nk: short query block over a long cache
+    (1, 2, 2, 517, 200, 128, True),     # Nq > Nk: leading rows have no key
+    (1, 2, 2, 517, 200, 64, False),
+    (2, 8, 2, 384, 384, 64, True),      # GQA 4:1, exact tile multiple
+    (1, 6, 1, 129, 1000, 128, True),    # MQA, one row past a tile
+    (3, 2, 1, 1, 700, 128, True),       # single query row (decode-like prefill)
+    (1, 2, 2, 1000, 3000, 128, True),
+    (1, 4, 2, 640, 640, 64, False),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: "B{}_Hq{}_Hkv{}_Nq{}_Nk{}_d{}_{}".format(*c[:6], "c" if c[6] else "n"))
+def test_small_problems_all_rows(la, cfg):
+    B, Hq, Hkv, Nq, Nk, d, causal = cfg
+    p = workloads.make_prefill(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=hash(cfg) % 10_000)
+    check_all_rows(la, p)
+
+
+VARLEN = [
+    ([5, 300, 0, 129, 1000, 1], [5, 300, 17, 700, 1000, 1], 128, True),
+    ([256, 3, 600], [100, 3, 2000], 128, True),     # a sequence with Nq > Nk
+    ([77, 512, 512], [1024, 1500, 512], 64, True),
+    ([77, 400, 33], [300, 400, 1000], 128, False),
+]
+
+
+@pytest.mark.parametrize("cfg", VARLEN, ids=lambda c: f"varlen_{len(c[0])}seq_d{c[2]}_{'c' if c[3] else 'n'}")
+def test_varlen_all_rows(la, cfg):
+    ql, kl, d, causal = cfg
+    p = workloads.make_varlen(ql, kl, 4, 2, d, causal=causal, seed=sum(ql) + sum(kl))
+    check_all_rows(la, p)
+
+
+def test_no_keys_gives_zero_rows(la):
+    p = workloads.make_varlen([3, 40], [0, 0], 2, 2, 128, causal=False, seed=3)
+    out, lse = run_prefill(la, p)
+    torch.cuda.synchronize()
+    assert (out == 0).all() and torch.isneginf(lse).all()
+
+
+# ---------------------------------------------------------------- one-hot: which keys are attended
+def one_hot_check(la, p, bases):
+    """Q = 0 and V one-hot over a window of d keys: the nonzero pattern of O
+    must equal the oracle's allowed set exactly, the magnitude must name the
+    K/V head, and exp(lse) must be the allowed-key count."""
+    for base in bases:
+        ph = workloads.one_hot_values(p, base)
+        out, lse = run_prefill(la, ph)
+        torch.cuda.synchronize()
+        rows = oracle.all_rows(ph)
+        ref_o, ref_lse = oracle.prefill(ph, rows)
+        go, gl = gather_prefill(ph, out, lse, rows)
+        assert np.array_equal(go != 0, ref_o != 0), f"base {base}: attended-key pattern differs"
+        cnt = np.where(np.isfinite(ref_lse), np.rint(np.exp(ref_lse)), 0)
+        g_of_h = (rows[:, 1] // (p.Hq // p.Hkv)) + 1
+        nz = go != 0
+        assert np.array_equal(np.rint((go * cnt[:, None])[nz]), np.broadcast_to(g_of_h[:, None], go.shape)[nz]), \
+            f"base {base}: K/V head map differs"
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(gl), fin)
+        assert np.array_equal(np.rint(np.exp(gl[fin])), cnt[fin]), f"base {base}: allowed-key count differs"
+
+
+def test_one_hot_tiny_all_windows(la):
+    for causal in (False, True):
+        p = workloads.tiny(causal)
+        one_hot_check(la, p, range(0, p.Nk, p.d))
+
+
+def test_one_hot_gqa_unequal_lengths(la):
+    p = workloads.make_prefill(2, 8, 2, 200, 517, 128, causal=True, seed=12)
+    one_hot_check(la, p, [0, 128, 256, 389, 517 - 128])
+
+
+def test_one_hot_varlen(la):
+    p = workloads.make_varlen([5, 300, 129, 600], [5, 300, 700, 200], 4, 2, 64, causal=True, seed=13)
+    one_hot_check(la, p, [0, 64, 128, 192, 300, 450, 636])
+
+
+# ---------------------------------------------------------------- mixed shapes in one process
+def test_shape_order_independence(la):
+    """Shape A then B then A again: identical bits for A, both match the
+    oracle (a kernel keyed only on the GQA ratio would mix these up)."""
+    a = workloads.make_prefill(1, 4, 2, 256, 256, 128, causal=True, seed=21)  # Hq 4, Hkv 2
+    b = workloads.make_prefill(1, 2, 1, 256, 256, 128, causal=True, seed=22)  # Hq 2, Hkv 1
+    oa1, la1 = run_prefill(la, a)
+    ob, lb = run_prefill(la, b)
+    oa2, la2 = run_prefill(la, a)
+    torch.cuda.synchronize()
+    assert torch.equal(oa1, oa2) and torch.equal(la1, la2)
+    for p, (o, l) in ((a, (oa1, la1)), (b, (ob, lb))):
+        rows = oracle.all_rows(p)
+        ref_o, ref_lse = oracle.prefill(p, rows)
+        go, gl = gather_prefill(p, o, l, rows)
+        assert_close(p.name, go, gl, ref_o, ref_lse)
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled rows
+@pytest.mark.parametrize("name", ["mha_causal", "gqa_causal", "varlen_chunked"])
+def test_full_size_sampled_rows(la, name):
+    p = getattr(workloads, name)()
+    out, lse = run_prefill(la, p)
+    torch.cuda.synchronize()
+    per = 64 if name == "varlen_chunked" else 512
+    lens = [nq for nq, _ in p.seq_lens()]
+    rows = workloads.sample_rows(None, lens, p.Hq, per, seed=p.seed + 500)
+    ref_o, ref_lse = oracle.prefill(p, rows.numpy())
+    go, gl = gather_prefill(p, out, lse, rows.numpy())
+    stats = assert_close(p.name, go, gl, ref_o, ref_lse)
+    print(p.name, stats)
