@@ -1,0 +1,522 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * attn_fwd on the MHA causal prefill workload (B=4, Hq=Hkv=16, N=4096,
+    d=128, bottom-right causal), and
+  * attn_decode_paged on the paged split-KV decode workload (B=64, Hq=32,
+    Hkv=8, d=128, lengths U[4096, 32768], 16-token pages, 200k-page pool).
+`value` is the prefill throughput in TFLOP/s (exact attended query-key pairs
+x 4 x d, i.e. causal-adjusted); the decode bandwidth in GB/s (algorithmic
+bytes: every K/V row the sequences own, read once, plus q, out, lse and the
+block-table rows) is reported beside it.  Both are timed per call with CUDA
+events on the launching stream; L2 is flushed (a 256 MB write) between steps,
+outside the timed calls.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
+                  [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|tiny|paged_decode]
+
+--impl reference times the fp64 CPU oracle on the host cores (bounded row
+samples of the same workload, same metric and unit).  Under torchrun each rank
+runs an independent replica on its own GPU (the path needs no exchange);
+rank 0 prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+PREFILL_WORKLOADS = ("mha_causal", "gqa_causal", "varlen_chunked", "tiny")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- accounting
+def attended_pairs(p) -> int:
+    """Exact number of (query, key) pairs the mask allows, over all heads."""
+    total = 0
+    for nq, nk in p.seq_lens():
+        if nq <= 0 or nk <= 0:
+            continue
+        if not p.causal:
+            total += nq * nk
+            continue
+        off = nk - nq
+        # row i sees min(nk, max(0, i + off + 1)) keys
+        for_rows = 0
+        i0 = max(0, -off)                    # first row with any key
+        i_full = max(i0, nk - off - 1)       # from here rows see all nk keys
+        i_full = min(i_full, nq)
+        n_part = max(0, i_full - i0)
+        # sum_{i=i0}^{i_full-1} (i + off + 1)
+        for_rows += n_part * (i0 + off + 1) + n_part * (n_part - 1) // 2
+        for_rows += max(0, nq - i_full) * nk
+        total += for_rows
+    return total * p.Hq
+
+
+def prefill_flops(p) -> float:
+    return 4.0 * p.d * attended_pairs(p)
+
+
+def prefill_flops_literal(p) -> float:
+    """4*Nq*Nk*d*H*B, halved for causal (the coarse textbook count)."""
+    tot = sum(4.0 * nq * nk * p.d for nq, nk in p.seq_lens()) * p.Hq
+    return tot / 2 if p.causal else tot
+
+
+def prefill_bytes(p) -> float:
+    tq = sum(nq for nq, _ in p.seq_lens())
+    tk = sum(nk for _, nk in p.seq_lens())
+    return 2.0 * p.d * (2 * tq * p.Hq + 2 * tk * p.Hkv) + 4.0 * tq * p.Hq
+
+
+def decode_bytes(d) -> float:
+    """Algorithmic bytes of one decode call: each sequence's K and V rows once,
+    q and out, lse, and the block-table entries the sequences use."""
+    lens = d.seq_lens.cpu().tolist()
+    kv = sum(lens) * d.Hkv * d.d * 2 * 2
+    pages = sum(-(-L // d.page_size) for L in lens)
+    return float(kv + 2 * d.B * d.Hq * d.d * 2 + 4 * d.B * d.Hq + 4 * pages + 4 * d.B)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return {k: float(j[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max_sum(world, t_max: float, units: float, device=None):
+    """(max over ranks of t_max, sum over ranks of units)."""
+    if world <= 1:
+        return t_max, units
+    import torch.distributed as dist
+    dev = device if device is not None else torch.device("cpu")
+    a = torch.tensor([t_max], dtype=torch.float64, device=dev)
+    b = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(a.item()), float(b.item())
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+def oracle_sample_rate(p, target_s: float, seed: int, max_rows: int = 1 << 20):
+    """Times the oracle on seeded rows of prefill problem p; grows the sample
+    until it takes about target_s.  Returns (flops/s, rows, seconds, threads)."""
+    import numpy as np
+    import oracle
+    threads = oracle.num_threads()
+    lens = [nq for nq, _ in p.seq_lens()]
+    g = torch.Generator().manual_seed(seed)
+    n = 64
+    while True:
+        b = torch.randint(0, p.B, (n,), generator=g)
+        h = torch.randint(0, p.Hq, (n,), generator=g)
+        i = (torch.rand(n, generator=g) * torch.tensor([lens[x] for x in b.tolist()], dtype=torch.float32)).long()
+        rows = torch.stack([b, h, i], 1).numpy().astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill(p, rows, threads=threads)
+        dt = time.perf_counter() - t0
+        fl = 4.0 * p.d * sum(row_keys(p, int(r[0]), int(r[2])) for r in rows)
+        if dt >= target_s * 0.5 or n >= max_rows:
+            return fl / dt, n, dt, threads, fl
+        n = min(max_rows, int(n * max(2.0, target_s / max(dt, 1e-3))))
+
+
+def row_keys(p, b, i):
+    nq, nk = p.seq_lens()[b]
+    if not p.causal:
+        return nk
+    return max(0, min(nk, i + nk - nq + 1))
+
+
+def oracle_decode_rate(d, target_s: float, seed: int):
+    import numpy as np
+    import oracle
+    threads = oracle.num_threads()
+    g = torch.Generator().manual_seed(seed)
+    n = 32
+    lens = d.seq_lens.cpu().tolist()
+    while True:
+        b = torch.randint(0, d.B, (n,), generator=g)
+        h = torch.randint(0, d.Hq, (n,), generator=g)
+        rows = torch.stack([b, h], 1).numpy().astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.decode(d, rows, threads=threads)
+        dt = time.perf_counter() - t0
+        byts = sum(lens[int(r[0])] * d.d * 2 * 2 for r in rows)
+        if dt >= target_s * 0.5 or n >= d.B * d.Hq * 8:
+            return byts / dt, n, dt, threads
+        n = int(n * max(2.0, target_s / max(dt, 1e-3)))
+
+
+# ---------------------------------------------------------------- main
+def make_workloads(name, device):
+    prefill = decode = None
+    if name in ("hot_path",) + PREFILL_WORKLOADS:
+        pname = "mha_causal" if name == "hot_path" else name
+        prefill = getattr(workloads, pname)() if pname != "tiny" else workloads.tiny(True)
+    if name in ("hot_path", "paged_decode"):
+        decode = workloads.paged_decode(device=device)
+    return prefill, decode
+
+
+def run_reference(args, world, rank):
+    """fp64 CPU oracle on bounded samples of the same workload."""
+    if rank != 0:
+        return 0
+    # the headline of the hot-path step is the prefill metric; the CPU arm
+    # times that part (the decode pool would not fit a bounded CPU sample)
+    name = "mha_causal" if args.workload == "hot_path" else args.workload
+    prefill, decode = make_workloads(name, "cpu")
+    per_step = float(os.environ.get("ATTN_REFERENCE_STEP_SECONDS", "4.0"))
+    if prefill is not None:
+        rate_fn = lambda s: oracle_sample_rate(prefill, per_step, seed=s)[0]
+        unit, metric_scale = "TFLOP/s", 1e-12
+    else:
+        rate_fn = lambda s: oracle_decode_rate(decode, per_step, seed=s)[0]
+        unit, metric_scale = "GB/s", 1e-9
+    for w in range(args.warmup):
+        rate_fn(10_000 + w)
+    rates = [rate_fn(20_000 + s) for s in range(args.steps)]
+    value = statistics.median(rates) * metric_scale
+    import oracle
+    cores = oracle.num_threads()
+    sample = (f"each step: seeded rows of the {prefill.name if prefill else decode.name} workload, "
+              f"about {per_step:.0f} s of fp64 oracle work, rate = work/seconds")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": prefill.name if prefill else decode.name},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "fwd TFLOP/s & % bf16 tensor peak; split-KV decode GB/s & % HBM peak"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["libattn", "reference"], default="libattn")
+    ap.add_argument("--workload", default="hot_path",
+                    choices=["hot_path", "paged_decode"] + list(PREFILL_WORKLOADS))
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import exact_io_aware_04_gb300 as la
+    la.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, peaks_kind = load_peaks()
+
+    prefill, decode = make_workloads(args.workload, dev)
+    # ---- device-resident inputs
+    if prefill is not None:
+        pg = prefill.to(dev)
+        if prefill.varlen:
+            fargs = (pg.q, pg.k, pg.v)
+            fkw = dict(causal=pg.causal, scale=pg.scale, cu_seqlens_q=pg.cu_q, cu_seqlens_k=pg.cu_k)
+        else:
+            fargs = (pg.q.view(pg.B, pg.Nq, pg.Hq, pg.d), pg.k.view(pg.B, pg.Nk, pg.Hkv, pg.d),
+                     pg.v.view(pg.B, pg.Nk, pg.Hkv, pg.d))
+            fkw = dict(causal=pg.causal, scale=pg.scale)
+        f_out = torch.empty_like(fargs[0])
+        f_lse = torch.empty((pg.Hq, pg.q.shape[0]) if prefill.varlen else (pg.B, pg.Hq, pg.Nq),
+                            dtype=torch.float32, device=dev)
+        fkw.update(out=f_out, lse=f_lse)
+        p_flops = prefill_flops(prefill)
+    if decode is not None:
+        ws = torch.empty(la.attn_decode_workspace_size(decode.B, decode.Hq, decode.Hkv, decode.d,
+                                                       decode.page_size, decode.max_pages, 0),
+                         dtype=torch.uint8, device=dev)
+        d_out = torch.empty_like(decode.q)
+        d_lse = torch.empty((decode.B, decode.Hq), dtype=torch.float32, device=dev)
+        dargs = (decode.q, decode.k_cache, decode.v_cache, decode.block_table, decode.seq_lens)
+        dkw = dict(scale=decode.scale, out=d_out, lse=d_lse, workspace=ws)
+        d_bytes = decode_bytes(decode)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        flush.fill_(1)
+        if ev is not None:
+            ev[0].record(stream)
+        if prefill is not None:
+            la.attn_fwd(*fargs, **fkw)
+        if ev is not None:
+            ev[1].record(stream)
+        if decode is not None:
+            la.attn_decode_paged(*dargs, **dkw)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if la.attn_get_device_status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            step(events[i])
+        torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    st = la.attn_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {la.attn_status_string(st)} after the timed region")
+    f_ms = [e[0].elapsed_time(e[1]) for e in events]
+    d_ms = [e[1].elapsed_time(e[2]) for e in events]
+    f_tot, d_tot = sum(f_ms), sum(d_ms)
+    step_ms = (f_tot + d_tot) / args.steps
+
+    # whole-job figures (max time over ranks, units summed over ranks)
+    rooflines = {}
+    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) rounded to bf16)"}
+    if prefill is not None:
+        f_max, f_units = reduce_max_sum(world, f_tot, p_flops * args.steps, dev)
+        value = f_units / (f_max * 1e-3) / 1e12
+        ach = p_flops / (f_tot / args.steps * 1e-3) / 1e12
+        rooflines["attn_fwd"] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+                                 "frac_nominal": ach / NOMINAL["bf16_tflops"], "traffic": None,
+                                 "peak_source": f"{peaks_kind} bf16 burst",
+                                 "ms_per_launch_median": statistics.median(f_ms),
+                                 "ms_per_launch_p95": sorted(f_ms)[int(0.95 * (len(f_ms) - 1))],
+                                 "flops_per_launch": p_flops,
+                                 "flops_per_launch_literal_formula": prefill_flops_literal(prefill)}
+        line.update(value=value, unit="TFLOP/s")
+    if decode is not None:
+        d_max, d_units = reduce_max_sum(world, d_tot, d_bytes * args.steps, dev)
+        dval = d_units / (d_max * 1e-3) / 1e9
+        ach = d_bytes / (d_tot / args.steps * 1e-3) / 1e9
+        rooflines["attn_decode_paged"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                          "frac": ach / peaks["hbm_gbs"], "frac_nominal": ach / NOMINAL["hbm_gbs"],
+                                          "traffic": None, "peak_source": f"{peaks_kind} copy bandwidth",
+                                          "ms_per_call_median": statistics.median(d_ms),
+                                          "ms_per_call_p95": sorted(d_ms)[int(0.95 * (len(d_ms) - 1))],
+                                          "bytes_per_call": d_bytes, "launches_per_call": 2}
+        line["decode"] = {"value": dval, "unit": "GB/s", "frac_of_measured_hbm": dval / world / peaks["hbm_gbs"],
+                          "frac_of_8TBs": dval / world / NOMINAL["hbm_gbs"]}
+        if prefill is None:
+            line.update(value=dval, unit="GB/s")
+    dominant = max(rooflines, key=lambda k: (f_tot if k == "attn_fwd" else d_tot))
+    line["roofline"] = dict(rooflines[dominant], kernel=dominant)
+    line["rooflines"] = rooflines
+    line["ms_per_step"] = step_ms
+    line["gpu_launches"] = args.steps * ((1 if prefill is not None else 0) + (2 if decode is not None else 0))
+    cfg = {"workload": ("mha_causal_b4_h16_n4096_d128 + paged_decode_b64_hq32_hkv8_d128"
+                        if args.workload == "hot_path" else (prefill or decode).name),
+           "l2": "flushed between steps (256 MB write, outside the timed calls)",
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if prefill is not None:
+        cfg.update(prefill={"B": prefill.B, "Hq": prefill.Hq, "Hkv": prefill.Hkv, "Nq": prefill.Nq,
+                            "Nk": prefill.Nk, "d": prefill.d, "causal": prefill.causal,
+                            "varlen": prefill.varlen})
+    if decode is not None:
+        cfg.update(decode={"B": decode.B, "Hq": decode.Hq, "Hkv": decode.Hkv, "d": decode.d,
+                           "page_size": decode.page_size, "num_pages": decode.num_pages,
+                           "tokens": int(decode.seq_lens.sum())})
+    line["config"] = cfg
+    line["clocks"] = clocks.summary()
+    line["wall_s_timed_region"] = t_wall
+
+    # ---- end to end through the public API with pinned host buffers
+    line["e2e"] = measure_e2e(la, prefill, decode, fargs if prefill is not None else None,
+                              fkw if prefill is not None else None, dargs if decode is not None else None,
+                              dkw if decode is not None else None, stream, world, dev,
+                              steps=min(args.steps, 20))
+
+    if rank == 0 and world == 1 and args.cpu_baseline_seconds > 0:
+        line["cpu_baseline"] = cpu_baseline(prefill, decode, args.cpu_baseline_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev, steps):
+    """The headline metric through the public API with the step's inputs in
+    pinned host memory: H2D copies, the call, and a D2H read of the result,
+    all inside the timed region."""
+    if prefill is not None:
+        host_in = [t.cpu().pin_memory() for t in fargs]
+        dev_in = [torch.empty_like(t) for t in fargs]
+        host_out = torch.empty(fkw["out"].shape, dtype=fkw["out"].dtype).pin_memory()
+        host_lse = torch.empty(fkw["lse"].shape, dtype=fkw["lse"].dtype).pin_memory()
+        kw = dict(fkw)
+        flops = prefill_flops(prefill)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+        def one():
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            la.attn_fwd(*dev_in, **kw)
+            host_out.copy_(kw["out"], non_blocking=True)
+            host_lse.copy_(kw["lse"], non_blocking=True)
+        units, unit, scale = flops, "TFLOP/s", 1e-12
+    else:
+        host_q = dargs[0].cpu().pin_memory()
+        dev_q = torch.empty_like(dargs[0])
+        host_out = torch.empty(dkw["out"].shape, dtype=dkw["out"].dtype).pin_memory()
+        host_lse = torch.empty(dkw["lse"].shape, dtype=dkw["lse"].dtype).pin_memory()
+        h2d = host_q.numel() * host_q.element_size()
+        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+        def one():
+            dev_q.copy_(host_q, non_blocking=True)
+            la.attn_decode_paged(dev_q, *dargs[1:], **dkw)
+            host_out.copy_(dkw["out"], non_blocking=True)
+            host_lse.copy_(dkw["lse"], non_blocking=True)
+        units, unit, scale = decode_bytes(decode), "GB/s", 1e-9
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    t_max, tot_units = reduce_max_sum(world, ms, units * steps, dev)
+    return {"value": tot_units / (t_max * 1e-3) * scale, "unit": unit, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "note": "prefill inputs copied from pinned host memory each step" if prefill is not None else
+                    "decode query copied each step; the paged cache stays resident"}
+
+
+def cpu_baseline(prefill, decode, seconds):
+    try:
+        if prefill is not None:
+            host = prefill.to("cpu")
+            rate, n, dt, threads, fl = oracle_sample_rate(host, seconds, seed=4242)
+            return {"value": rate * 1e-12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                    "sample": f"{n} seeded query rows of {prefill.name} ({fl / 1e9:.1f} GFLOP fp64) in {dt:.1f} s"}
+        host = decode.to("cpu")
+        rate, n, dt, threads = oracle_decode_rate(host, seconds, seed=4242)
+        return {"value": rate * 1e-9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                "sample": f"{n} seeded (sequence, head) rows of {decode.name} in {dt:.1f} s"}
+    except Exception as e:  # the baseline never blocks the GPU line
+        return {"value": None, "unit": None, "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

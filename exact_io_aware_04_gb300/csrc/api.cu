@@ -122,7 +122,8 @@ extern "C" {
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens_q,
                      const int* cu_seqlens_k, void* stream) {
-    if (!q || !k || !v || !out || !lse) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: NULL tensor pointer");
+    if (!q || !out || !lse) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: NULL tensor pointer");
+    if ((!k || !v) && Nk > 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: NULL k/v with keys present");
     if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr))
         return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: give both cu_seqlens or neither");
     if (B < 0 || Nq < 0 || Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: negative size");
@@ -130,6 +131,10 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
     if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
     if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: scale must be finite and > 0");
     if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+    if (Nk == 0) {  // no keys: K/V are never read (NULL allowed)
+        k = q;
+        v = q;
+    }
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
         return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: tensor pointers must be 16-byte aligned");
     if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd: head_dim %d (built: 64, 128)", d);

@@ -687,6 +687,7 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         if (st != ATTN_OK) return st;
     }
     {
+        // with no keys the maps point at q (one row, never read)
         const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, t_k};
         const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
         attn_status st = encode_tma_bf16(&p.tm_k, a.k, 2, dims, strides, box, true);

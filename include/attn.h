@@ -84,10 +84,11 @@ typedef enum {
  *          T_k = Nk = cu_seqlens_k[B]); per-sequence lengths are read on the
  *          device.  lse [Hq, T_q] fp32 (written).
  *   d (head_dim) in {64, 128}; other values return ATTN_ERR_UNSUPPORTED.
- *   scale: finite; usually 1/sqrt(d).  causal: 0 or 1 (bottom-right corner,
+ *   scale: finite and > 0; usually 1/sqrt(d).  causal: 0 or 1 (bottom-right corner,
  *   per sequence).
  * Returns ATTN_OK once the work is enqueued on `stream`.
- * Rejects (ATTN_ERR_INVALID_ARG): NULL q/k/v/out/lse, exactly one cu_seqlens
+ * k and v may be NULL only when Nk == 0 (no keys: every row is empty).
+ * Rejects (ATTN_ERR_INVALID_ARG): NULL q/out/lse (or k/v with Nk > 0), exactly one cu_seqlens
  * NULL, B < 0, Hq <= 0, Hkv <= 0, Hq % Hkv != 0, Nq < 0, Nk < 0, scale not
  * finite, a pointer not 16-byte aligned.  B == 0 or Nq == 0 enqueues nothing.
  */

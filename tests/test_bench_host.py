@@ -1,0 +1,81 @@
+"""Host-side logic of bench.py on CPU: FLOP/byte accounting, the reduction
+over ranks (gloo, two processes), and the reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("nq,nk,causal", [(7, 7, True), (5, 2, True), (2, 5, True), (9, 4, False),
+                                          (1, 700, True), (517, 200, True), (300, 300, True)])
+def test_attended_pairs_brute_force(nq, nk, causal):
+    p = workloads.make_prefill(1, 3, 1, nq, nk, 8, causal=causal, seed=1)
+    brute = 3 * sum(1 for i in range(nq) for j in range(nk) if (not causal or j <= i + nk - nq))
+    assert bench.attended_pairs(p) == brute
+
+
+def test_mha_causal_flops():
+    p = workloads.make_prefill(4, 16, 16, 4096, 4096, 128, causal=True, seed=1)
+    assert bench.prefill_flops(p) == 4 * 128 * 64 * 4096 * 4097 // 2
+    assert bench.prefill_flops_literal(p) == 4 * 4096 * 4096 * 128 * 64 / 2
+
+
+def test_decode_bytes():
+    d = workloads.make_decode([17, 32], 8, 2, 128, num_pages=8, seed=1)
+    kv = (17 + 32) * 2 * 128 * 2 * 2
+    assert bench.decode_bytes(d) == kv + 2 * 2 * 8 * 128 * 2 + 4 * 2 * 8 + 4 * (2 + 2) + 4 * 2
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t, u = bench.reduce_max_sum(world, 10.0 + rank, 100.0 * (rank + 1))
+    bench.barrier(world)
+    q.put((rank, t, u))
+    dist.destroy_process_group()
+
+
+def test_reduce_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, t, u in got:
+        assert t == 11.0 and u == 300.0
+
+
+def test_reference_arm_json_line():
+    env = dict(os.environ, ATTN_REFERENCE_STEP_SECONDS="0.3")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny", "--steps", "2", "--warmup", "1"], capture_output=True, text=True, env=env,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
