@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     ATTN_OK,
     AttnError,
     attn_decode_paged,
+    attn_decode_paged_noalloc,
     attn_decode_workspace_size,
     attn_fwd,
     attn_get_device_status,

@@ -209,3 +209,41 @@ def attn_get_device_status(stream=None) -> int:
 
 def attn_set_validation(enabled: bool) -> bool:
     return bool(lib().attn_set_validation(1 if enabled else 0))
+
+
+def attn_decode_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_table: torch.Tensor, seq_lens: torch.Tensor, *,
+                              scale: Optional[float] = None, num_splits: int = 0,
+                              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                              stream=None):
+    """attn_decode_paged without a workspace: for callers that cannot
+    allocate device memory at call time, the library keeps the per-chunk
+    partials in its own fixed 32 MiB device array (shared by all calls, so
+    calls must not overlap on the GPU).  Returns (out, lse)."""
+    L = lib()
+    f = L.attn_decode_paged_noalloc
+    if f.argtypes is None:
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        f.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I, P]
+        f.restype = I
+    _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache", torch.bfloat16)
+    _need(v_cache, "v_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4 or q.dim() != 3:
+        raise ValueError("q [B, Hq, d]; caches [num_pages, page, Hkv, d]")
+    B, Hq, d = (int(x) for x in q.shape)
+    num_pages, page, Hkv = int(k_cache.shape[0]), int(k_cache.shape[1]), int(k_cache.shape[2])
+    if block_table.dim() != 2 or int(block_table.shape[0]) != B or int(seq_lens.numel()) != B:
+        raise ValueError("block_table [B, max_pages] and seq_lens [B] required")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    _check(f(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+             _ptr(out), _ptr(lse), B, Hq, Hkv, d, page, num_pages, float(scale), int(num_splits),
+             _stream_handle(stream)))
+    return out, lse

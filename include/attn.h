@@ -160,6 +160,42 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size,
                                   int max_pages_per_seq, int num_splits);
 
 /*
+ * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot
+ * allocate device memory when they call (no counterpart in the pages this
+ * library follows; it exists for integration only).
+ *
+ * Some callers cannot give the library a workspace: a plug-in whose host
+ * runtime owns every device allocation and offers it no allocator, or a
+ * serving loop that reserves its memory once and may not call cudaMalloc or
+ * cudaFree afterwards (those calls can synchronise the whole device).  This
+ * entry point takes the same arguments as attn_decode_paged minus the
+ * workspace and keeps the per-chunk partial results in a fixed 32 MiB array
+ * compiled into the library; every GPU that loads the library holds that
+ * array until the process exits.  It allocates nothing.
+ *
+ *  - Limit: the scratch that attn_decode_workspace_size reports for the same
+ *    sizes must be at most 32 MiB (33554432 bytes); larger sizes return
+ *    ATTN_ERR_INVALID_ARG with a message.  A larger num_splits page range
+ *    (fewer chunks) shrinks the requirement.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) and remembers it; make that first call before any
+ *    stream capture begins.
+ *  - All calls share the one array and it keeps the last call's contents
+ *    (nothing in it needs to start at zero).  Calls that overlap on the GPU
+ *    -- on different streams, or from different threads -- race on it: order
+ *    them on one stream or with events.
+ * Everything else (layouts, errors, the result) is as for attn_decode_paged.
+ */
+attn_status attn_decode_paged_noalloc(const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const int *block_table, int max_pages_per_seq,
+                                      const int *seq_lens,
+                                      void *out, float *lse,
+                                      int B, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                      float scale, int num_splits,
+                                      void *stream);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the
  * device error word of the current device: ATTN_OK, ATTN_ERR_TIMEOUT or
  * ATTN_ERR_BAD_INDEX (the first error recorded since the last read), or
