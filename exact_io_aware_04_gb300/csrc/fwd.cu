@@ -348,7 +348,6 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
         mma_tmem_smem(tmem_o, tmem_p + kk * 8, smem_desc_sw128(v_tile + kk * 2048, C::kPanelBytes, 1024), idesc,
                       (!first || kk > 0) ? 1u : 0u);
 }
-
 template <int HD>
 __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                       uint32_t tmem, int n_items) {
@@ -510,9 +509,16 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                 for (int c = 0; c < 128; ++c)
                     if (c > lim) x[c] = -INFINITY;
             }
-            float mx = x[0];
+            // row max: 3-input max over 8 independent chains
+            float mc[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+            for (int c = 0; c < 8; ++c) mc[c] = fmaxf(x[c], x[c + 8]);
+#pragma unroll
+            for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], x[c + k], x[c + 8 + k]);
+            }
+            const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
             const float mx2 = mx * sl2;
             if (j == 0) {
                 m_ref = mx2;
@@ -523,30 +529,47 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                     const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_ref - m_new);
                     l *= alpha;
                     m_ref = m_new;
+                    const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
                     for (int cc = 0; cc < HD; cc += 32) {
                         float o[32];
                         tmem_ld_32cols_f(t_o + cc, o);
                         tmem_ld_wait_f(o);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                        for (int c = 0; c < 32; c += 2) {
+                            const uint64_t v = f2_mul(f2_pack(o[c], o[c + 1]), a2);
+                            f2_unpack(v, o[c], o[c + 1]);
+                        }
                         tmem_st_32cols(t_o + cc, reinterpret_cast<const uint32_t(&)[32]>(o));
                     }
                 }
             }
+            // p = 2^(s*scale*log2e - m): packed FMA for the argument, one
+            // ex2 per element, four independent packed partial sums
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float lsum = 0.f;
+            const uint64_t sc2 = f2_pack(sl2, sl2);
+            const uint64_t nm2 = f2_pack(-m_use, -m_use);
+            uint64_t ls[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
-                    const float a = fast_exp2(fmaf(x[h * 64 + c], sl2, -m_use));
-                    const float b = fast_exp2(fmaf(x[h * 64 + c + 1], sl2, -m_use));
-                    lsum += a + b;
+                    float a, b;
+                    f2_unpack(f2_fma(f2_pack(x[h * 64 + c], x[h * 64 + c + 1]), sc2, nm2), a, b);
+                    a = fast_exp2(a);
+                    b = fast_exp2(b);
+                    ls[(c >> 1) & 3] = f2_add(ls[(c >> 1) & 3], f2_pack(a, b));
                     pk[c >> 1] = pack_bf16x2(a, b);
                 }
                 tmem_st_32cols(t_s + h * 32, pk);
+            }
+            float lsum;
+            {
+                const uint64_t s01 = f2_add(ls[0], ls[1]), s23 = f2_add(ls[2], ls[3]);
+                float lo, hi;
+                f2_unpack(f2_add(s01, s23), lo, hi);
+                lsum = lo + hi;
             }
             l += lsum;
             tmem_st_wait();
