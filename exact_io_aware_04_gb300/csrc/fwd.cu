@@ -327,27 +327,31 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
 }
 
 // ---------------------------------------------------------------- MMA warp (one thread)
+// Descriptors are built once per kernel; each K-step adds a compile-time
+// offset (the 14-bit start-address field never overflows: shared memory is
+// below 256 KB).  The tensor pipe's input queue is shallow, so issue is
+// close to synchronous with execution: the issuing thread keeps the work
+// between MMA groups to the minimum.
 template <int HD>
-__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_tile, uint32_t k_tile) {
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
     using C = Cfg<HD>;
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
 #pragma unroll
     for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * C::kPanelBytes + (kk & 3) * 32;
-        mma_smem_smem(tmem_d, smem_desc_sw128(q_tile + off, 16, 1024), smem_desc_sw128(k_tile + off, 16, 1024), idesc,
-                      kk > 0);
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4);
+        mma_smem_smem(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0);
     }
 }
 
 template <int HD>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_tile, bool first) {
-    using C = Cfg<HD>;
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool first) {
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, HD, true);
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_tmem_smem(tmem_o, tmem_p + kk * 8, smem_desc_sw128(v_tile + kk * 2048, C::kPanelBytes, 1024), idesc,
+        mma_tmem_smem(tmem_o, tmem_p + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
                       (!first || kk > 0) ? 1u : 0u);
 }
+
 template <int HD>
 __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                       uint32_t tmem, int n_items) {
@@ -356,7 +360,11 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
     constexpr int S = C::kStages;
     const uint32_t sm_k0 = smem0 + 2 * C::kTileBytes;
     const uint32_t sm_v0 = sm_k0 + S * C::kTileBytes;
-    const uint32_t q0 = smem0, q1 = smem0 + C::kTileBytes;
+    const uint64_t dq0 = smem_desc_sw128(smem0, 16, 1024);
+    const uint64_t dq1 = smem_desc_sw128(smem0 + C::kTileBytes, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sm_k0, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sm_v0, C::kPanelBytes, 1024);
+    constexpr uint64_t kStageDesc = C::kTileBytes >> 4;  // descriptor step between ring stages
     const uint32_t ts0 = tmem + C::col_s(0), ts1 = tmem + C::col_s(1);
     const uint32_t to0 = tmem + C::col_o(0), to1 = tmem + C::col_o(1);
     const int grid = gridDim.x, cta = blockIdx.x;
@@ -378,13 +386,13 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
         if (!ok) break;
         tc_fence_after_sync();
         {
-            const uint32_t kt = sm_k0 + (kc % S) * C::kTileBytes;
+            const uint64_t dk = dk0 + (kc % S) * kStageDesc;
             if (n0 > 0) {
-                issue_s<HD>(ts0, q0, kt);
+                issue_s<HD>(ts0, dq0, dk);
                 tc_commit(bar_at(bar0, BI::s_full + 0));
             }
             if (n1 > 0) {
-                issue_s<HD>(ts1, q1, kt);
+                issue_s<HD>(ts1, dq1, dk);
                 tc_commit(bar_at(bar0, BI::s_full + 1));
             }
         }
@@ -393,7 +401,7 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
         if (n == 1) tc_commit(bar_at(bar0, BI::q_empty));
         for (int j = 0; j < n && ok; ++j) {
             const uint32_t vst = vc % S;
-            const uint32_t vt = sm_v0 + vst * C::kTileBytes;
+            const uint64_t dv = dv0 + vst * kStageDesc;
             ok = mbar_wait(bar_at(bar0, BI::v_full + vst), (vc / S) & 1, p.err);
             if (!ok) break;
             const bool next = j + 1 < n;
@@ -404,20 +412,20 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
                 if (ok && j == 0 && oc0 > 0) ok = mbar_wait(bar_at(bar0, BI::o_empty + 0), (oc0 - 1) & 1, p.err);
                 if (!ok) break;
                 tc_fence_after_sync();
-                issue_pv<HD>(to0, ts0, vt, j == 0);
+                issue_pv<HD>(to0, ts0, dv, j == 0);
                 if (j == n0 - 1) {
                     tc_commit(bar_at(bar0, BI::o_final + 0));
                     ++oc0;
                 }
             }
             const uint32_t kst = kc % S;
-            const uint32_t kt = sm_k0 + kst * C::kTileBytes;
+            const uint64_t dk = dk0 + kst * kStageDesc;
             if (next) {
                 ok = mbar_wait(bar_at(bar0, BI::k_full + kst), (kc / S) & 1, p.err);
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (j + 1 < n0) {
-                    issue_s<HD>(ts0, q0, kt);
+                    issue_s<HD>(ts0, dq0, dk);
                     tc_commit(bar_at(bar0, BI::s_full + 0));
                 }
             }
@@ -428,7 +436,7 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
                 if (ok && j == 0 && oc1 > 0) ok = mbar_wait(bar_at(bar0, BI::o_empty + 1), (oc1 - 1) & 1, p.err);
                 if (!ok) break;
                 tc_fence_after_sync();
-                issue_pv<HD>(to1, ts1, vt, j == 0);
+                issue_pv<HD>(to1, ts1, dv, j == 0);
                 if (j == n1 - 1) {
                     tc_commit(bar_at(bar0, BI::o_final + 1));
                     ++oc1;
@@ -438,7 +446,7 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
             ++vc;
             if (next) {
                 if (j + 1 < n1) {
-                    issue_s<HD>(ts1, q1, kt);
+                    issue_s<HD>(ts1, dq1, dk);
                     tc_commit(bar_at(bar0, BI::s_full + 1));
                 }
                 tc_commit(bar_at(bar0, BI::k_empty + kst));

@@ -1,4 +1,4 @@
 // status.h -- status codes shared by host and device code of libattn.
 #pragma once
 
-#include "../../include/attn.h"
+#include "attn.h"  // include/attn.h (on the -I path)
