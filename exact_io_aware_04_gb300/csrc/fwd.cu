@@ -63,7 +63,10 @@ struct Cfg {
     static constexpr int kPanels = HD / 64;          // 64-element (128-byte) column panels
     static constexpr int kPanelBytes = kBM * 128;    // 128 rows x 128 bytes
     static constexpr int kTileBytes = kPanels * kPanelBytes;
-    static constexpr int kStages = HD == 128 ? 2 : 4;  // K ring depth == V ring depth
+    // K/V ring: slot u of an item holds V_{u-1} and K_u (what one step of
+    // the MMA issuer consumes), so each step needs one wait and one release
+    static constexpr int kStages = HD == 128 ? 2 : 4;
+    static constexpr int kSlotBytes = 2 * kTileBytes;  // [K part][V part]
     static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
     static constexpr uint32_t kTmemCols = 512;
     // tensor-memory column of S_t / P_t and of O_t
@@ -250,8 +253,8 @@ __device__ __forceinline__ int snake(int round, int cta, int grid) {
 template <int S>
 struct BarIdx {
     static constexpr int q_full = 0, q_empty = 1;
-    static constexpr int k_full = 2, k_empty = 2 + S, v_full = 2 + 2 * S, v_empty = 2 + 3 * S;
-    static constexpr int s_full = 2 + 4 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
+    static constexpr int kv_full = 2, kv_empty = 2 + S;
+    static constexpr int s_full = 2 + 2 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
     static constexpr int mma_done = o_empty + 2;
     static constexpr int count = mma_done + 1;
 };
@@ -265,10 +268,9 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
     using C = Cfg<HD>;
     using BI = BarIdx<C::kStages>;
     constexpr int S = C::kStages;
-    const uint32_t sm_k0 = smem0 + 2 * C::kTileBytes;
-    const uint32_t sm_v0 = sm_k0 + S * C::kTileBytes;
+    const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const int grid = gridDim.x, cta = blockIdx.x;
-    uint32_t kc = 0, vc = 0, qc = 0;
+    uint32_t uc = 0, qc = 0;
     bool ok = true;
     Item it;
     for (int r = 0; ok && r * grid < n_items; ++r) {
@@ -292,37 +294,31 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
                             it.h * HD + pn * 64, y);
         }
         ++qc;
-        for (int j = 0; j < n && ok; ++j) {
-            const int y = it.s.k_base + j * kBN;
-            {
-                const uint32_t st = kc % S;
-                if (kc >= S) ok = mbar_wait(bar_at(bar0, BI::k_empty + st), ((kc / S) - 1) & 1, p.err);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar_at(bar0, BI::k_full + st), C::kTileBytes);
+        // slots u = 0..n: V_{u-1} (u >= 1) and K_u (u < n)
+        for (int u = 0; u <= n && ok; ++u) {
+            const uint32_t st = uc % S;
+            if (uc >= S) ok = mbar_wait(bar_at(bar0, BI::kv_empty + st), ((uc / S) - 1) & 1, p.err);
+            if (!ok) break;
+            const uint32_t slot = ring0 + st * C::kSlotBytes;
+            const uint32_t full = bar_at(bar0, BI::kv_full + st);
+            mbar_arrive_expect_tx(full, (u < n ? C::kTileBytes : 0) + (u >= 1 ? C::kTileBytes : 0));
+            if (u < n) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_2d(sm_k0 + st * C::kTileBytes + pn * C::kPanelBytes, &p.tm_k,
-                                bar_at(bar0, BI::k_full + st), g * HD + pn * 64, y);
-                ++kc;
+                    tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * 64, it.s.k_base + u * kBN);
             }
-            {
-                const uint32_t st = vc % S;
-                if (vc >= S) ok = mbar_wait(bar_at(bar0, BI::v_empty + st), ((vc / S) - 1) & 1, p.err);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar_at(bar0, BI::v_full + st), C::kTileBytes);
+            if (u >= 1) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_2d(sm_v0 + st * C::kTileBytes + pn * C::kPanelBytes, &p.tm_v,
-                                bar_at(bar0, BI::v_full + st), g * HD + pn * 64, y);
-                ++vc;
+                    tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
+                                it.s.k_base + (u - 1) * kBN);
             }
+            ++uc;
         }
     }
     // Drain: every load issued must have landed before the CTA exits.
-    for (uint32_t i = (kc > S ? kc - S : 0); i < kc; ++i)
-        mbar_wait(bar_at(bar0, BI::k_full + i % S), (i / S) & 1, p.err);
-    for (uint32_t i = (vc > S ? vc - S : 0); i < vc; ++i)
-        mbar_wait(bar_at(bar0, BI::v_full + i % S), (i / S) & 1, p.err);
+    for (uint32_t i = (uc > S ? uc - S : 0); i < uc; ++i)
+        mbar_wait(bar_at(bar0, BI::kv_full + i % S), (i / S) & 1, p.err);
     if (qc > 0) mbar_wait(bar_at(bar0, BI::q_full), (qc - 1) & 1, p.err);
 }
 
@@ -358,17 +354,16 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
     using C = Cfg<HD>;
     using BI = BarIdx<C::kStages>;
     constexpr int S = C::kStages;
-    const uint32_t sm_k0 = smem0 + 2 * C::kTileBytes;
-    const uint32_t sm_v0 = sm_k0 + S * C::kTileBytes;
+    const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const uint64_t dq0 = smem_desc_sw128(smem0, 16, 1024);
     const uint64_t dq1 = smem_desc_sw128(smem0 + C::kTileBytes, 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(sm_k0, 16, 1024);
-    const uint64_t dv0 = smem_desc_sw128(sm_v0, C::kPanelBytes, 1024);
-    constexpr uint64_t kStageDesc = C::kTileBytes >> 4;  // descriptor step between ring stages
+    const uint64_t dk0 = smem_desc_sw128(ring0, 16, 1024);                              // K part of slot 0
+    const uint64_t dv0 = smem_desc_sw128(ring0 + C::kTileBytes, C::kPanelBytes, 1024);  // V part of slot 0
+    constexpr uint64_t kSlotDesc = C::kSlotBytes >> 4;  // descriptor step between ring slots
     const uint32_t ts0 = tmem + C::col_s(0), ts1 = tmem + C::col_s(1);
     const uint32_t to0 = tmem + C::col_o(0), to1 = tmem + C::col_o(1);
     const int grid = gridDim.x, cta = blockIdx.x;
-    uint32_t kc = 0, vc = 0, qc = 0, pc0 = 0, pc1 = 0, oc0 = 0, oc1 = 0;
+    uint32_t uc = 0, qc = 0, pc0 = 0, pc1 = 0, oc0 = 0, oc1 = 0;
     bool ok = true;
     Item it;
     for (int r = 0; ok && r * grid < n_items; ++r) {
@@ -381,12 +376,11 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
         ok = mbar_wait(bar_at(bar0, BI::q_full), qc & 1, p.err);
         ++qc;
         if (!ok) break;
-        // K_0 -> S0(0), S1(0)
-        ok = mbar_wait(bar_at(bar0, BI::k_full + kc % S), (kc / S) & 1, p.err);
+        // slot 0 of the item: K_0 -> S0(0), S1(0)
+        ok = mbar_wait(bar_at(bar0, BI::kv_full + uc % S), (uc / S) & 1, p.err);
         if (!ok) break;
-        tc_fence_after_sync();
         {
-            const uint64_t dk = dk0 + (kc % S) * kStageDesc;
+            const uint64_t dk = dk0 + (uc % S) * kSlotDesc;
             if (n0 > 0) {
                 issue_s<HD>(ts0, dq0, dk);
                 tc_commit(bar_at(bar0, BI::s_full + 0));
@@ -395,17 +389,17 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
                 issue_s<HD>(ts1, dq1, dk);
                 tc_commit(bar_at(bar0, BI::s_full + 1));
             }
+            tc_commit(bar_at(bar0, BI::kv_empty + uc % S));
+            ++uc;
+            if (n == 1) tc_commit(bar_at(bar0, BI::q_empty));
         }
-        tc_commit(bar_at(bar0, BI::k_empty + kc % S));
-        ++kc;
-        if (n == 1) tc_commit(bar_at(bar0, BI::q_empty));
+        // slot j+1: V_j -> PV0(j), PV1(j) and K_{j+1} -> S0(j+1), S1(j+1)
         for (int j = 0; j < n && ok; ++j) {
-            const uint32_t vst = vc % S;
-            const uint64_t dv = dv0 + vst * kStageDesc;
-            ok = mbar_wait(bar_at(bar0, BI::v_full + vst), (vc / S) & 1, p.err);
+            const uint32_t st = uc % S;
+            ok = mbar_wait(bar_at(bar0, BI::kv_full + st), (uc / S) & 1, p.err);
             if (!ok) break;
-            const bool next = j + 1 < n;
-            // ---- tile 0: PV0(j), then S0(j+1)
+            const uint64_t dk = dk0 + st * kSlotDesc;
+            const uint64_t dv = dv0 + st * kSlotDesc;
             if (j < n0) {
                 ok = mbar_wait(bar_at(bar0, BI::p_ready + 0), pc0 & 1, p.err);
                 ++pc0;
@@ -418,18 +412,10 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
                     ++oc0;
                 }
             }
-            const uint32_t kst = kc % S;
-            const uint64_t dk = dk0 + kst * kStageDesc;
-            if (next) {
-                ok = mbar_wait(bar_at(bar0, BI::k_full + kst), (kc / S) & 1, p.err);
-                if (!ok) break;
-                tc_fence_after_sync();
-                if (j + 1 < n0) {
-                    issue_s<HD>(ts0, dq0, dk);
-                    tc_commit(bar_at(bar0, BI::s_full + 0));
-                }
+            if (j + 1 < n0) {
+                issue_s<HD>(ts0, dq0, dk);
+                tc_commit(bar_at(bar0, BI::s_full + 0));
             }
-            // ---- tile 1: PV1(j), then S1(j+1)
             if (j < n1) {
                 ok = mbar_wait(bar_at(bar0, BI::p_ready + 1), pc1 & 1, p.err);
                 ++pc1;
@@ -442,17 +428,13 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
                     ++oc1;
                 }
             }
-            tc_commit(bar_at(bar0, BI::v_empty + vst));
-            ++vc;
-            if (next) {
-                if (j + 1 < n1) {
-                    issue_s<HD>(ts1, dq1, dk);
-                    tc_commit(bar_at(bar0, BI::s_full + 1));
-                }
-                tc_commit(bar_at(bar0, BI::k_empty + kst));
-                ++kc;
-                if (j + 2 == n) tc_commit(bar_at(bar0, BI::q_empty));
+            if (j + 1 < n1) {
+                issue_s<HD>(ts1, dq1, dk);
+                tc_commit(bar_at(bar0, BI::s_full + 1));
             }
+            tc_commit(bar_at(bar0, BI::kv_empty + st));
+            ++uc;
+            if (j + 2 == n) tc_commit(bar_at(bar0, BI::q_empty));
         }
     }
     // Drain: all issued tensor-core work must finish before TMEM is freed.
