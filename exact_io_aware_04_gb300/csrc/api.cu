@@ -234,6 +234,8 @@ attn_status attn_get_device_status(void* stream) {
 
 int attn_set_validation(int enabled) { return g_validation.exchange(enabled ? 1 : 0); }
 
+int attn_test_drop_page_load(int enabled) { return attn::set_drop_page_load(enabled); }
+
 const char* attn_status_string(attn_status status) {
     switch (status) {
         case ATTN_OK: return "ATTN_OK";

@@ -25,6 +25,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -48,6 +49,7 @@ struct DecodeParams {
     int pages_per_chunk, max_chunks, head_groups, heads_per_cta, m_tiles;
     float scale_log2;
     int validate;
+    int drop_first_page;  // test hook: CTA (0, 0) skips its first page copy
     int* err;
 };
 
@@ -139,7 +141,8 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
                     const int it = base + i;
                     const int st = it % n_stages;
                     if (it >= n_stages) ok = mbar_wait(smem_addr(&bar_empty[st]), ((it / n_stages) - 1) & 1, p.err);
-                    if (ok) {
+                    const bool drop = p.drop_first_page && it == 0 && blockIdx.x == 0 && blockIdx.y == 0;
+                    if (ok && !drop) {
                         const uint32_t dst = smem0 + st * stage_bytes;
                         mbar_arrive_expect_tx(smem_addr(&bar_full[st]), stage_bytes);
                         tma_load_5d(dst, &p.tm_k, smem_addr(&bar_full[st]), 0, 0, hg * HG, 0, page);
@@ -153,7 +156,8 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
         }
         if (lane == 0) {
             // drain: every issued copy has landed before the CTA may exit
-            for (int it = max(0, issued - n_stages); it < issued; ++it)
+            const int first = p.drop_first_page && blockIdx.x == 0 && blockIdx.y == 0 ? 1 : 0;
+            for (int it = max(first, issued + first - n_stages); it < issued + first; ++it)
                 mbar_wait(smem_addr(&bar_full[it % n_stages]), (it / n_stages) & 1, p.err);
         }
         __syncwarp();
@@ -421,6 +425,7 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     p.m_tiles = (p.group + 15) / 16;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.validate = validation_enabled() ? 1 : 0;
+    p.drop_first_page = set_drop_page_load(0);  // consume the one-shot test switch
     p.err = dev.err_word;
 
     if (p.validate)
@@ -469,6 +474,12 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
 }
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_drop_page_load{0};
+}  // namespace
+
+int set_drop_page_load(int enabled) { return g_drop_page_load.exchange(enabled ? 1 : 0); }
 
 bool make_decode_plan(int B, int Hq, int Hkv, int d, int page_size, int max_pages, int num_splits,
                       DecodePlan* plan) {

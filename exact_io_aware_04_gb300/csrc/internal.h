@@ -30,6 +30,9 @@ attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const 
 
 bool validation_enabled();
 
+// One-shot test switch: the next paged-decode launch drops one page copy.
+int set_drop_page_load(int enabled);
+
 // ---- launchers (one per translation unit) ----
 struct FwdArgs {
     const void *q, *k, *v;

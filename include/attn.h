@@ -213,6 +213,17 @@ attn_status attn_get_device_status(void *stream);
  */
 int attn_set_validation(int enabled);
 
+/*
+ * attn_test_drop_page_load -- test hook for the failure path (not for
+ * production use).  When called with 1, the next attn_decode_paged launch
+ * makes one CTA (chunk 0 of sequence 0) skip its first page copy, so the
+ * consumer warps' bounded wait for that page expires: the kernel records
+ * ATTN_ERR_TIMEOUT in the device error word and returns instead of hanging;
+ * the outputs of that sequence are undefined.  The switch clears itself after
+ * one launch.  Returns the previous setting.
+ */
+int attn_test_drop_page_load(int enabled);
+
 /* attn_status_string -- static, human-readable name of a status code. */
 const char *attn_status_string(attn_status status);
 

@@ -105,3 +105,19 @@ def test_full_size_paged_decode(la):
     stats = assert_close(dd.name, out.float().cpu().numpy().reshape(-1, dd.d), lse.cpu().numpy().reshape(-1),
                          ref_o, ref_lse)
     print(dd.name, stats)
+
+
+def test_timeout_path_reports_and_recovers(la):
+    """Failure detection without a fault: one CTA's first page copy is dropped
+    (test hook), its consumers' bounded wait expires, the kernel reports
+    ATTN_ERR_TIMEOUT through the device error word and returns; the context
+    stays usable and the next call is correct."""
+    dd = workloads.make_decode([300, 40, 700], 8, 2, 128, num_pages=128, seed=31, nan_fill_unused=True)
+    assert la.attn_get_device_status() == 0
+    L = la.lib()
+    assert L.attn_test_drop_page_load(1) == 0
+    out, lse = run_decode(la, dd)
+    assert la.attn_get_device_status() == la.ATTN_ERR_TIMEOUT
+    assert L.attn_test_drop_page_load(0) == 0   # the switch was consumed by that launch
+    check(la, dd)
+    assert la.attn_get_device_status() == 0
