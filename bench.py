@@ -13,7 +13,8 @@ events on the launching stream; L2 is flushed (a 256 MB write) between steps,
 outside the timed calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
-                  [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|tiny|paged_decode]
+                  [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|tiny|paged_decode|
+                              paged_decode_small]
 
 --impl reference times the fp64 CPU oracle on the host cores (bounded row
 samples of the same workload, same metric and unit).  Under torchrun each rank
@@ -93,6 +94,35 @@ def decode_bytes(d) -> float:
     kv = sum(lens) * d.Hkv * d.d * 2 * 2
     pages = sum(-(-L // d.page_size) for L in lens)
     return float(kv + 2 * d.B * d.Hq * d.d * 2 + 4 * d.B * d.Hq + 4 * pages + 4 * d.B)
+
+
+KERNEL_SOURCES = {
+    "attn_fwd": ["exact_io_aware_04_gb300/csrc/fwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
+    "attn_decode_paged": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
+}
+
+
+def source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/traffic.json (an ncu capture), or
+    None when no capture exists for this workload or the kernel source has
+    changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel, {}).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha256") != source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def load_peaks():
@@ -255,6 +285,8 @@ def make_workloads(name, device):
         prefill = getattr(workloads, pname)() if pname != "tiny" else workloads.tiny(True)
     if name in ("hot_path", "paged_decode"):
         decode = workloads.paged_decode(device=device)
+    if name == "paged_decode_small":
+        decode = workloads.paged_decode_small(device=device)
     return prefill, decode
 
 
@@ -303,7 +335,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libattn", "reference"], default="libattn")
     ap.add_argument("--workload", default="hot_path",
-                    choices=["hot_path", "paged_decode"] + list(PREFILL_WORKLOADS))
+                    choices=["hot_path", "paged_decode", "paged_decode_small"] + list(PREFILL_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
@@ -392,7 +424,9 @@ def main(argv=None):
         ach = p_flops / (f_tot / args.steps * 1e-3) / 1e12
         rooflines["attn_fwd"] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
                                  "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                                 "frac_nominal": ach / NOMINAL["bf16_tflops"], "traffic": None,
+                                 "frac_nominal": ach / NOMINAL["bf16_tflops"],
+                                 "traffic": measured_traffic("attn_fwd", prefill.name),
+                                 "compulsory_bytes": prefill_bytes(prefill),
                                  "peak_source": f"{peaks_kind} bf16 burst",
                                  "ms_per_launch_median": statistics.median(f_ms),
                                  "ms_per_launch_p95": sorted(f_ms)[int(0.95 * (len(f_ms) - 1))],
@@ -405,7 +439,8 @@ def main(argv=None):
         ach = d_bytes / (d_tot / args.steps * 1e-3) / 1e9
         rooflines["attn_decode_paged"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                           "frac": ach / peaks["hbm_gbs"], "frac_nominal": ach / NOMINAL["hbm_gbs"],
-                                          "traffic": None, "peak_source": f"{peaks_kind} copy bandwidth",
+                                          "traffic": measured_traffic("attn_decode_paged", decode.name),
+                                          "peak_source": f"{peaks_kind} copy bandwidth",
                                           "ms_per_call_median": statistics.median(d_ms),
                                           "ms_per_call_p95": sorted(d_ms)[int(0.95 * (len(d_ms) - 1))],
                                           "bytes_per_call": d_bytes, "launches_per_call": 2}

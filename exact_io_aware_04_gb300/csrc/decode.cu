@@ -26,6 +26,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -338,10 +339,15 @@ struct CombineParams {
 };
 
 // One warp per (sequence, query head): lse = log sum_i exp(lse_i), O = sum_i
-// exp(lse_i - lse) O_i over the chunks the sequence actually has.
+// exp(lse_i - lse) O_i over the chunks the sequence actually has.  Lane l
+// owns d-elements [l*d/32, (l+1)*d/32) as one vector load per chunk; the
+// weights of 32 chunks at a time are computed once and broadcast by shuffle,
+// so the partial-output loads of consecutive chunks are independent.
 template <int HD>
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineParams p) {
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(256) attn_decode_combine_kernel(const CombineParams p) {
+    constexpr int V = HD / 32;  // floats per lane
+    using Vec = typename std::conditional<V == 4, float4, float2>::type;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= p.B * p.Hq) return;
     const int b = row / p.Hq;
@@ -350,33 +356,47 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineP
     const int n = (len + chunk_tokens - 1) / chunk_tokens;
     const float* lse_s = p.part_lse + static_cast<size_t>(row) * p.max_chunks;
     float mx = -INFINITY;
-    for (int i = lane; i < n; i += 32) mx = fmaxf(mx, lse_s[i]);
+    for (int i = lane; i < n; i += 32) mx = fmaxf(mx, __ldg(lse_s + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float acc[HD / 32];
+    float acc[V];
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) acc[c] = 0.f;
-    float total = 0.f;
-    if (mx != -INFINITY) {
-        for (int i = lane; i < n; i += 32) total += expf(lse_s[i] - mx);
+    for (int c = 0; c < V; ++c) acc[c] = 0.f;
+    __nv_bfloat16* dst = p.out + static_cast<size_t>(row) * HD + lane * V;
+    if (mx == -INFINITY) {  // no keys: O = 0, lse = -inf
+        if (lane == 0) p.lse[row] = -INFINITY;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-        const float lse_tot = mx + logf(total);
-        const float* po = p.part_o + static_cast<size_t>(row) * p.max_chunks * HD;
-        for (int i = 0; i < n; ++i) {
-            const float li = lse_s[i];
-            if (li == -INFINITY) continue;
-            const float w = expf(li - lse_tot);
-#pragma unroll
-            for (int c = 0; c < HD / 32; ++c) acc[c] = fmaf(w, po[static_cast<size_t>(i) * HD + c * 32 + lane], acc[c]);
-        }
-        if (lane == 0) p.lse[row] = lse_tot;
-    } else if (lane == 0) {
-        p.lse[row] = -INFINITY;
+        for (int c = 0; c < V; ++c) dst[c] = __float2bfloat16_rn(0.f);
+        return;
     }
-    __nv_bfloat16* dst = p.out + static_cast<size_t>(row) * HD;
+    float total = 0.f;
+    for (int i = lane; i < n; i += 32) total += expf(__ldg(lse_s + i) - mx);
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) dst[c * 32 + lane] = __float2bfloat16_rn(acc[c]);
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    const float lse_tot = mx + logf(total);
+    const float* po = p.part_o + static_cast<size_t>(row) * p.max_chunks * HD + lane * V;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int m = min(32, n - c0);
+        const float li = lane < m ? __ldg(lse_s + c0 + lane) : -INFINITY;
+        const float wl = li == -INFINITY ? 0.f : expf(li - lse_tot);
+#pragma unroll 4
+        for (int k = 0; k < m; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wl, k);
+            const Vec x = __ldg(reinterpret_cast<const Vec*>(po + static_cast<size_t>(c0 + k) * HD));
+            const float* xs = reinterpret_cast<const float*>(&x);
+#pragma unroll
+            for (int c = 0; c < V; ++c) acc[c] = fmaf(w, xs[c], acc[c]);
+        }
+    }
+    if (lane == 0) p.lse[row] = lse_tot;
+    if (V == 4) {
+        uint2 w2;
+        w2.x = pack_bf16x2(acc[0], acc[1]);
+        w2.y = pack_bf16x2(acc[2 % V], acc[3 % V]);
+        *reinterpret_cast<uint2*>(dst) = w2;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0], acc[1 % V]);
+    }
 }
 
 // Optional check of seq_lens and of the block-table entries each sequence uses.
@@ -464,7 +484,7 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     c.pages_per_chunk = plan.pages_per_chunk;
     c.max_chunks = plan.max_chunks;
     const int rows = a.B * a.Hq;
-    attn_decode_combine_kernel<HD><<<(rows + 3) / 4, 128, 0, stream>>>(c);
+    attn_decode_combine_kernel<HD><<<(rows + 7) / 8, 256, 0, stream>>>(c);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error_message("attn_decode_combine launch: %s", cudaGetErrorString(e));

@@ -247,6 +247,16 @@ def decode_lengths(seed=SEED_BASE + 4, n=64, lo=4096, hi=32768):
     return randint(lo, hi, n, seed).tolist()
 
 
+def paged_decode_small(device="cpu", nan_fill_unused=False) -> Decode:
+    """The paged decode layout at one eighth of the lengths (U[512, 4096]) in a
+    25,000-page pool (1.6 GB of K+V): a case small enough for multi-pass
+    profiler captures of the same kernel."""
+    lens = decode_lengths(seed=SEED_BASE + 5, lo=512, hi=4096)
+    return make_decode(lens, 32, 8, 128, num_pages=25_000, seed=SEED_BASE + 5, page_size=16,
+                       max_pages=256, nan_fill_unused=nan_fill_unused,
+                       name="paged_decode_small_b64_hq32_hkv8_d128", device=device)
+
+
 def paged_decode(device="cpu", nan_fill_unused=False) -> Decode:
     """B=64, Hq=32, Hkv=8, d=128, len ~ U[4096, 32768], 16-token pages in a
     200,000-page pool (one pool each for K and V), block table [64, 2048]."""
