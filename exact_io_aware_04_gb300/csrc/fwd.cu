@@ -6,8 +6,9 @@
 //   warps 0-3  softmax group 0: owns query tile 0 (one thread per row)
 //   warps 4-7  softmax group 1: owns query tile 1
 //   warp  8    producer: TMA loads of Q tiles and a ring of K and V tiles
-//   warp  9    MMA issuer (one thread) and tensor-memory owner
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  9    MMA issuer of query tile 0 (one thread), tensor-memory owner
+//   warp  10   MMA issuer of query tile 1 (one thread)
+//   warp  11   idle (it completes the third warpgroup)
 // The softmax warpgroups raise their register budget to kSoftmaxRegs and the
 // third warpgroup lowers its own to kControlRegs (setmaxnreg).
 // Tensor memory (512 columns x 128 lanes x 32 bit):
@@ -250,13 +251,21 @@ __device__ __forceinline__ int snake(int round, int cta, int grid) {
 }
 
 // Shared-memory barrier indices (each barrier is 8 bytes at bar0 + 8*index).
+// Per query tile t: q_full+t, q_empty+t, s_full+t, p_ready+t, o_final+t,
+// o_empty+t, tok+t (issuer t has issued its MMAs of a ring slot), mma_done+t.
+// Per ring slot s: kv_full+s, kv_empty+s (one release from each issuer).
 template <int S>
 struct BarIdx {
-    static constexpr int q_full = 0, q_empty = 1;
-    static constexpr int kv_full = 2, kv_empty = 2 + S;
-    static constexpr int s_full = 2 + 2 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
-    static constexpr int mma_done = o_empty + 2;
-    static constexpr int count = mma_done + 1;
+    static constexpr int q_full = 0, q_empty = 2;
+    static constexpr int kv_full = 4, kv_empty = 4 + S;
+    static constexpr int s_full = 4 + 2 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
+    static constexpr int tok = o_empty + 2, mma_done = tok + 2;
+    static constexpr int count = mma_done + 2;
+    __device__ static constexpr uint32_t arrivals(int i) {
+        return (i >= p_ready && i < p_ready + 2) || (i >= o_empty && i < o_empty + 2) ? 4u
+               : (i >= kv_empty && i < kv_empty + S)                                   ? 2u
+                                                                                       : 1u;
+    }
 };
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); }
@@ -270,7 +279,7 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
     constexpr int S = C::kStages;
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const int grid = gridDim.x, cta = blockIdx.x;
-    uint32_t uc = 0, qc = 0;
+    uint32_t uc = 0, qc[2] = {0, 0};
     bool ok = true;
     Item it;
     for (int r = 0; ok && r * grid < n_items; ++r) {
@@ -280,20 +289,20 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
         const int n = max(it.n[0], it.n[1]);
         if (n == 0) continue;
         const int g = it.h / p.group;
-        if (qc > 0) ok = mbar_wait(bar_at(bar0, BI::q_empty), (qc - 1) & 1, p.err);
-        if (!ok) break;
-        const uint32_t qbytes = (it.n[0] > 0 ? C::kTileBytes : 0) + (it.n[1] > 0 ? C::kTileBytes : 0);
-        mbar_arrive_expect_tx(bar_at(bar0, BI::q_full), qbytes);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (it.n[t] == 0) continue;
+            if (qc[t] > 0) ok = mbar_wait(bar_at(bar0, BI::q_empty + t), (qc[t] - 1) & 1, p.err);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar_at(bar0, BI::q_full + t), C::kTileBytes);
             const int y = it.s.q_base + it.pair * kPairRows + t * kBM;
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
-                tma_load_2d(smem0 + t * C::kTileBytes + pn * C::kPanelBytes, &p.tm_q, bar_at(bar0, BI::q_full),
+                tma_load_2d(smem0 + t * C::kTileBytes + pn * C::kPanelBytes, &p.tm_q, bar_at(bar0, BI::q_full + t),
                             it.h * HD + pn * 64, y);
+            ++qc[t];
         }
-        ++qc;
+        if (!ok) break;
         // slots u = 0..n: V_{u-1} (u >= 1) and K_u (u < n)
         for (int u = 0; u <= n && ok; ++u) {
             const uint32_t st = uc % S;
@@ -319,7 +328,8 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
     // Drain: every load issued must have landed before the CTA exits.
     for (uint32_t i = (uc > S ? uc - S : 0); i < uc; ++i)
         mbar_wait(bar_at(bar0, BI::kv_full + i % S), (i / S) & 1, p.err);
-    if (qc > 0) mbar_wait(bar_at(bar0, BI::q_full), (qc - 1) & 1, p.err);
+    for (int t = 0; t < 2; ++t)
+        if (qc[t] > 0) mbar_wait(bar_at(bar0, BI::q_full + t), (qc[t] - 1) & 1, p.err);
 }
 
 // ---------------------------------------------------------------- MMA warp (one thread)
@@ -348,98 +358,83 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
                       (!first || kk > 0) ? 1u : 0u);
 }
 
+// Two issuing threads, one per query tile, that take turns slot by slot: a
+// thread issues its MMAs of ring slot u only after the other thread has
+// issued its MMAs of the preceding turn (the `tok` barriers), so the tensor
+// pipe sees the single-issuer order
+//     ..., PV0(j), S0(j+1), PV1(j), S1(j+1), PV0(j+1), ...
+// while each thread's barrier waits overlap the other thread's MMAs (issue is
+// close to synchronous with execution, so a wait in a lone issuer idles the
+// tensor pipe).  Slot u of an item holds V_{u-1} and K_u: issuer t runs
+// PV_t(u-1) if u-1 < n_t and S_t(u) if u < n_t, then releases the slot.
 template <int HD>
 __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
-                                      uint32_t tmem, int n_items) {
+                                      uint32_t tmem, int n_items, int t) {
     using C = Cfg<HD>;
     using BI = BarIdx<C::kStages>;
     constexpr int S = C::kStages;
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
-    const uint64_t dq0 = smem_desc_sw128(smem0, 16, 1024);
-    const uint64_t dq1 = smem_desc_sw128(smem0 + C::kTileBytes, 16, 1024);
+    const uint64_t dq = smem_desc_sw128(smem0 + t * C::kTileBytes, 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(ring0, 16, 1024);                              // K part of slot 0
     const uint64_t dv0 = smem_desc_sw128(ring0 + C::kTileBytes, C::kPanelBytes, 1024);  // V part of slot 0
     constexpr uint64_t kSlotDesc = C::kSlotBytes >> 4;  // descriptor step between ring slots
-    const uint32_t ts0 = tmem + C::col_s(0), ts1 = tmem + C::col_s(1);
-    const uint32_t to0 = tmem + C::col_o(0), to1 = tmem + C::col_o(1);
+    const uint32_t ts = tmem + C::col_s(t);
+    const uint32_t to = tmem + C::col_o(t);
+    const uint32_t b_q_full = bar_at(bar0, BI::q_full + t), b_q_empty = bar_at(bar0, BI::q_empty + t);
+    const uint32_t b_s_full = bar_at(bar0, BI::s_full + t), b_p_ready = bar_at(bar0, BI::p_ready + t);
+    const uint32_t b_o_final = bar_at(bar0, BI::o_final + t), b_o_empty = bar_at(bar0, BI::o_empty + t);
+    const uint32_t b_tok_mine = bar_at(bar0, BI::tok + t), b_tok_other = bar_at(bar0, BI::tok + (1 - t));
     const int grid = gridDim.x, cta = blockIdx.x;
-    uint32_t uc = 0, qc = 0, pc0 = 0, pc1 = 0, oc0 = 0, oc1 = 0;
+    uint32_t uc = 0, qc = 0, pc = 0, oc = 0;
     bool ok = true;
     Item it;
     for (int r = 0; ok && r * grid < n_items; ++r) {
         const int k = snake(r, cta, grid);
         if (k >= n_items) continue;
         item_at(p, sc, k, it);
-        const int n0 = it.n[0], n1 = it.n[1];
-        const int n = max(n0, n1);
+        const int n = max(it.n[0], it.n[1]);
+        const int nt = t == 0 ? it.n[0] : it.n[1];
         if (n == 0) continue;
-        ok = mbar_wait(bar_at(bar0, BI::q_full), qc & 1, p.err);
-        ++qc;
-        if (!ok) break;
-        // slot 0 of the item: K_0 -> S0(0), S1(0)
-        ok = mbar_wait(bar_at(bar0, BI::kv_full + uc % S), (uc / S) & 1, p.err);
-        if (!ok) break;
-        {
-            const uint64_t dk = dk0 + (uc % S) * kSlotDesc;
-            if (n0 > 0) {
-                issue_s<HD>(ts0, dq0, dk);
-                tc_commit(bar_at(bar0, BI::s_full + 0));
-            }
-            if (n1 > 0) {
-                issue_s<HD>(ts1, dq1, dk);
-                tc_commit(bar_at(bar0, BI::s_full + 1));
-            }
-            tc_commit(bar_at(bar0, BI::kv_empty + uc % S));
-            ++uc;
-            if (n == 1) tc_commit(bar_at(bar0, BI::q_empty));
-        }
-        // slot j+1: V_j -> PV0(j), PV1(j) and K_{j+1} -> S0(j+1), S1(j+1)
-        for (int j = 0; j < n && ok; ++j) {
-            const uint32_t st = uc % S;
-            ok = mbar_wait(bar_at(bar0, BI::kv_full + st), (uc / S) & 1, p.err);
+        if (nt > 0) {
+            ok = mbar_wait(b_q_full, qc & 1, p.err);
+            ++qc;
             if (!ok) break;
-            const uint64_t dk = dk0 + st * kSlotDesc;
-            const uint64_t dv = dv0 + st * kSlotDesc;
-            if (j < n0) {
-                ok = mbar_wait(bar_at(bar0, BI::p_ready + 0), pc0 & 1, p.err);
-                ++pc0;
-                if (ok && j == 0 && oc0 > 0) ok = mbar_wait(bar_at(bar0, BI::o_empty + 0), (oc0 - 1) & 1, p.err);
-                if (!ok) break;
+        }
+        for (int u = 0; u <= n && ok; ++u) {
+            const uint32_t st = uc % S;
+            const bool pv = u >= 1 && u - 1 < nt;
+            const bool sm = u < nt;
+            ok = mbar_wait(bar_at(bar0, BI::kv_full + st), (uc / S) & 1, p.err);
+            if (ok && pv) {
+                ok = mbar_wait(b_p_ready, pc & 1, p.err);
+                ++pc;
+                if (ok && u == 1 && oc > 0) ok = mbar_wait(b_o_empty, (oc - 1) & 1, p.err);
+            }
+            // my turn: issuer 0 follows issuer 1's previous turn, issuer 1 follows issuer 0's turn on this slot
+            if (ok && (t == 1 || uc > 0)) ok = mbar_wait(b_tok_other, (t == 1 ? uc : uc - 1) & 1, p.err);
+            if (!ok) break;
+            if (pv) {
                 tc_fence_after_sync();
-                issue_pv<HD>(to0, ts0, dv, j == 0);
-                if (j == n0 - 1) {
-                    tc_commit(bar_at(bar0, BI::o_final + 0));
-                    ++oc0;
+                issue_pv<HD>(to, ts, dv0 + st * kSlotDesc, u == 1);
+                if (u == nt) {
+                    tc_commit(b_o_final);
+                    ++oc;
                 }
             }
-            if (j + 1 < n0) {
-                issue_s<HD>(ts0, dq0, dk);
-                tc_commit(bar_at(bar0, BI::s_full + 0));
+            if (sm) {
+                issue_s<HD>(ts, dq, dk0 + st * kSlotDesc);
+                tc_commit(b_s_full);
+                if (u == nt - 1) tc_commit(b_q_empty);
             }
-            if (j < n1) {
-                ok = mbar_wait(bar_at(bar0, BI::p_ready + 1), pc1 & 1, p.err);
-                ++pc1;
-                if (ok && j == 0 && oc1 > 0) ok = mbar_wait(bar_at(bar0, BI::o_empty + 1), (oc1 - 1) & 1, p.err);
-                if (!ok) break;
-                tc_fence_after_sync();
-                issue_pv<HD>(to1, ts1, dv, j == 0);
-                if (j == n1 - 1) {
-                    tc_commit(bar_at(bar0, BI::o_final + 1));
-                    ++oc1;
-                }
-            }
-            if (j + 1 < n1) {
-                issue_s<HD>(ts1, dq1, dk);
-                tc_commit(bar_at(bar0, BI::s_full + 1));
-            }
-            tc_commit(bar_at(bar0, BI::kv_empty + st));
+            if (pv || sm) tc_commit(bar_at(bar0, BI::kv_empty + st));
+            else mbar_arrive(bar_at(bar0, BI::kv_empty + st));
+            mbar_arrive(b_tok_mine);
             ++uc;
-            if (j + 2 == n) tc_commit(bar_at(bar0, BI::q_empty));
         }
     }
-    // Drain: all issued tensor-core work must finish before TMEM is freed.
-    tc_commit(bar_at(bar0, BI::mma_done));
-    mbar_wait(bar_at(bar0, BI::mma_done), 0, p.err);
+    // Drain: all tensor-core work this thread issued must finish before TMEM is freed.
+    tc_commit(bar_at(bar0, BI::mma_done + t));
+    mbar_wait(bar_at(bar0, BI::mma_done + t), 0, p.err);
 }
 
 // ---------------------------------------------------------------- softmax warpgroups
@@ -633,11 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (p.varlen) build_schedule(p, sched);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < BI::count; ++i) {
-            uint32_t cnt = 1;
-            if ((i >= BI::p_ready && i < BI::p_ready + 2) || (i >= BI::o_empty && i < BI::o_empty + 2)) cnt = 4;
-            mbar_init(bar_at(bar0, i), cnt);
-        }
+        for (int i = 0; i < BI::count; ++i) mbar_init(bar_at(bar0, i), BI::arrivals(i));
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -658,7 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (warp >= 8) {
         regs_decrease<kControlRegs>();
         if (warp == kProducerWarp && lane == 0) role_producer<HD>(p, sched, smem0, bar0, n_items);
-        if (warp == kMmaWarp && lane == 0) role_mma<HD>(p, sched, smem0, bar0, tmem, n_items);
+        if (warp == kMmaWarp && lane == 0) role_mma<HD>(p, sched, smem0, bar0, tmem, n_items, 0);
+        if (warp == kMmaWarp + 1 && lane == 0) role_mma<HD>(p, sched, smem0, bar0, tmem, n_items, 1);
         __syncwarp();
     } else {
         regs_increase<kSoftmaxRegs>();
