@@ -13,8 +13,8 @@ events on the launching stream; L2 is flushed (a 256 MB write) between steps,
 outside the timed calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
-                  [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|tiny|paged_decode|
-                              paged_decode_small]
+                  [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|swa_causal|tiny|
+                              paged_decode|paged_decode_small]
 
 --impl reference times the fp64 CPU oracle on the host cores (bounded row
 samples of the same workload, same metric and unit).  Under torchrun each rank
@@ -37,11 +37,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import workloads  # noqa: E402
 
-PREFILL_WORKLOADS = ("mha_causal", "gqa_causal", "varlen_chunked", "tiny")
+PREFILL_WORKLOADS = ("mha_causal", "gqa_causal", "varlen_chunked", "swa_causal", "tiny")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -49,25 +50,20 @@ L2_FLUSH_BYTES = 256 << 20
 
 # ---------------------------------------------------------------- accounting
 def attended_pairs(p) -> int:
-    """Exact number of (query, key) pairs the mask allows, over all heads."""
+    """Exact number of (query, key) pairs the mask allows, over all heads:
+    row i of a sequence keeps keys [c - left, c + right] inside [0, nk) with
+    c = i + nk - nq (a side < 0 unbounded; causal caps right at 0)."""
+    left, right = (int(x) for x in getattr(p, "window", (-1, -1)))
+    if p.causal:
+        right = 0
     total = 0
     for nq, nk in p.seq_lens():
         if nq <= 0 or nk <= 0:
             continue
-        if not p.causal:
-            total += nq * nk
-            continue
-        off = nk - nq
-        # row i sees min(nk, max(0, i + off + 1)) keys
-        for_rows = 0
-        i0 = max(0, -off)                    # first row with any key
-        i_full = max(i0, nk - off - 1)       # from here rows see all nk keys
-        i_full = min(i_full, nq)
-        n_part = max(0, i_full - i0)
-        # sum_{i=i0}^{i_full-1} (i + off + 1)
-        for_rows += n_part * (i0 + off + 1) + n_part * (n_part - 1) // 2
-        for_rows += max(0, nq - i_full) * nk
-        total += for_rows
+        c = np.arange(nq, dtype=np.int64) + (nk - nq)
+        lo = np.maximum(c - left, 0) if left >= 0 else np.zeros_like(c)
+        hi = np.minimum(c + right, nk - 1) if right >= 0 else np.full_like(c, nk - 1)
+        total += int(np.maximum(hi - lo + 1, 0).sum())
     return total * p.Hq
 
 
@@ -251,10 +247,15 @@ def oracle_sample_rate(p, target_s: float, seed: int, max_rows: int = 1 << 20):
 
 
 def row_keys(p, b, i):
+    """Keys row i of sequence b keeps (the attended_pairs rule for one row)."""
     nq, nk = p.seq_lens()[b]
-    if not p.causal:
-        return nk
-    return max(0, min(nk, i + nk - nq + 1))
+    left, right = (int(x) for x in getattr(p, "window", (-1, -1)))
+    if p.causal:
+        right = 0
+    c = i + nk - nq
+    lo = max(c - left, 0) if left >= 0 else 0
+    hi = min(c + right, nk - 1) if right >= 0 else nk - 1
+    return max(0, hi - lo + 1)
 
 
 def oracle_decode_rate(d, target_s: float, seed: int):
@@ -360,6 +361,8 @@ def main(argv=None):
             fargs = (pg.q.view(pg.B, pg.Nq, pg.Hq, pg.d), pg.k.view(pg.B, pg.Nk, pg.Hkv, pg.d),
                      pg.v.view(pg.B, pg.Nk, pg.Hkv, pg.d))
             fkw = dict(causal=pg.causal, scale=pg.scale)
+        if tuple(prefill.window) != (-1, -1):
+            fkw["window"] = tuple(prefill.window)
         f_out = torch.empty_like(fargs[0])
         f_lse = torch.empty((pg.Hq, pg.q.shape[0]) if prefill.varlen else (pg.B, pg.Hq, pg.Nq),
                             dtype=torch.float32, device=dev)

@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
             P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
             L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P]
             L.attn_fwd.restype = I
+            L.attn_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P, P]
+            L.attn_fwd_window.restype = I
             L.attn_decode_paged.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
             L.attn_decode_paged.restype = I
             L.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
@@ -106,7 +108,7 @@ def _need(t: torch.Tensor, name: str, dtype):
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
-             scale: Optional[float] = None,
+             scale: Optional[float] = None, window: Optional[tuple] = None,
              cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
     """Prefill forward.  Returns (out, lse).
@@ -114,7 +116,9 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
     Dense: q [B, Nq, Hq, d] and k/v [B, Nk, Hkv, d] (or the flattened
     [B*N, H, d] with B given by a 4-D tensor only).  Packed: q [T_q, Hq, d],
     k/v [T_k, Hkv, d] with int32 cu_seqlens_q/k of B+1 entries.
-    lse is [B, Hq, Nq] (dense) or [Hq, T_q] (packed), fp32."""
+    lse is [B, Hq, Nq] (dense) or [Hq, T_q] (packed), fp32.
+    window = (left, right) selects the local band mask (attn_fwd_window);
+    -1 leaves a side unbounded."""
     _need(q, "q", torch.bfloat16)
     _need(k, "k", torch.bfloat16)
     _need(v, "v", torch.bfloat16)
@@ -151,9 +155,15 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
     _need(lse, "lse", torch.float32)
     if out.shape != q.shape or tuple(lse.shape) != tuple(lse_shape):
         raise ValueError("out/lse have the wrong shape")
-    _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
-                          float(scale), 1 if causal else 0, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-                          _stream_handle(stream)))
+    if window is None:
+        _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                              float(scale), 1 if causal else 0, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                              _stream_handle(stream)))
+    else:
+        left, right = (int(x) for x in window)
+        _check(lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
+                                     float(scale), 1 if causal else 0, left, right, _ptr(cu_seqlens_q),
+                                     _ptr(cu_seqlens_k), _stream_handle(stream)))
     return out, lse
 
 

@@ -119,9 +119,9 @@ using namespace attn;
 
 extern "C" {
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
-                     int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens_q,
-                     const int* cu_seqlens_k, void* stream) {
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                            int Hkv, int Nq, int Nk, int d, float scale, int causal, int window_left,
+                            int window_right, const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream) {
     if (!q || !out || !lse) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: NULL tensor pointer");
     if ((!k || !v) && Nk > 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: NULL k/v with keys present");
     if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr))
@@ -131,6 +131,9 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
     if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
     if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: scale must be finite and > 0");
     if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: causal must be 0 or 1");
+    if (window_left < -1 || window_right < -1)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd: window sides must be >= 0, or -1 for unbounded (%d, %d)",
+                    window_left, window_right);
     if (Nk == 0) {  // no keys: K/V are never read (NULL allowed)
         k = q;
         v = q;
@@ -156,9 +159,18 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
     a.d = d;
     a.scale = scale;
     a.causal = causal;
+    a.win_left = window_left;
+    a.win_right = window_right;
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
     return launch_fwd(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, void* stream) {
+    return attn_fwd_window(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, -1, -1, cu_seqlens_q,
+                           cu_seqlens_k, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size, int max_pages_per_seq,

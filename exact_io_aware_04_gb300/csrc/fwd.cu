@@ -31,9 +31,14 @@
 // PagedAttention", FA4 paragraph): the reference max of a row is only moved
 // when the tile max exceeds it by more than 2^8 in the exponent, which keeps O
 // and l on one common reference (exact in real arithmetic) while skipping
-// almost every rescale.  Causal tiles wholly above the bottom-right boundary
-// are never loaded; only tiles that cross it or a sequence edge are masked
-// ("FlashAttention: Part 1", section 3.5).
+// almost every rescale.  The mask is a band per sequence: query row i keeps
+// keys [i + Nk - Nq - left, i + Nk - Nq + right] inside [0, Nk), a side < 0
+// being unbounded ("Deep Dive - FlashAttention", section "Causal 2.1 is the
+// decode gotcha", its bottom-right corner and its local-window paragraph);
+// causal is right = 0.  Tiles wholly outside the band are never loaded; only
+// tiles that cross a band edge or a sequence edge are masked ("FlashAttention:
+// Part 1", section 3.5).  The two query tiles of an item stream the union of
+// their tile ranges; a tile sits out the slots outside its own range.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <string.h>
@@ -85,7 +90,8 @@ struct FwdParams {
     const int* cu_k;
     int B, Hq, Hkv, group;
     int Nq, Nk;         // dense: per-sequence lengths; packed: total rows
-    int causal, varlen;
+    int win_left, win_right;  // band half-widths in keys, < 0 = unbounded (causal: right = 0)
+    int varlen;
     float scale_log2;   // scale * log2(e)
     int* err;
 };
@@ -116,32 +122,58 @@ __device__ __forceinline__ Seq seq_of(const FwdParams& p, int b) {
     return s;
 }
 
-// Number of K/V tiles a query tile starting at local row q_start needs.
-__device__ __forceinline__ int kv_tiles(int q_start, int nq, int nk, int causal) {
+// First and last allowed key of local query row i (inclusive; last < first
+// means none), clamped to [-1, nk].
+__device__ __forceinline__ int key_first(long long i, int nq, int nk, int left) {
+    if (left < 0) return 0;
+    const long long k = i + nk - nq - left;
+    return static_cast<int>(k < 0 ? 0 : (k > nk ? nk : k));
+}
+__device__ __forceinline__ int key_last(long long i, int nq, int nk, int right) {
+    if (right < 0) return nk - 1;
+    const long long k = i + nk - nq + right;
+    return static_cast<int>(k < -1 ? -1 : (k > nk - 1 ? nk - 1 : k));
+}
+
+// K/V tiles [lo, hi) that the query tile starting at local row q_start needs
+// (lo == hi == 0 when it needs none).
+__device__ __forceinline__ void kv_range(int q_start, int nq, int nk, int left, int right, int& lo, int& hi) {
+    lo = hi = 0;
     const int rows = min(nq - q_start, kBM);
-    if (rows <= 0 || nk <= 0) return 0;
-    const int all = (nk + kBN - 1) / kBN;
-    if (!causal) return all;
-    const int last_key = q_start + rows - 1 + (nk - nq);  // last row's last allowed key
-    if (last_key < 0) return 0;
-    return min(last_key / kBN + 1, all);
+    if (rows <= 0 || nk <= 0) return;
+    const int kmin = key_first(q_start, nq, nk, left);
+    const int kmax = key_last(static_cast<long long>(q_start) + rows - 1, nq, nk, right);
+    if (kmax < kmin) return;
+    lo = kmin / kBN;
+    hi = kmax / kBN + 1;
 }
 
 struct Item {
     int b, pair, h;
     Seq s;
-    int n[2];       // K/V tiles per query tile
-    int rows[2];    // valid query rows per tile
+    int lo[2], hi[2];  // K/V tile range per query tile
+    int n[2];          // hi - lo
+    int j0, len;       // the item's stream: K/V tiles [j0, j0 + len)
+    int rows[2];       // valid query rows per tile
 };
 
 __device__ __forceinline__ void fill_item(const FwdParams& p, Item& it) {
     it.s = seq_of(p, it.b);
+    int j1 = 0;
+    it.j0 = 0x7fffffff;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
         const int q_start = it.pair * kPairRows + t * kBM;
         it.rows[t] = clampi(it.s.nq - q_start, 0, kBM);
-        it.n[t] = kv_tiles(q_start, it.s.nq, it.s.nk, p.causal);
+        kv_range(q_start, it.s.nq, it.s.nk, p.win_left, p.win_right, it.lo[t], it.hi[t]);
+        it.n[t] = it.hi[t] - it.lo[t];
+        if (it.n[t] > 0) {
+            it.j0 = min(it.j0, it.lo[t]);
+            j1 = max(j1, it.hi[t]);
+        }
     }
+    if (j1 == 0) it.j0 = 0;
+    it.len = j1 - it.j0;
 }
 
 // Work list shared by all roles of a CTA (packed mode only).
@@ -181,9 +213,10 @@ __device__ void build_schedule(const FwdParams& p, Schedule& sc) {
         for (int pr = 0; pr < np; ++pr, ++pos) {
             sc.tmp_b[pos] = b;
             sc.tmp_p[pos] = pr;
-            const int c0 = kv_tiles(pr * kPairRows, s.nq, s.nk, p.causal);
-            const int c1 = kv_tiles(pr * kPairRows + kBM, s.nq, s.nk, p.causal);
-            sc.tmp_c[pos] = max(c0, c1);
+            int lo0, hi0, lo1, hi1;
+            kv_range(pr * kPairRows, s.nq, s.nk, p.win_left, p.win_right, lo0, hi0);
+            kv_range(pr * kPairRows + kBM, s.nq, s.nk, p.win_left, p.win_right, lo1, hi1);
+            sc.tmp_c[pos] = hi1 > lo1 ? max(hi0, hi1) - (hi0 > lo0 ? lo0 : lo1) : hi0 - lo0;
         }
     }
     __syncthreads();
@@ -207,7 +240,7 @@ __device__ __forceinline__ void item_at(const FwdParams& p, const Schedule& sc, 
         const int per = p.B * p.Hq;
         const int pairs = (p.Nq + kPairRows - 1) / kPairRows;
         const int pi = k / per;
-        it.pair = p.causal ? pairs - 1 - pi : pi;
+        it.pair = p.win_right >= 0 ? pairs - 1 - pi : pi;  // bounded right edge: later pairs see more keys
         const int rem = k - pi * per;
         it.b = rem / p.Hq;
         it.h = rem - it.b * p.Hq;
@@ -286,7 +319,7 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
         const int k = snake(r, cta, grid);
         if (k >= n_items) continue;
         item_at(p, sc, k, it);
-        const int n = max(it.n[0], it.n[1]);
+        const int n = it.len;
         if (n == 0) continue;
         const int g = it.h / p.group;
 #pragma unroll
@@ -303,7 +336,7 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
             ++qc[t];
         }
         if (!ok) break;
-        // slots u = 0..n: V_{u-1} (u >= 1) and K_u (u < n)
+        // slots u = 0..n: V_{j0+u-1} (u >= 1) and K_{j0+u} (u < n)
         for (int u = 0; u <= n && ok; ++u) {
             const uint32_t st = uc % S;
             if (uc >= S) ok = mbar_wait(bar_at(bar0, BI::kv_empty + st), ((uc / S) - 1) & 1, p.err);
@@ -314,13 +347,14 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
             if (u < n) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * 64, it.s.k_base + u * kBN);
+                    tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * 64,
+                                it.s.k_base + (it.j0 + u) * kBN);
             }
             if (u >= 1) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
                     tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
-                                it.s.k_base + (u - 1) * kBN);
+                                it.s.k_base + (it.j0 + u - 1) * kBN);
             }
             ++uc;
         }
@@ -365,8 +399,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 //     ..., PV0(j), S0(j+1), PV1(j), S1(j+1), PV0(j+1), ...
 // while each thread's barrier waits overlap the other thread's MMAs (issue is
 // close to synchronous with execution, so a wait in a lone issuer idles the
-// tensor pipe).  Slot u of an item holds V_{u-1} and K_u: issuer t runs
-// PV_t(u-1) if u-1 < n_t and S_t(u) if u < n_t, then releases the slot.
+// tensor pipe).  Slot u of an item holds V_{j-1} and K_j (j = j0 + u):
+// issuer t runs PV_t(j-1) and S_t(j) for the tiles inside its own range
+// [lo_t, hi_t), then releases the slot.
 template <int HD>
 __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                       uint32_t tmem, int n_items, int t) {
@@ -392,9 +427,11 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
         const int k = snake(r, cta, grid);
         if (k >= n_items) continue;
         item_at(p, sc, k, it);
-        const int n = max(it.n[0], it.n[1]);
+        const int n = it.len;
         const int nt = t == 0 ? it.n[0] : it.n[1];
         if (n == 0) continue;
+        // this tile's range, relative to the stream
+        const int ulo = (t == 0 ? it.lo[0] : it.lo[1]) - it.j0, uhi = ulo + nt;
         if (nt > 0) {
             ok = mbar_wait(b_q_full, qc & 1, p.err);
             ++qc;
@@ -402,21 +439,21 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
         }
         for (int u = 0; u <= n && ok; ++u) {
             const uint32_t st = uc % S;
-            const bool pv = u >= 1 && u - 1 < nt;
-            const bool sm = u < nt;
+            const bool pv = u - 1 >= ulo && u - 1 < uhi;
+            const bool sm = u >= ulo && u < uhi;
             ok = mbar_wait(bar_at(bar0, BI::kv_full + st), (uc / S) & 1, p.err);
             if (ok && pv) {
                 ok = mbar_wait(b_p_ready, pc & 1, p.err);
                 ++pc;
-                if (ok && u == 1 && oc > 0) ok = mbar_wait(b_o_empty, (oc - 1) & 1, p.err);
+                if (ok && u - 1 == ulo && oc > 0) ok = mbar_wait(b_o_empty, (oc - 1) & 1, p.err);
             }
             // my turn: issuer 0 follows issuer 1's previous turn, issuer 1 follows issuer 0's turn on this slot
             if (ok && (t == 1 || uc > 0)) ok = mbar_wait(b_tok_other, (t == 1 ? uc : uc - 1) & 1, p.err);
             if (!ok) break;
             if (pv) {
                 tc_fence_after_sync();
-                issue_pv<HD>(to, ts, dv0 + st * kSlotDesc, u == 1);
-                if (u == nt) {
+                issue_pv<HD>(to, ts, dv0 + st * kSlotDesc, u - 1 == ulo);
+                if (u == uhi) {
                     tc_commit(b_o_final);
                     ++oc;
                 }
@@ -424,7 +461,7 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
             if (sm) {
                 issue_s<HD>(ts, dq, dk0 + st * kSlotDesc);
                 tc_commit(b_s_full);
-                if (u == nt - 1) tc_commit(b_q_empty);
+                if (u == uhi - 1) tc_commit(b_q_empty);
             }
             if (pv || sm) tc_commit(bar_at(bar0, BI::kv_empty + st));
             else mbar_arrive(bar_at(bar0, BI::kv_empty + st));
@@ -464,16 +501,20 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
         const int rows_t = t == 0 ? it.rows[0] : it.rows[1];
         if (rows_t == 0) continue;
         const int nt = t == 0 ? it.n[0] : it.n[1];
+        const int jlo = t == 0 ? it.lo[0] : it.lo[1];
         const int q_tile0 = it.pair * kPairRows + t * kBM;
         const int q_local = q_tile0 + row_in_tile;
         const bool row_valid = row_in_tile < rows_t;
-        const int off = it.s.nk - it.s.nq;
-        // last allowed key of this row, and of the tile's first row (inclusive)
-        const int kmax_row = p.causal ? min(q_local + off, it.s.nk - 1) : it.s.nk - 1;
-        const int kmax_first = p.causal ? min(q_tile0 + off, it.s.nk - 1) : it.s.nk - 1;
+        const int nq = it.s.nq, nk = it.s.nk;
+        // allowed keys of this row; a tile needs masking when it reaches past
+        // the first row's last key or before the last row's first key
+        const int kmin_row = key_first(q_local, nq, nk, p.win_left);
+        const int kmax_row = key_last(q_local, nq, nk, p.win_right);
+        const int kmax_first = key_last(q_tile0, nq, nk, p.win_right);
+        const int kmin_last = key_first(q_tile0 + kBM - 1, nq, nk, p.win_left);
         float m_ref = -INFINITY;
         float l = 0.f;
-        for (int j = 0; j < nt; ++j) {
+        for (int j = jlo; j < jlo + nt; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, scnt & 1, p.err));
             ++scnt;
             if (!ok) break;
@@ -488,11 +529,17 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             tmem_ld_wait_f(x + 64);
             tmem_ld_wait_f(x + 96);
             const int k0 = j * kBN;
-            if (k0 + kBN - 1 > kmax_first) {
-                const int lim = kmax_row - k0;  // columns > lim are masked
+            if (k0 < kmin_last) {  // crosses the band's left edge (and maybe its right one)
+                const int hi_lim = kmax_row - k0;  // columns outside [lo_lim, hi_lim] are masked
+                const int lo_lim = kmin_row - k0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (c > lim) x[c] = -INFINITY;
+                    if (c > hi_lim || c < lo_lim) x[c] = -INFINITY;
+            } else if (k0 + kBN - 1 > kmax_first) {  // crosses the right edge or the sequence end only
+                const int hi_lim = kmax_row - k0;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (c > hi_lim) x[c] = -INFINITY;
             }
             // row max: 3-input max over 8 independent chains
             float mc[8];
@@ -505,7 +552,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             }
             const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
             const float mx2 = mx * sl2;
-            if (j == 0) {
+            if (j == jlo) {
                 m_ref = mx2;
             } else {
                 const bool need = mx2 > m_ref + kRescaleThreshold;
@@ -710,7 +757,8 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     p.group = a.Hq / a.Hkv;
     p.Nq = a.Nq;
     p.Nk = a.Nk;
-    p.causal = a.causal ? 1 : 0;
+    p.win_left = a.win_left < 0 ? -1 : a.win_left;
+    p.win_right = a.causal ? 0 : (a.win_right < 0 ? -1 : a.win_right);
     p.varlen = varlen ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.err = dev.err_word;

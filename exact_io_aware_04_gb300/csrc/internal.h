@@ -41,6 +41,7 @@ struct FwdArgs {
     int B, Hq, Hkv, Nq, Nk, d;
     float scale;
     int causal;
+    int win_left, win_right;  // local window, < 0 = unbounded
     const int *cu_q, *cu_k;
 };
 attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream);

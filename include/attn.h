@@ -100,6 +100,28 @@ attn_status attn_fwd(const void *q, const void *k, const void *v,
                      void *stream);
 
 /*
+ * attn_fwd_window -- attn_fwd with a local (sliding-window) band mask.
+ *
+ * Operation: as attn_fwd, with the mask of "Deep Dive - FlashAttention",
+ * section "Causal 2.1 is the decode gotcha", paragraph on local attention:
+ * query row i of a sequence with Nq_b queries and Nk_b keys keeps keys
+ *     i + Nk_b - Nq_b - window_left  <=  j  <=  i + Nk_b - Nq_b + window_right
+ * inside [0, Nk_b); a side of -1 is unbounded; with causal = 1 the causal
+ * corner restricts the set further (which makes window_right irrelevant).
+ * K/V tiles that no row of a query tile keeps are never loaded ("FlashAttention:
+ * Part 1", section 3.5, applied to both band edges), so the cost follows the
+ * band's width rather than Nk.  window_left = window_right = -1 is attn_fwd.
+ * Layout, ownership and every other rule: as attn_fwd.
+ * Rejects (ATTN_ERR_INVALID_ARG) in addition: window_left or window_right < -1.
+ */
+attn_status attn_fwd_window(const void *q, const void *k, const void *v,
+                            void *out, float *lse,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                            float scale, int causal, int window_left, int window_right,
+                            const int *cu_seqlens_q, const int *cu_seqlens_k,
+                            void *stream);
+
+/*
  * attn_decode_paged -- one new query per sequence over a paged K/V cache,
  * split along the keys (split-KV) with a log-sum-exp combine.
  *

@@ -13,7 +13,11 @@ Parity status of each function (what pins it, see ``tests/test_oracle.py``):
                   example (printed values), keep matrices for both causal
                   corners, the GQA head map, torch SDPA fp64 MATH backend with
                   an explicit bottom-right keep mask, shift invariance, the
-                  log-sum-exp merge identity, rows summing to one.
+                  log-sum-exp merge identity, rows summing to one; the local
+                  window through its special cases (unbounded = full, right 0
+                  = causal corner, (0, 0) = the single diagonal key, a window
+                  covering every key = full, left-only window with causal =
+                  causal minus the far keys).
   decode_rows  -- pinned: equals prefill_rows on the keys gathered through the
                   block table as the paged-gather example describes, and the
                   example's gathered shape.
@@ -57,6 +61,8 @@ def _load():
             D = ctypes.c_double
             lib.oracle_prefill_rows.argtypes = [P, P, P, I, I, I, I, I, I, D, I, P, P, P, L, P, P, I]
             lib.oracle_prefill_rows.restype = I
+            lib.oracle_prefill_rows_window.argtypes = [P, P, P, I, I, I, I, I, I, D, I, I, I, P, P, P, L, P, P, I]
+            lib.oracle_prefill_rows_window.restype = I
             lib.oracle_decode_rows.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, L, P, P, I]
             lib.oracle_decode_rows.restype = I
             lib.oracle_num_threads.argtypes = []
@@ -89,10 +95,11 @@ def _ptr(a):
 
 
 def prefill_rows(q, k, v, *, B, Hq, Hkv, Nq, Nk, scale, causal, rows,
-                 cu_q=None, cu_k=None, threads: int = 0):
+                 cu_q=None, cu_k=None, window=(-1, -1), threads: int = 0):
     """Rows (b, h, i) of softmax(QK^T*scale + mask) V and their lse, fp64.
 
-    q [T_q, Hq, d], k/v [T_k, Hkv, d] bf16; rows int [n, 3].
+    q [T_q, Hq, d], k/v [T_k, Hkv, d] bf16; rows int [n, 3]; window =
+    (left, right) local window, -1 = unbounded on that side.
     Returns (out [n, d] float64, lse [n] float64)."""
     d = int(q.shape[-1])
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
@@ -101,10 +108,11 @@ def prefill_rows(q, k, v, *, B, Hq, Hkv, Nq, Nk, scale, causal, rows,
     out = np.zeros((n, d), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
     cq, ck = _i32(cu_q), _i32(cu_k)
-    rc = _load().oracle_prefill_rows(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d,
-                                     float(scale), int(bool(causal)), _ptr(cq), _ptr(ck),
-                                     _ptr(r), n, _ptr(out), _ptr(lse),
-                                     threads if threads > 0 else num_threads())
+    left, right = (int(x) for x in window)
+    rc = _load().oracle_prefill_rows_window(_ptr(qb), _ptr(kb), _ptr(vb), B, Hq, Hkv, Nq, Nk, d,
+                                            float(scale), int(bool(causal)), left, right, _ptr(cq), _ptr(ck),
+                                            _ptr(r), n, _ptr(out), _ptr(lse),
+                                            threads if threads > 0 else num_threads())
     if rc != 0:
         raise ValueError(f"oracle_prefill_rows rejected its arguments (status {rc})")
     return out, lse
@@ -148,7 +156,7 @@ def prefill(p, rows=None, threads: int = 0):
         rows = all_rows(p)
     return prefill_rows(p.q, p.k, p.v, B=p.B, Hq=p.Hq, Hkv=p.Hkv, Nq=p.Nq, Nk=p.Nk,
                         scale=p.scale, causal=p.causal, rows=rows, cu_q=p.cu_q, cu_k=p.cu_k,
-                        threads=threads)
+                        window=getattr(p, "window", (-1, -1)), threads=threads)
 
 
 def decode(p, rows=None, threads: int = 0):

@@ -10,7 +10,9 @@
  * What one output row is (the definition, written out; no tiling and no online
  * recurrence -- two plain passes over the allowed keys):
  *
- *   A_i   = { j : 0 <= j < Nk_b  and  (not causal  or  j <= i + Nk_b - Nq_b) }
+ *   A_i   = { j : 0 <= j < Nk_b  and  (not causal  or  j <= i + Nk_b - Nq_b)
+ *                and (left < 0 or j >= i + Nk_b - Nq_b - left)
+ *                and (right < 0 or j <= i + Nk_b - Nq_b + right) }
  *   s_j   = scale * sum_c q[i,c] * k[j,c]                 for j in A_i
  *   m     = max_{j in A_i} s_j
  *   l     = sum_{j in A_i} exp(s_j - m)
@@ -32,6 +34,9 @@
  *    log-sum-exp merge unchanged);
  *  - keep rule j <= i + Nk - Nq (bottom-right corner): same page, section
  *    "Causal 2.1 is the decode gotcha";
+ *  - local window (left, right): keep i + Nk - Nq - left <= j <= i + Nk - Nq
+ *    + right, a side of -1 being unbounded, intersected with the causal rule
+ *    when both are given: same section, paragraph on local attention;
  *  - query head h reads K/V head h / (Hq / Hkv) (consecutive groups): same
  *    page, section "The public interface is several kernels";
  *  - packed sequences: sequence b owns tokens [cu[b], cu[b+1]), section
@@ -64,11 +69,15 @@ static double bf16_value(uint16_t bits)
 }
 
 /* ---- the mask: is key j allowed for query row i of a (nq, nk) sequence? ---- */
-static int key_allowed(long i, long j, long nq, long nk, int causal)
+static int key_allowed(long i, long j, long nq, long nk, int causal, long left, long right)
 {
     if (j < 0 || j >= nk)
         return 0;
     if (causal && j > i + nk - nq) /* bottom-right aligned corner */
+        return 0;
+    if (left >= 0 && j < i + nk - nq - left) /* local window, left side */
+        return 0;
+    if (right >= 0 && j > i + nk - nq + right) /* local window, right side */
         return 0;
     return 1;
 }
@@ -98,7 +107,7 @@ static const uint16_t *key_row(const key_store *ks, const uint16_t *base, long j
 
 /* ---- one output row, by the definition ---- */
 static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
-                       long i, long nq, long nk, int causal, double scale,
+                       long i, long nq, long nk, int causal, long left, long right, double scale,
                        double *s, double *out, double *lse)
 {
     const int d = ks->d;
@@ -107,7 +116,7 @@ static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
 
     /* pass 1: scores of the allowed keys and their maximum */
     for (long j = 0; j < nk; ++j) {
-        if (!key_allowed(i, j, nq, nk, causal))
+        if (!key_allowed(i, j, nq, nk, causal, left, right))
             continue;
         const uint16_t *k_row = key_row(ks, ks->k, j, g);
         double dot = 0.0;
@@ -129,7 +138,7 @@ static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
     /* pass 2: normaliser and value-weighted sum, relative to the maximum */
     double l = 0.0;
     for (long j = 0; j < nk; ++j) {
-        if (!key_allowed(i, j, nq, nk, causal))
+        if (!key_allowed(i, j, nq, nk, causal, left, right))
             continue;
         double w = exp(s[j] - m);
         l += w;
@@ -147,6 +156,7 @@ typedef struct {
     /* shared inputs */
     const uint16_t *q, *k, *v;
     int B, Hq, Hkv, Nq, Nk, d, causal, paged, page_size, max_pages;
+    long win_left, win_right;
     double scale;
     const int32_t *cu_q, *cu_k, *block_table, *seq_lens;
     const int32_t *rows;   /* prefill: (b, h, i) triples; decode: (b, h) pairs */
@@ -185,7 +195,8 @@ static void run_row(job *jb, long r, double *s)
             nk = jb->Nk;
         }
         const uint16_t *q_row = jb->q + ((q_first + i) * jb->Hq + h) * (long)jb->d;
-        attend_row(q_row, &ks, h / group, i, nq, nk, jb->causal, jb->scale, s, out, lse);
+        attend_row(q_row, &ks, h / group, i, nq, nk, jb->causal, jb->win_left, jb->win_right, jb->scale, s, out,
+                   lse);
     } else {
         int b = jb->rows[2 * r], h = jb->rows[2 * r + 1];
         long len = jb->seq_lens[b];
@@ -194,7 +205,7 @@ static void run_row(job *jb, long r, double *s)
         const uint16_t *q_row = jb->q + ((long)b * jb->Hq + h) * (long)jb->d;
         /* one query per sequence: it is the last position, so under the
          * bottom-right rule it sees every cached key (i = 0, nq = 1). */
-        attend_row(q_row, &ks, h / group, 0, 1, len, 0, jb->scale, s, out, lse);
+        attend_row(q_row, &ks, h / group, 0, 1, len, 0, -1, -1, jb->scale, s, out, lse);
     }
 }
 
@@ -266,12 +277,32 @@ int oracle_num_threads(void)
  * local to sequence b.  out [n_rows, d] and lse [n_rows] in fp64.
  * Returns 0, or -1 for invalid arguments, -2 when out of memory.
  */
+int oracle_prefill_rows_window(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                               double scale, int causal, int win_left, int win_right,
+                               const int32_t *cu_q, const int32_t *cu_k,
+                               const int32_t *rows, long n_rows,
+                               double *out, double *lse, int n_threads);
+
 int oracle_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         int B, int Hq, int Hkv, int Nq, int Nk, int d,
                         double scale, int causal,
                         const int32_t *cu_q, const int32_t *cu_k,
                         const int32_t *rows, long n_rows,
                         double *out, double *lse, int n_threads)
+{
+    return oracle_prefill_rows_window(q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, -1, -1, cu_q, cu_k,
+                                      rows, n_rows, out, lse, n_threads);
+}
+
+/* As oracle_prefill_rows, with a local window (win_left, win_right); -1 on a
+ * side leaves it unbounded. */
+int oracle_prefill_rows_window(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                               int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                               double scale, int causal, int win_left, int win_right,
+                               const int32_t *cu_q, const int32_t *cu_k,
+                               const int32_t *rows, long n_rows,
+                               double *out, double *lse, int n_threads)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || n_rows < 0)
         return -1;
@@ -294,6 +325,8 @@ int oracle_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     jb.q = q; jb.k = k; jb.v = v;
     jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.Nq = Nq; jb.Nk = Nk; jb.d = d;
     jb.causal = causal; jb.scale = scale;
+    jb.win_left = win_left < 0 ? -1 : win_left;
+    jb.win_right = win_right < 0 ? -1 : win_right;
     jb.cu_q = cu_q; jb.cu_k = cu_k;
     jb.rows = rows; jb.n_rows = n_rows;
     jb.out = out; jb.lse = lse;

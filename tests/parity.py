@@ -9,6 +9,9 @@ Which keys are attended is checked bit-exactly (one-hot tests).
 import numpy as np
 import torch
 
+import oracle
+import workloads
+
 O_MAX_ABS = 1e-2
 O_REL_RMS = 5e-3
 LSE_ABS = 1e-3
@@ -55,16 +58,39 @@ def gather_prefill(p, out, lse, rows):
 def run_prefill(la, p, device="cuda"):
     """attn_fwd on a workloads.Prefill problem; returns (out, lse) on device."""
     g = p.to(device)
+    window = None if tuple(p.window) == (-1, -1) else tuple(p.window)
     if p.varlen:
-        return la.attn_fwd(g.q, g.k, g.v, causal=p.causal, scale=p.scale,
+        return la.attn_fwd(g.q, g.k, g.v, causal=p.causal, scale=p.scale, window=window,
                            cu_seqlens_q=g.cu_q, cu_seqlens_k=g.cu_k)
     q = g.q.view(p.B, p.Nq, p.Hq, p.d)
     k = g.k.view(p.B, p.Nk, p.Hkv, p.d)
     v = g.v.view(p.B, p.Nk, p.Hkv, p.d)
-    return la.attn_fwd(q, k, v, causal=p.causal, scale=p.scale)
+    return la.attn_fwd(q, k, v, causal=p.causal, scale=p.scale, window=window)
 
 
 def run_decode(la, d, device="cuda", num_splits=0):
     g = d.to(device)
     return la.attn_decode_paged(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, scale=d.scale,
                                 num_splits=num_splits)
+
+
+def one_hot_check(la, p, bases):
+    """Q = 0 and V one-hot over a window of d keys: the nonzero pattern of O
+    must equal the oracle's allowed set exactly, the magnitude must name the
+    K/V head, and exp(lse) must be the allowed-key count."""
+    for base in bases:
+        ph = workloads.one_hot_values(p, base)
+        out, lse = run_prefill(la, ph)
+        torch.cuda.synchronize()
+        rows = oracle.all_rows(ph)
+        ref_o, ref_lse = oracle.prefill(ph, rows)
+        go, gl = gather_prefill(ph, out, lse, rows)
+        assert np.array_equal(go != 0, ref_o != 0), f"base {base}: attended-key pattern differs"
+        cnt = np.where(np.isfinite(ref_lse), np.rint(np.exp(ref_lse)), 0)
+        g_of_h = (rows[:, 1] // (p.Hq // p.Hkv)) + 1
+        nz = go != 0
+        assert np.array_equal(np.rint((go * cnt[:, None])[nz]), np.broadcast_to(g_of_h[:, None], go.shape)[nz]), \
+            f"base {base}: K/V head map differs"
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(gl), fin)
+        assert np.array_equal(np.rint(np.exp(gl[fin])), cnt[fin]), f"base {base}: allowed-key count differs"

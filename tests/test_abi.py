@@ -68,6 +68,16 @@ def test_fwd_host_rejections(lib):
     assert fwd(lib, Nq=0) == 0
 
 
+def test_fwd_window_host_rejections(lib):
+    def w(left, right, Nq=8):
+        return lib.attn_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, Nq, 8, 128, 0.1, 0, left, right,
+                                   None, None, None)
+    assert w(-2, 0) == -1
+    assert w(0, -7) == -1
+    assert w(-1, -1, Nq=0) == 0                      # valid window, nothing to do
+    assert w(5, 0, Nq=0) == 0
+
+
 def dec(lib, ws_bytes=1 << 30, B=2, Hq=8, Hkv=2, d=128, page=16, num_pages=10, max_pages=4, splits=0,
         scale=0.1, ws=ctypes.c_void_p(0x10000), bt=FAKE):
     return lib.attn_decode_paged(FAKE, FAKE, FAKE, bt, max_pages, FAKE, FAKE, FAKE, B, Hq, Hkv, d, page,

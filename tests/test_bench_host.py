@@ -24,6 +24,19 @@ def test_attended_pairs_brute_force(nq, nk, causal):
     assert bench.attended_pairs(p) == brute
 
 
+@pytest.mark.parametrize("nq,nk,causal,window", [(7, 7, True, (2, -1)), (5, 9, False, (1, 2)),
+                                                 (9, 5, False, (0, 0)), (300, 700, True, (128, 5)),
+                                                 (40, 40, False, (-1, 3)), (3, 50, False, (60, 60))])
+def test_attended_pairs_window_brute_force(nq, nk, causal, window):
+    p = workloads.make_prefill(1, 2, 1, nq, nk, 8, causal=causal, seed=1, window=window)
+    left, right = window
+    def keep(i, j):
+        c = i + nk - nq
+        return ((not causal or j <= c) and (left < 0 or j >= c - left) and (right < 0 or j <= c + right))
+    brute = 2 * sum(1 for i in range(nq) for j in range(nk) if keep(i, j))
+    assert bench.attended_pairs(p) == brute
+
+
 def test_mha_causal_flops():
     p = workloads.make_prefill(4, 16, 16, 4096, 4096, 128, causal=True, seed=1)
     assert bench.prefill_flops(p) == 4 * 128 * 64 * 4096 * 4097 // 2

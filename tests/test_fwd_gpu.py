@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads
-from parity import assert_close, gather_prefill, run_prefill
+from parity import assert_close, gather_prefill, one_hot_check, run_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -78,28 +78,6 @@ def test_no_keys_gives_zero_rows(la):
 
 
 # ---------------------------------------------------------------- one-hot: which keys are attended
-def one_hot_check(la, p, bases):
-    """Q = 0 and V one-hot over a window of d keys: the nonzero pattern of O
-    must equal the oracle's allowed set exactly, the magnitude must name the
-    K/V head, and exp(lse) must be the allowed-key count."""
-    for base in bases:
-        ph = workloads.one_hot_values(p, base)
-        out, lse = run_prefill(la, ph)
-        torch.cuda.synchronize()
-        rows = oracle.all_rows(ph)
-        ref_o, ref_lse = oracle.prefill(ph, rows)
-        go, gl = gather_prefill(ph, out, lse, rows)
-        assert np.array_equal(go != 0, ref_o != 0), f"base {base}: attended-key pattern differs"
-        cnt = np.where(np.isfinite(ref_lse), np.rint(np.exp(ref_lse)), 0)
-        g_of_h = (rows[:, 1] // (p.Hq // p.Hkv)) + 1
-        nz = go != 0
-        assert np.array_equal(np.rint((go * cnt[:, None])[nz]), np.broadcast_to(g_of_h[:, None], go.shape)[nz]), \
-            f"base {base}: K/V head map differs"
-        fin = np.isfinite(ref_lse)
-        assert np.array_equal(np.isfinite(gl), fin)
-        assert np.array_equal(np.rint(np.exp(gl[fin])), cnt[fin]), f"base {base}: allowed-key count differs"
-
-
 def test_one_hot_tiny_all_windows(la):
     for causal in (False, True):
         p = workloads.tiny(causal)

@@ -141,7 +141,7 @@ def test_empty_rows_and_single_key_rows():
 # ---------------------------------------------------------------------------
 # mask corner and head map, read off the oracle's outputs
 # ---------------------------------------------------------------------------
-def keep_matrix(nq, nk, causal):
+def keep_matrix(nq, nk, causal, window=(-1, -1)):
     """Q = 0, V = identity on keys: O[i, c] > 0 exactly when key c is allowed."""
     d = max(nk, 2)
     q = torch.zeros(nq, 1, d)
@@ -150,7 +150,8 @@ def keep_matrix(nq, nk, causal):
     for j in range(nk):
         v[j, 0, j] = 1.0
     out, lse = oracle.prefill_rows(bf16(q), bf16(k), bf16(v), B=1, Hq=1, Hkv=1, Nq=nq, Nk=nk,
-                                   scale=1.0, causal=causal, rows=[[0, 0, i] for i in range(nq)])
+                                   scale=1.0, causal=causal, rows=[[0, 0, i] for i in range(nq)],
+                                   window=window)
     keep = (out[:, :nk] > 0).astype(int)
     # each allowed key carries weight 1/|A_i| exactly; lse = ln|A_i|
     for i in range(nq):
@@ -171,6 +172,56 @@ def test_bottom_right_keep_matrices():
     for case in g["top_left"]:
         assert keep_matrix(case["q"], case["k"], causal=True) != case["keep"]
     assert keep_matrix(2, 5, causal=False) == [[1] * 5] * 2
+
+
+def test_local_window_special_cases():
+    """The local window reduces to masks fixed elsewhere: no window is the full
+    matrix, right = 0 alone is the printed bottom-right causal corner, (0, 0)
+    keeps only the corner diagonal key, and a window wider than the keys
+    changes nothing."""
+    g = golden("local_window.json")
+    printed = {(c["q"], c["k"]): c["keep"] for c in golden("causal_keep.json")["bottom_right"]}
+    for nq, nk in g["shapes"]:
+        full = [[1] * nk for _ in range(nq)]
+        corner = keep_matrix(nq, nk, causal=True)
+        diag = [[int(j == i + nk - nq) for j in range(nk)] for i in range(nq)]
+        want = {"full": full, "bottom_right_causal": corner, "diagonal": diag}
+        for red in g["reductions"]:
+            got = keep_matrix(nq, nk, causal=red["causal"], window=tuple(red["window"]))
+            assert got == want[red["equals"]], (nq, nk, red)
+        if (nq, nk) in printed:
+            assert keep_matrix(nq, nk, causal=False, window=(-1, 0)) == printed[(nq, nk)]
+        wide = nq + nk
+        assert keep_matrix(nq, nk, causal=False, window=(wide, wide)) == full
+        assert keep_matrix(nq, nk, causal=True, window=(wide, wide)) == corner
+
+
+def test_local_window_sides_compose_and_grow_by_one_key():
+    """Each side acts alone: the (left, right) set is the intersection of the
+    (left, -1) and (-1, right) sets (and of the causal set when causal), and
+    widening one side by one adds exactly the single key just outside it."""
+    for nq, nk in [(5, 9), (9, 5), (7, 7), (1, 6)]:
+        for left in range(0, 5):
+            for right in range(0, 5):
+                both = np.array(keep_matrix(nq, nk, False, (left, right)))
+                lonly = np.array(keep_matrix(nq, nk, False, (left, -1)))
+                ronly = np.array(keep_matrix(nq, nk, False, (-1, right)))
+                assert (both == (lonly & ronly)).all()
+                caus = np.array(keep_matrix(nq, nk, True, (left, right)))
+                assert (caus == (both & np.array(keep_matrix(nq, nk, True)))).all()
+                wider_l = np.array(keep_matrix(nq, nk, False, (left + 1, right)))
+                wider_r = np.array(keep_matrix(nq, nk, False, (left, right + 1)))
+                dl, dr = wider_l - both, wider_r - both
+                assert dl.min() >= 0 and dr.min() >= 0
+                for i in range(nq):
+                    assert dl[i].sum() <= 1 and dr[i].sum() <= 1
+                    if dl[i].sum():   # the added key sits just left of the row's leftmost kept key
+                        j = int(np.argmax(dl[i]))
+                        assert both[i, j + 1: j + 2].tolist() == [1] or not both[i].any()
+                        assert not both[i, :j + 1].any()
+                    if dr[i].sum():
+                        j = int(np.argmax(dr[i]))
+                        assert not both[i, j:].any()
 
 
 def test_gqa_head_map():
@@ -197,16 +248,19 @@ def test_gqa_head_map():
 # ---------------------------------------------------------------------------
 # against a library routine: torch SDPA, fp64 MATH backend, explicit mask
 # ---------------------------------------------------------------------------
-def sdpa_reference(q, k, v, nq, nk, hq, hkv, scale, causal):
-    """q [nq, hq, d], k/v [nk, hkv, d] -> (out [hq, nq, d], lse [hq, nq]) in fp64."""
+def sdpa_reference(q, k, v, nq, nk, hq, hkv, scale, causal, keep=None):
+    """q [nq, hq, d], k/v [nk, hkv, d] -> (out [hq, nq, d], lse [hq, nq]) in fp64.
+    keep, when given, is the boolean [nq, nk] mask to use instead of the
+    causal corner."""
     from torch.nn.attention import SDPBackend, sdpa_kernel
     import torch.nn.functional as F
     qd = q.double().permute(1, 0, 2)[None]
     kd = k.double().permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)[None]
     vd = v.double().permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)[None]
-    keep = torch.ones(nq, nk, dtype=torch.bool)
-    if causal:
-        keep = torch.arange(nk)[None, :] <= torch.arange(nq)[:, None] + nk - nq
+    if keep is None:
+        keep = torch.ones(nq, nk, dtype=torch.bool)
+        if causal:
+            keep = torch.arange(nk)[None, :] <= torch.arange(nq)[:, None] + nk - nq
     with sdpa_kernel(SDPBackend.MATH):
         out = F.scaled_dot_product_attention(qd, kd, vd, attn_mask=keep, is_causal=False,
                                              dropout_p=0.0, scale=scale)[0]
@@ -233,6 +287,41 @@ def test_matches_sdpa_fp64(nq, nk, hq, hkv, d, causal):
         if has_key[i]:
             assert np.abs(out[r] - ref[h, i].numpy()).max() <= 1e-12
             assert abs(lse[r] - float(ref_lse[h, i])) <= 1e-12
+        else:
+            assert (out[r] == 0).all() and np.isneginf(lse[r])
+
+
+@pytest.mark.parametrize("nq,nk,left,right,causal", [
+    (16, 40, 5, 0, True), (40, 16, 3, 2, False), (33, 33, 8, -1, True), (20, 50, -1, 7, False),
+    (24, 24, 0, 0, False), (12, 70, 10, 3, True),
+])
+def test_local_window_matches_sdpa_fp64_with_band_mask(nq, nk, left, right, causal):
+    """Random data through SDPA (fp64 MATH backend) with the keep mask built
+    from the page's statement of the window as a boolean band; rows with no
+    key return 0 and -inf."""
+    torch.manual_seed(nq * 1000 + nk * 7 + left)
+    hq, hkv, d = 4, 2, 16
+    q, k, v = bf16(torch.randn(nq, hq, d)), bf16(torch.randn(nk, hkv, d)), bf16(torch.randn(nk, hkv, d))
+    scale = 1.0 / math.sqrt(d)
+    i = torch.arange(nq)[:, None]
+    j = torch.arange(nk)[None, :]
+    centre = i + nk - nq
+    keep = torch.ones(nq, nk, dtype=torch.bool)
+    if left >= 0:
+        keep &= j >= centre - left
+    if right >= 0:
+        keep &= j <= centre + right
+    if causal:
+        keep &= j <= centre
+    rows = [[0, h, r] for h in range(hq) for r in range(nq)]
+    out, lse = oracle.prefill_rows(q, k, v, B=1, Hq=hq, Hkv=hkv, Nq=nq, Nk=nk, scale=scale,
+                                   causal=causal, rows=rows, window=(left, right))
+    ref, ref_lse, keep = sdpa_reference(q, k, v, nq, nk, hq, hkv, scale, causal, keep=keep)
+    has_key = keep.any(dim=-1)
+    for r, (_, h, ii) in enumerate(rows):
+        if has_key[ii]:
+            assert np.abs(out[r] - ref[h, ii].numpy()).max() <= 1e-12
+            assert abs(lse[r] - float(ref_lse[h, ii])) <= 1e-12
         else:
             assert (out[r] == 0).all() and np.isneginf(lse[r])
 

@@ -24,6 +24,9 @@ MUTATIONS = {
     "normaliser perturbed": ("out[c] /= l;", "out[c] /= (l + 1e-13);"),
     "scale dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
     "empty row lse zero": ("*lse = -INFINITY;\n        return;", "*lse = 0.0;\n        return;"),
+    "window left side off by one": ("j < i + nk - nq - left)", "j <= i + nk - nq - left)"),
+    "window right side mirrored": ("j > i + nk - nq + right)", "j > i + nk - nq - right)"),
+    "window measured from the top-left": ("j < i + nk - nq - left)", "j < i - left)"),
 }
 
 

@@ -83,6 +83,7 @@ class Prefill:
     cu_q: Optional[torch.Tensor] = None  # int32 [B+1] or None (dense)
     cu_k: Optional[torch.Tensor] = None
     seed: int = 0
+    window: tuple = (-1, -1)   # local window (left, right) in keys, -1 = unbounded
 
     @property
     def varlen(self) -> bool:
@@ -103,17 +104,17 @@ class Prefill:
 
 
 def make_prefill(B, Hq, Hkv, Nq, Nk, d, *, causal, seed, scale=None, name="custom",
-                 device="cpu") -> Prefill:
+                 device="cpu", window=(-1, -1)) -> Prefill:
     """Dense problem: B sequences of Nq queries over Nk keys."""
     q = randn_bf16((B * Nq, Hq, d), seed * 7 + 1, device)
     k = randn_bf16((B * Nk, Hkv, d), seed * 7 + 2, device)
     v = randn_bf16((B * Nk, Hkv, d), seed * 7 + 3, device)
     return Prefill(name, q, k, v, B, Hq, Hkv, Nq, Nk, d,
-                   1.0 / math.sqrt(d) if scale is None else scale, causal, seed=seed)
+                   1.0 / math.sqrt(d) if scale is None else scale, causal, seed=seed, window=tuple(window))
 
 
 def make_varlen(q_lens, k_lens, Hq, Hkv, d, *, causal, seed, scale=None, name="varlen",
-                device="cpu") -> Prefill:
+                device="cpu", window=(-1, -1)) -> Prefill:
     """Packed problem: sequence b has q_lens[b] queries and k_lens[b] keys."""
     q_lens = [int(x) for x in q_lens]
     k_lens = [int(x) for x in k_lens]
@@ -126,7 +127,7 @@ def make_varlen(q_lens, k_lens, Hq, Hkv, d, *, causal, seed, scale=None, name="v
     v = randn_bf16((max(Tk, 1), Hkv, d), seed * 7 + 3, device)[:Tk]
     return Prefill(name, q, k, v, B, Hq, Hkv, max(q_lens + [0]), max(k_lens + [0]), d,
                    1.0 / math.sqrt(d) if scale is None else scale, causal,
-                   cu_q=cu_q.to(device), cu_k=cu_k.to(device), seed=seed)
+                   cu_q=cu_q.to(device), cu_k=cu_k.to(device), seed=seed, window=tuple(window))
 
 
 def _cumsum(xs):
@@ -156,6 +157,14 @@ def gqa_causal(device="cpu") -> Prefill:
     c_star = gqa_hot_channel(p.d)
     p.k[:, :, c_star] = p.k[:, :, c_star] * 3
     return p
+
+
+def swa_causal(device="cpu") -> Prefill:
+    """Sliding-window prefill: B=2, Hq=32, Hkv=8, N=16384, d=128, causal with
+    a 4096-key window (window (4095, 0): each query sees itself and the 4095
+    keys before it)."""
+    return make_prefill(2, 32, 8, 16384, 16384, 128, causal=True, seed=SEED_BASE + 6,
+                        name="swa_causal_b2_hq32_hkv8_n16384_w4096_d128", device=device, window=(4095, 0))
 
 
 def gqa_hot_channel(d: int) -> int:
