@@ -21,6 +21,12 @@ Parity status of each function (what pins it, see ``tests/test_oracle.py``):
   decode_rows  -- pinned: equals prefill_rows on the keys gathered through the
                   block table as the paged-gather example describes, and the
                   example's gathered shape.
+  decode_multi_rows -- pinned: Nq = 1 equals decode_rows; the printed
+                  bottom-right keep matrices read through a paged cache; equals
+                  prefill_rows (bottom-right causal, Nq queries) on the
+                  gathered keys.
+  append_kv    -- pinned: brute-force gather of the written positions through
+                  the block table; untouched slots keep their bytes.
 """
 from __future__ import annotations
 
@@ -65,6 +71,8 @@ def _load():
             lib.oracle_prefill_rows_window.restype = I
             lib.oracle_decode_rows.argtypes = [P, P, P, P, I, P, I, I, I, I, I, D, P, L, P, P, I]
             lib.oracle_decode_rows.restype = I
+            lib.oracle_decode_multi_rows.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, D, I, P, L, P, P, I]
+            lib.oracle_decode_multi_rows.restype = I
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -165,3 +173,62 @@ def decode(p, rows=None, threads: int = 0):
         rows = np.asarray([(b, h) for b in range(p.B) for h in range(p.Hq)], dtype=np.int32)
     return decode_rows(p.q, p.k_cache, p.v_cache, p.block_table, p.seq_lens, scale=p.scale,
                        rows=rows, threads=threads)
+
+
+def decode_multi_rows(q, k_cache, v_cache, block_table, seq_lens, *, scale, causal, rows, threads: int = 0):
+    """Rows (b, h, i) of Nq-query paged attention, fp64.
+
+    q [B, Nq, Hq, d] (query i of sequence b is position seq_lens[b] - Nq + i);
+    caches [num_pages, page, Hkv, d]; rows int [n, 3].  Returns (out [n, d], lse [n])."""
+    B, Nq, Hq, d = (int(x) for x in q.shape)
+    page, Hkv = int(k_cache.shape[1]), int(k_cache.shape[2])
+    qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    r = _i32(rows).reshape(-1, 3)
+    n = r.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    rc = _load().oracle_decode_multi_rows(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(bt), int(bt.shape[1]),
+                                          _ptr(sl), B, Nq, Hq, Hkv, d, page, float(scale), int(bool(causal)),
+                                          _ptr(r), n, _ptr(out), _ptr(lse),
+                                          threads if threads > 0 else num_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_decode_multi_rows rejected its arguments (status {rc})")
+    return out, lse
+
+
+def append_kv(k_cache, v_cache, block_table, seq_lens, k_new, v_new):
+    """The in-place cache update, on copies: new row i of sequence b goes to
+    position seq_lens[b] - Nq + i, i.e. page block_table[b][pos // page] at
+    slot pos % page.  Positions below zero, and page ids outside the pool, are
+    skipped.  k_new/v_new [B, Nq, Hkv, d].  Returns (k_cache', v_cache')."""
+    kc, vc = k_cache.clone(), v_cache.clone()
+    B, Nq = int(k_new.shape[0]), int(k_new.shape[1])
+    page, pool = int(kc.shape[1]), int(kc.shape[0])
+    bt = block_table.cpu()
+    lens = [int(x) for x in seq_lens.cpu().tolist()]
+    for b in range(B):
+        for i in range(Nq):
+            pos = lens[b] - Nq + i
+            if pos < 0 or pos // page >= bt.shape[1]:
+                continue
+            pg = int(bt[b, pos // page])
+            if 0 <= pg < pool:
+                kc[pg, pos % page] = k_new[b, i]
+                vc[pg, pos % page] = v_new[b, i]
+    return kc, vc
+
+
+def decode_kvcache(p, rows=None, threads: int = 0):
+    """decode_multi_rows over a workloads.KVCacheDecode problem, on the cache
+    after its append (all (b, h, i) rows by default)."""
+    kc, vc = p.k_cache, p.v_cache
+    if p.k_new is not None:
+        kc, vc = append_kv(kc, vc, p.block_table, p.seq_lens, p.k_new, p.v_new)
+    if rows is None:
+        rows = np.asarray([(b, h, i) for b in range(p.B) for h in range(p.Hq) for i in range(p.Nq)],
+                          dtype=np.int32)
+    return decode_multi_rows(p.q, kc, vc, p.block_table, p.seq_lens, scale=p.scale, causal=p.causal,
+                             rows=rows, threads=threads)
+

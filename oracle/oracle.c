@@ -44,7 +44,11 @@
  *  - paged keys: logical token t of sequence b sits in physical page
  *    block_table[b][t / page] at slot t % page: "FlashAttention-3 and
  *    PagedAttention", sections "Block tables and what the kernel does" and
- *    "Runnable Example: Measuring the IO Gap" (the block-table gather).
+ *    "Runnable Example: Measuring the IO Gap" (the block-table gather);
+ *  - several new queries per sequence over the paged cache: query i of Nq is
+ *    the position len - Nq + i and takes the bottom-right rule with Nq
+ *    queries and len keys ("Deep Dive - FlashAttention", sections "Causal 2.1
+ *    is the decode gotcha" and "Paged KV is a lookup, not a cache manager").
  *
  * Inputs are bf16 bit patterns (uint16); each is widened exactly to double.
  * Threads: POSIX threads over output rows; each row is computed by one thread
@@ -197,7 +201,7 @@ static void run_row(job *jb, long r, double *s)
         const uint16_t *q_row = jb->q + ((q_first + i) * jb->Hq + h) * (long)jb->d;
         attend_row(q_row, &ks, h / group, i, nq, nk, jb->causal, jb->win_left, jb->win_right, jb->scale, s, out,
                    lse);
-    } else {
+    } else if (jb->paged == 1) {
         int b = jb->rows[2 * r], h = jb->rows[2 * r + 1];
         long len = jb->seq_lens[b];
         ks.pages = jb->block_table + (long)b * jb->max_pages;
@@ -206,6 +210,16 @@ static void run_row(job *jb, long r, double *s)
         /* one query per sequence: it is the last position, so under the
          * bottom-right rule it sees every cached key (i = 0, nq = 1). */
         attend_row(q_row, &ks, h / group, 0, 1, len, 0, -1, -1, jb->scale, s, out, lse);
+    } else {
+        /* Nq queries per sequence over the paged cache: query i is position
+         * len - Nq + i, so under the bottom-right rule (with causal) it sees
+         * keys j <= i + len - Nq; without causal it sees all len keys. */
+        int b = jb->rows[3 * r], h = jb->rows[3 * r + 1], i = jb->rows[3 * r + 2];
+        long len = jb->seq_lens[b];
+        ks.pages = jb->block_table + (long)b * jb->max_pages;
+        ks.page_size = jb->page_size;
+        const uint16_t *q_row = jb->q + (((long)b * jb->Nq + i) * jb->Hq + h) * (long)jb->d;
+        attend_row(q_row, &ks, h / group, i, jb->Nq, len, jb->causal, -1, -1, jb->scale, s, out, lse);
     }
 }
 
@@ -363,6 +377,45 @@ int oracle_decode_rows(const uint16_t *q, const uint16_t *k_cache, const uint16_
     jb.q = q; jb.k = k_cache; jb.v = v_cache;
     jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.d = d;
     jb.paged = 1; jb.page_size = page_size; jb.max_pages = max_pages;
+    jb.scale = scale;
+    jb.block_table = block_table; jb.seq_lens = seq_lens;
+    jb.rows = rows; jb.n_rows = n_rows;
+    jb.out = out; jb.lse = lse;
+    jb.max_keys = max_keys;
+    return run_job(&jb, n_threads);
+}
+
+/*
+ * Several queries per sequence over the paged cache.  q [B, Nq, Hq, d] (query
+ * i of sequence b is its position seq_lens[b] - Nq + i); caches and block
+ * table as oracle_decode_rows; rows: n_rows triples (b, h, i).
+ * Returns 0, or -1 for invalid arguments, -2 when out of memory.
+ */
+int oracle_decode_multi_rows(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                             const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                             int B, int Nq, int Hq, int Hkv, int d, int page_size, double scale, int causal,
+                             const int32_t *rows, long n_rows,
+                             double *out, double *lse, int n_threads)
+{
+    if (B < 0 || Nq <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || page_size <= 0 || n_rows < 0)
+        return -1;
+    long max_keys = 1;
+    for (long r = 0; r < n_rows; ++r) {
+        int b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= Nq)
+            return -1;
+        long len = seq_lens[b];
+        if (len < 0 || len > (long)max_pages * page_size)
+            return -1;
+        if (len > max_keys)
+            max_keys = len;
+    }
+    job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k_cache; jb.v = v_cache;
+    jb.B = B; jb.Nq = Nq; jb.Hq = Hq; jb.Hkv = Hkv; jb.d = d;
+    jb.causal = causal ? 1 : 0;
+    jb.paged = 2; jb.page_size = page_size; jb.max_pages = max_pages;
     jb.scale = scale;
     jb.block_table = block_table; jb.seq_lens = seq_lens;
     jb.rows = rows; jb.n_rows = n_rows;

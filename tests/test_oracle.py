@@ -457,6 +457,107 @@ def test_decode_equals_dense_on_gathered_keys():
             r += 1
 
 
+def test_decode_multi_with_one_query_equals_decode():
+    p = workloads.make_decode([40, 17, 1, 0, 33], 4, 2, 16, num_pages=14, seed=8, nan_fill_unused=True,
+                              max_pages=4)
+    o1, l1 = oracle.decode(p)
+    rows = np.asarray([(b, h, 0) for b in range(p.B) for h in range(p.Hq)], dtype=np.int32)
+    for causal in (False, True):
+        o2, l2 = oracle.decode_multi_rows(p.q[:, None], p.k_cache, p.v_cache, p.block_table, p.seq_lens,
+                                          scale=p.scale, causal=causal, rows=rows)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def _paged_one_hot(lens, nq, page):
+    """Q = 0 and V one-hot by logical token over a shuffled paged pool."""
+    need = [-(-L // page) for L in lens]
+    n_pages = sum(need) + 3
+    perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(5)).tolist()
+    width = max(lens)
+    table = torch.full((len(lens), max(need)), -1, dtype=torch.int32)
+    kc = torch.zeros(n_pages, page, 1, width)
+    vc = torch.full((n_pages, page, 1, width), float("nan"))
+    pos = 0
+    for b, L in enumerate(lens):
+        for pi in range(need[b]):
+            pg = perm[pos]
+            pos += 1
+            table[b, pi] = pg
+            vc[pg] = 0.0
+            for s in range(page):
+                t = pi * page + s
+                if t < L:
+                    vc[pg, s, 0, t] = 1.0
+    q = torch.zeros(len(lens), nq, 1, width)
+    return bf16(q), bf16(kc), bf16(vc), table, torch.tensor(lens, dtype=torch.int32)
+
+
+def test_decode_multi_printed_keep_matrices():
+    """The printed bottom-right keep matrices, read through a paged cache:
+    Nq new queries over a sequence of Nk cached keys."""
+    g = golden("causal_keep.json")
+    for case in g["bottom_right"]:
+        nq, nk = case["q"], case["k"]
+        q, kc, vc, table, lens = _paged_one_hot([nk], nq, page=2)
+        rows = [[0, 0, i] for i in range(nq)]
+        out, lse = oracle.decode_multi_rows(q, kc, vc, table, lens, scale=1.0, causal=True, rows=rows)
+        keep = (out[:, :nk] > 0).astype(int).tolist()
+        assert keep == case["keep"]
+        out, _ = oracle.decode_multi_rows(q, kc, vc, table, lens, scale=1.0, causal=False, rows=rows)
+        assert (out[:, :nk] > 0).all()
+
+
+def test_decode_multi_equals_prefill_on_gathered_keys():
+    lens = [40, 3, 1, 33, 16]
+    nq = 3
+    p = workloads.make_decode(lens, 4, 2, 16, num_pages=14, seed=9, nan_fill_unused=True, max_pages=4)
+    q = bf16(torch.randn(p.B, nq, p.Hq, p.d, generator=torch.Generator().manual_seed(3)))
+    rows = np.asarray([(b, h, i) for b in range(p.B) for h in range(p.Hq) for i in range(nq)], dtype=np.int32)
+    for causal in (True, False):
+        out, lse = oracle.decode_multi_rows(q, p.k_cache, p.v_cache, p.block_table, p.seq_lens, scale=p.scale,
+                                            causal=causal, rows=rows)
+        for r, (b, h, i) in enumerate(rows):
+            L = lens[b]
+            table = p.block_table[b, :-(-L // p.page_size)].tolist()
+            kk = paged_gather(p.k_cache, table, L)
+            vv = paged_gather(p.v_cache, table, L)
+            o, l = oracle.prefill_rows(q[b], kk, vv, B=1, Hq=p.Hq, Hkv=p.Hkv, Nq=nq, Nk=L, scale=p.scale,
+                                       causal=causal, rows=[[0, h, i]])
+            assert np.array_equal(out[r], o[0]) and (lse[r] == l[0] or (np.isneginf(lse[r]) and np.isneginf(l[0])))
+
+
+def test_append_kv_writes_exactly_the_new_positions():
+    """Brute force: after the append, position L - Nq + i of sequence b, looked
+    up through the block table, holds new row i; every other slot keeps its
+    bytes; positions below zero and page ids outside the pool are skipped."""
+    lens = [40, 2, 17, 0]
+    nq = 3
+    p = workloads.make_decode(lens, 4, 2, 16, num_pages=10, seed=10, max_pages=4)
+    g = torch.Generator().manual_seed(4)
+    k_new = bf16(torch.randn(p.B, nq, p.Hkv, p.d, generator=g))
+    v_new = bf16(torch.randn(p.B, nq, p.Hkv, p.d, generator=g))
+    bt = p.block_table.clone()
+    bt[2, 1] = 10_000    # position 16 of sequence 2 lives in a page outside the pool
+    kc, vc = oracle.append_kv(p.k_cache, p.v_cache, bt, p.seq_lens, k_new, v_new)
+    written = set()
+    for b, L in enumerate(lens):
+        for i in range(nq):
+            pos = L - nq + i
+            if pos < 0:
+                continue
+            pg = int(bt[b, pos // 16])
+            if not 0 <= pg < p.num_pages:
+                continue
+            written.add((pg, pos % 16))
+            assert torch.equal(kc[pg, pos % 16], k_new[b, i]) and torch.equal(vc[pg, pos % 16], v_new[b, i])
+    # 3 + 2 (one position of sequence 1 is negative) + 2 (position 16 of sequence 2 is skipped) + 0
+    assert len(written) == 7
+    mask = torch.ones(p.num_pages, 16, dtype=torch.bool)
+    for pg, s in written:
+        mask[pg, s] = False
+    assert torch.equal(kc[mask], p.k_cache[mask]) and torch.equal(vc[mask], p.v_cache[mask])
+
+
 def test_thread_count_does_not_change_results():
     p = workloads.make_prefill(2, 4, 2, 37, 70, 16, causal=True, seed=9)
     a = oracle.prefill(p, threads=1)

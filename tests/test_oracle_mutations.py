@@ -27,6 +27,10 @@ MUTATIONS = {
     "window left side off by one": ("j < i + nk - nq - left)", "j <= i + nk - nq - left)"),
     "window right side mirrored": ("j > i + nk - nq + right)", "j > i + nk - nq - right)"),
     "window measured from the top-left": ("j < i + nk - nq - left)", "j < i - left)"),
+    "multi-query decode reads query 0 for every row": ("(((long)b * jb->Nq + i) * jb->Hq + h)",
+                                                        "(((long)b * jb->Nq) * jb->Hq + h)"),
+    "multi-query decode ignores causal": ("attend_row(q_row, &ks, h / group, i, jb->Nq, len, jb->causal,",
+                                          "attend_row(q_row, &ks, h / group, i, jb->Nq, len, 0,"),
 }
 
 

@@ -24,7 +24,8 @@ tiny (B1 H2 N256 d64), MHA causal (B4 H16 N4096 d128), GQA causal
 (B2 Hq32 Hkv8 N8192 d128, one K channel x3), varlen chunked prefill
 (16 sequences, Nk ~ U[1024, 16384], Nq = min(512, Nk)) and paged split-KV
 decode (B64 Hq32 Hkv8 d128, len ~ U[4096, 32768], 16-token pages in a
-200k-page pool).
+200k-page pool); beyond those, a sliding-window prefill and a four-query
+speculative decode step over the paged cache with an in-place append.
 """
 from __future__ import annotations
 
@@ -273,6 +274,79 @@ def paged_decode(device="cpu", nan_fill_unused=False) -> Decode:
     return make_decode(lens, 32, 8, 128, num_pages=200_000, seed=SEED_BASE + 4, page_size=16,
                        max_pages=2048, nan_fill_unused=nan_fill_unused,
                        name="paged_decode_b64_hq32_hkv8_d128", device=device)
+
+
+@dataclasses.dataclass
+class KVCacheDecode:
+    """Nq new queries per sequence over a paged cache, with the new tokens'
+    K/V appended in place first (k_new None: no append).  seq_lens counts the
+    tokens after the append; query i of sequence b is position
+    seq_lens[b] - Nq + i."""
+    name: str
+    q: torch.Tensor            # [B, Nq, Hq, d]
+    k_new: Optional[torch.Tensor]  # [B, Nq, Hkv, d] or None
+    v_new: Optional[torch.Tensor]
+    k_cache: torch.Tensor      # [P, page, Hkv, d]
+    v_cache: torch.Tensor
+    block_table: torch.Tensor  # int32 [B, max_pages]
+    seq_lens: torch.Tensor     # int32 [B]
+    B: int
+    Nq: int
+    Hq: int
+    Hkv: int
+    d: int
+    page_size: int
+    num_pages: int
+    scale: float
+    causal: bool
+    seed: int = 0
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+    def to(self, device) -> "KVCacheDecode":
+        f = lambda t: None if t is None else t.to(device)
+        return dataclasses.replace(self, q=f(self.q), k_new=f(self.k_new), v_new=f(self.v_new),
+                                   k_cache=f(self.k_cache), v_cache=f(self.v_cache),
+                                   block_table=f(self.block_table), seq_lens=f(self.seq_lens))
+
+
+def make_kvcache_decode(seq_lens, Nq, Hq, Hkv, d, *, num_pages, seed, causal=True, append=True, page_size=16,
+                        max_pages=None, scale=None, nan_fill_unused=False, name="kvcache_decode",
+                        device="cpu") -> KVCacheDecode:
+    """The cache and block table of make_decode for the lengths after the
+    append.  With append, the slots the new tokens will occupy hold NaN until
+    the call writes them, so attending before (or without) the write shows."""
+    base = make_decode(seq_lens, Hq, Hkv, d, num_pages=num_pages, seed=seed, page_size=page_size,
+                       max_pages=max_pages, scale=scale, nan_fill_unused=nan_fill_unused, name=name,
+                       device=device)
+    B = base.B
+    q = randn_bf16((B, Nq, Hq, d), seed * 7 + 5, device)
+    k_new = v_new = None
+    if append:
+        k_new = randn_bf16((B, Nq, Hkv, d), seed * 7 + 6, device)
+        v_new = randn_bf16((B, Nq, Hkv, d), seed * 7 + 7, device)
+        table = base.block_table.cpu()
+        for b, L in enumerate(int(x) for x in seq_lens):
+            for i in range(Nq):
+                pos = L - Nq + i
+                if pos >= 0:
+                    pg = int(table[b, pos // page_size])
+                    base.k_cache[pg, pos % page_size] = float("nan")
+                    base.v_cache[pg, pos % page_size] = float("nan")
+    return KVCacheDecode(name, q, k_new, v_new, base.k_cache, base.v_cache, base.block_table, base.seq_lens,
+                         B, Nq, Hq, Hkv, d, page_size, num_pages, base.scale, bool(causal), seed=seed)
+
+
+def spec_decode(device="cpu") -> KVCacheDecode:
+    """Speculative-decoding verify step: B=64, Nq=4 new tokens per sequence,
+    Hq=32, Hkv=8, d=128, len ~ U[4096, 32768] after the append, causal, 16-token
+    pages in a 200,000-page pool, block table [64, 2048]."""
+    lens = decode_lengths(seed=SEED_BASE + 7)
+    return make_kvcache_decode(lens, 4, 32, 8, 128, num_pages=200_000, seed=SEED_BASE + 7, causal=True,
+                               append=True, max_pages=2048, name="spec_decode_b64_nq4_hq32_hkv8_d128",
+                               device=device)
 
 
 # --------------------------------------------------------------------------
