@@ -14,7 +14,7 @@ outside the timed calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
                   [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|swa_causal|tiny|
-                              paged_decode|paged_decode_small]
+                              paged_decode|paged_decode_small|spec_decode]
 
 --impl reference times the fp64 CPU oracle on the host cores (bounded row
 samples of the same workload, same metric and unit).  Under torchrun each rank
@@ -92,9 +92,26 @@ def decode_bytes(d) -> float:
     return float(kv + 2 * d.B * d.Hq * d.d * 2 + 4 * d.B * d.Hq + 4 * pages + 4 * d.B)
 
 
+def kvcache_bytes(p) -> float:
+    """Algorithmic bytes of one multi-query decode call with append: every
+    key and value row of each sequence once (the appended rows included),
+    the new K/V rows read and written once, q and out, lse, and the
+    block-table entries the sequences use."""
+    lens = p.seq_lens.cpu().tolist()
+    kv = sum(lens) * p.Hkv * p.d * 2 * 2
+    new = 0 if p.k_new is None else 2 * (2 * p.B * p.Nq * p.Hkv * p.d * 2)
+    pages = sum(-(-L // p.page_size) for L in lens)
+    return float(kv + new + 2 * p.B * p.Nq * p.Hq * p.d * 2 + 4 * p.B * p.Hq * p.Nq + 4 * pages + 4 * p.B)
+
+
+def is_kvcache(d) -> bool:
+    return isinstance(d, workloads.KVCacheDecode)
+
+
 KERNEL_SOURCES = {
     "attn_fwd": ["exact_io_aware_04_gb300/csrc/fwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
     "attn_decode_paged": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
+    "attn_decode_kvcache": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
 }
 
 
@@ -258,6 +275,40 @@ def row_keys(p, b, i):
     return max(0, hi - lo + 1)
 
 
+def oracle_kvcache_rate(p, target_s: float, seed: int):
+    """Times the oracle on seeded (b, h, i) rows of a multi-query decode
+    problem (cache already appended); bytes = the K/V rows each row reads."""
+    import oracle
+    threads = oracle.num_threads()
+    g = torch.Generator().manual_seed(seed)
+    n = 32
+    lens = p.seq_lens.cpu().tolist()
+    while True:
+        b = torch.randint(0, p.B, (n,), generator=g)
+        h = torch.randint(0, p.Hq, (n,), generator=g)
+        i = torch.randint(0, p.Nq, (n,), generator=g)
+        rows = torch.stack([b, h, i], 1).numpy().astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.decode_multi_rows(p.q, p.k_cache, p.v_cache, p.block_table, p.seq_lens, scale=p.scale,
+                                 causal=p.causal, rows=rows, threads=threads)
+        dt = time.perf_counter() - t0
+        keys = [lens[int(r[0])] - (p.Nq - 1 - int(r[2]) if p.causal else 0) for r in rows]
+        byts = sum(max(0, k) * p.d * 2 * 2 for k in keys)
+        if dt >= target_s * 0.5 or n >= p.B * p.Hq * p.Nq * 8:
+            return byts / dt, n, dt, threads
+        n = int(n * max(2.0, target_s / max(dt, 1e-3)))
+
+
+def appended_host_copy(p):
+    """Host copy of a multi-query decode problem with its append applied."""
+    import oracle
+    host = p.to("cpu")
+    if host.k_new is not None:
+        oracle.append_kv(host.k_cache, host.v_cache, host.block_table, host.seq_lens, host.k_new, host.v_new,
+                         inplace=True)
+    return host
+
+
 def oracle_decode_rate(d, target_s: float, seed: int):
     import numpy as np
     import oracle
@@ -288,6 +339,8 @@ def make_workloads(name, device):
         decode = workloads.paged_decode(device=device)
     if name == "paged_decode_small":
         decode = workloads.paged_decode_small(device=device)
+    if name == "spec_decode":
+        decode = workloads.spec_decode(device=device)
     return prefill, decode
 
 
@@ -303,6 +356,10 @@ def run_reference(args, world, rank):
     if prefill is not None:
         rate_fn = lambda s: oracle_sample_rate(prefill, per_step, seed=s)[0]
         unit, metric_scale = "TFLOP/s", 1e-12
+    elif is_kvcache(decode):
+        decode = appended_host_copy(decode)
+        rate_fn = lambda s: oracle_kvcache_rate(decode, per_step, seed=s)[0]
+        unit, metric_scale = "GB/s", 1e-9
     else:
         rate_fn = lambda s: oracle_decode_rate(decode, per_step, seed=s)[0]
         unit, metric_scale = "GB/s", 1e-9
@@ -336,7 +393,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libattn", "reference"], default="libattn")
     ap.add_argument("--workload", default="hot_path",
-                    choices=["hot_path", "paged_decode", "paged_decode_small"] + list(PREFILL_WORKLOADS))
+                    choices=["hot_path", "paged_decode", "paged_decode_small", "spec_decode"]
+                    + list(PREFILL_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
@@ -368,7 +426,19 @@ def main(argv=None):
                             dtype=torch.float32, device=dev)
         fkw.update(out=f_out, lse=f_lse)
         p_flops = prefill_flops(prefill)
-    if decode is not None:
+    d_kernel, d_fn, d_launches = None, None, 0
+    if decode is not None and is_kvcache(decode):
+        ws = torch.empty(la.attn_decode_kvcache_workspace_size(decode.B, decode.Nq, decode.Hq, decode.Hkv,
+                                                               decode.d, decode.page_size, decode.max_pages, 0),
+                         dtype=torch.uint8, device=dev)
+        d_out = torch.empty_like(decode.q)
+        d_lse = torch.empty((decode.B, decode.Hq, decode.Nq), dtype=torch.float32, device=dev)
+        dargs = (decode.q, decode.k_cache, decode.v_cache, decode.block_table, decode.seq_lens)
+        dkw = dict(k_new=decode.k_new, v_new=decode.v_new, causal=decode.causal, scale=decode.scale, out=d_out,
+                   lse=d_lse, workspace=ws)
+        d_bytes = kvcache_bytes(decode)
+        d_kernel, d_fn, d_launches = "attn_decode_kvcache", la.attn_decode_kvcache, 2 + (decode.k_new is not None)
+    elif decode is not None:
         ws = torch.empty(la.attn_decode_workspace_size(decode.B, decode.Hq, decode.Hkv, decode.d,
                                                        decode.page_size, decode.max_pages, 0),
                          dtype=torch.uint8, device=dev)
@@ -377,6 +447,7 @@ def main(argv=None):
         dargs = (decode.q, decode.k_cache, decode.v_cache, decode.block_table, decode.seq_lens)
         dkw = dict(scale=decode.scale, out=d_out, lse=d_lse, workspace=ws)
         d_bytes = decode_bytes(decode)
+        d_kernel, d_fn, d_launches = "attn_decode_paged", la.attn_decode_paged, 2
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(ev=None):
@@ -388,7 +459,7 @@ def main(argv=None):
         if ev is not None:
             ev[1].record(stream)
         if decode is not None:
-            la.attn_decode_paged(*dargs, **dkw)
+            d_fn(*dargs, **dkw)
         if ev is not None:
             ev[2].record(stream)
 
@@ -440,13 +511,13 @@ def main(argv=None):
         d_max, d_units = reduce_max_sum(world, d_tot, d_bytes * args.steps, dev)
         dval = d_units / (d_max * 1e-3) / 1e9
         ach = d_bytes / (d_tot / args.steps * 1e-3) / 1e9
-        rooflines["attn_decode_paged"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                          "frac": ach / peaks["hbm_gbs"], "frac_nominal": ach / NOMINAL["hbm_gbs"],
-                                          "traffic": measured_traffic("attn_decode_paged", decode.name),
-                                          "peak_source": f"{peaks_kind} copy bandwidth",
-                                          "ms_per_call_median": statistics.median(d_ms),
-                                          "ms_per_call_p95": sorted(d_ms)[int(0.95 * (len(d_ms) - 1))],
-                                          "bytes_per_call": d_bytes, "launches_per_call": 2}
+        rooflines[d_kernel] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": ach / peaks["hbm_gbs"], "frac_nominal": ach / NOMINAL["hbm_gbs"],
+                               "traffic": measured_traffic(d_kernel, decode.name),
+                               "peak_source": f"{peaks_kind} copy bandwidth",
+                               "ms_per_call_median": statistics.median(d_ms),
+                               "ms_per_call_p95": sorted(d_ms)[int(0.95 * (len(d_ms) - 1))],
+                               "bytes_per_call": d_bytes, "launches_per_call": d_launches}
         line["decode"] = {"value": dval, "unit": "GB/s", "frac_of_measured_hbm": dval / world / peaks["hbm_gbs"],
                           "frac_of_8TBs": dval / world / NOMINAL["hbm_gbs"]}
         if prefill is None:
@@ -455,7 +526,7 @@ def main(argv=None):
     line["roofline"] = dict(rooflines[dominant], kernel=dominant)
     line["rooflines"] = rooflines
     line["ms_per_step"] = step_ms
-    line["gpu_launches"] = args.steps * ((1 if prefill is not None else 0) + (2 if decode is not None else 0))
+    line["gpu_launches"] = args.steps * ((1 if prefill is not None else 0) + d_launches)
     cfg = {"workload": ("mha_causal_b4_h16_n4096_d128 + paged_decode_b64_hq32_hkv8_d128"
                         if args.workload == "hot_path" else (prefill or decode).name),
            "l2": "flushed between steps (256 MB write, outside the timed calls)",
@@ -468,6 +539,8 @@ def main(argv=None):
         cfg.update(decode={"B": decode.B, "Hq": decode.Hq, "Hkv": decode.Hkv, "d": decode.d,
                            "page_size": decode.page_size, "num_pages": decode.num_pages,
                            "tokens": int(decode.seq_lens.sum())})
+        if is_kvcache(decode):
+            cfg["decode"].update(Nq=decode.Nq, causal=decode.causal, append=decode.k_new is not None)
     line["config"] = cfg
     line["clocks"] = clocks.summary()
     line["wall_s_timed_region"] = t_wall
@@ -476,7 +549,7 @@ def main(argv=None):
     line["e2e"] = measure_e2e(la, prefill, decode, fargs if prefill is not None else None,
                               fkw if prefill is not None else None, dargs if decode is not None else None,
                               dkw if decode is not None else None, stream, world, dev,
-                              steps=min(args.steps, 20))
+                              steps=min(args.steps, 20), d_fn=d_fn)
 
     if rank == 0 and world == 1 and args.cpu_baseline_seconds > 0:
         line["cpu_baseline"] = cpu_baseline(prefill, decode, args.cpu_baseline_seconds)
@@ -488,7 +561,7 @@ def main(argv=None):
     return 0
 
 
-def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev, steps):
+def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev, steps, d_fn=None):
     """The headline metric through the public API with the step's inputs in
     pinned host memory: H2D copies, the call, and a D2H read of the result,
     all inside the timed region."""
@@ -510,19 +583,26 @@ def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev,
             host_lse.copy_(kw["lse"], non_blocking=True)
         units, unit, scale = flops, "TFLOP/s", 1e-12
     else:
-        host_q = dargs[0].cpu().pin_memory()
-        dev_q = torch.empty_like(dargs[0])
+        # the step's inputs: the queries (and the new tokens' K/V when appending)
+        names = ["q"] + [k for k in ("k_new", "v_new") if dkw.get(k) is not None]
+        src = {"q": dargs[0], **{k: dkw[k] for k in names[1:]}}
+        host_in = {k: src[k].cpu().pin_memory() for k in names}
+        dev_in = {k: torch.empty_like(src[k]) for k in names}
         host_out = torch.empty(dkw["out"].shape, dtype=dkw["out"].dtype).pin_memory()
         host_lse = torch.empty(dkw["lse"].shape, dtype=dkw["lse"].dtype).pin_memory()
-        h2d = host_q.numel() * host_q.element_size()
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+        kw = dict(dkw)
+        kw.update({k: dev_in[k] for k in names[1:]})
 
         def one():
-            dev_q.copy_(host_q, non_blocking=True)
-            la.attn_decode_paged(dev_q, *dargs[1:], **dkw)
+            for k in names:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            d_fn(dev_in["q"], *dargs[1:], **kw)
             host_out.copy_(dkw["out"], non_blocking=True)
             host_lse.copy_(dkw["lse"], non_blocking=True)
-        units, unit, scale = decode_bytes(decode), "GB/s", 1e-9
+        units = kvcache_bytes(decode) if is_kvcache(decode) else decode_bytes(decode)
+        unit, scale = "GB/s", 1e-9
     for _ in range(3):
         one()
     torch.cuda.synchronize()
@@ -538,7 +618,7 @@ def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev,
     return {"value": tot_units / (t_max * 1e-3) * scale, "unit": unit, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "note": "prefill inputs copied from pinned host memory each step" if prefill is not None else
-                    "decode query copied each step; the paged cache stays resident"}
+                    "decode queries (and new K/V rows) copied each step; the paged cache stays resident"}
 
 
 def cpu_baseline(prefill, decode, seconds):
@@ -548,6 +628,11 @@ def cpu_baseline(prefill, decode, seconds):
             rate, n, dt, threads, fl = oracle_sample_rate(host, seconds, seed=4242)
             return {"value": rate * 1e-12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                     "sample": f"{n} seeded query rows of {prefill.name} ({fl / 1e9:.1f} GFLOP fp64) in {dt:.1f} s"}
+        if is_kvcache(decode):
+            host = appended_host_copy(decode)
+            rate, n, dt, threads = oracle_kvcache_rate(host, seconds, seed=4242)
+            return {"value": rate * 1e-9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                    "sample": f"{n} seeded (sequence, head, query) rows of {decode.name} in {dt:.1f} s"}
         host = decode.to("cpu")
         rate, n, dt, threads = oracle_decode_rate(host, seconds, seed=4242)
         return {"value": rate * 1e-9, "unit": "GB/s", "cores": threads, "kind": "oracle",

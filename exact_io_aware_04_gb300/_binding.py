@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged.restype = I
             L.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
             L.attn_decode_workspace_size.restype = Z
+            L.attn_decode_kvcache.argtypes = [P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P]
+            L.attn_decode_kvcache.restype = I
+            L.attn_decode_kvcache_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+            L.attn_decode_kvcache_workspace_size.restype = Z
             L.attn_get_device_status.argtypes = [P]
             L.attn_get_device_status.restype = I
             L.attn_set_validation.argtypes = [I]
@@ -209,6 +213,61 @@ def attn_decode_paged(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                    float(scale), int(num_splits), _ptr(workspace),
                                    int(workspace.numel() * workspace.element_size()),
                                    _stream_handle(stream)))
+    return out, lse
+
+
+def attn_decode_kvcache_workspace_size(B: int, Nq: int, Hq: int, Hkv: int, d: int, page_size: int,
+                                       max_pages_per_seq: int, num_splits: int = 0) -> int:
+    return int(lib().attn_decode_kvcache_workspace_size(B, Nq, Hq, Hkv, d, page_size, max_pages_per_seq,
+                                                        num_splits))
+
+
+def attn_decode_kvcache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        block_table: torch.Tensor, seq_lens: torch.Tensor, *,
+                        k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                        causal: bool = True, scale: Optional[float] = None, num_splits: int = 0,
+                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None):
+    """Nq new queries per sequence over the paged cache, with the new tokens'
+    K/V appended in place first when k_new/v_new are given.  q [B, Nq, Hq, d];
+    k_new/v_new [B, Nq, Hkv, d]; caches [num_pages, page, Hkv, d] (written by
+    the append); seq_lens int32 [B] counts the tokens after the append.
+    Returns (out [B, Nq, Hq, d] bf16, lse [B, Hq, Nq] fp32)."""
+    _need(q, "q", torch.bfloat16)
+    _need(k_cache, "k_cache", torch.bfloat16)
+    _need(v_cache, "v_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("give both k_new and v_new or neither")
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4 or q.dim() != 4:
+        raise ValueError("q [B, Nq, Hq, d]; caches [num_pages, page, Hkv, d]")
+    B, Nq, Hq, d = (int(x) for x in q.shape)
+    num_pages, page, Hkv = int(k_cache.shape[0]), int(k_cache.shape[1]), int(k_cache.shape[2])
+    if k_new is not None:
+        _need(k_new, "k_new", torch.bfloat16)
+        _need(v_new, "v_new", torch.bfloat16)
+        if tuple(k_new.shape) != (B, Nq, Hkv, d) or k_new.shape != v_new.shape:
+            raise ValueError("k_new/v_new must be [B, Nq, Hkv, d]")
+    if block_table.dim() != 2 or int(block_table.shape[0]) != B or int(seq_lens.numel()) != B:
+        raise ValueError("block_table [B, max_pages] and seq_lens [B] required")
+    max_pages = int(block_table.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_bytes = attn_decode_kvcache_workspace_size(B, Nq, Hq, Hkv, d, page, max_pages, num_splits)
+    if ws_bytes == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "no decode plan for these sizes")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    _check(lib().attn_decode_kvcache(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(block_table), max_pages, _ptr(seq_lens), _ptr(out), _ptr(lse),
+                                     B, Nq, Hq, Hkv, d, page, num_pages, float(scale), 1 if causal else 0,
+                                     int(num_splits), _ptr(workspace),
+                                     int(workspace.numel() * workspace.element_size()), _stream_handle(stream)))
     return out, lse
 
 

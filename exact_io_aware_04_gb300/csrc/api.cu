@@ -176,39 +176,57 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size, int max_pages_per_seq,
                                   int num_splits) {
     DecodePlan plan;
-    if (!make_decode_plan(B, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan)) return 0;
+    if (!make_decode_plan(B, 1, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan)) return 0;
     return plan.total_bytes;
 }
 
-attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
-                              int max_pages_per_seq, const int* seq_lens, void* out, float* lse, int B, int Hq,
-                              int Hkv, int d, int page_size, int num_pages, float scale, int num_splits,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse || !workspace)
-        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: NULL pointer");
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
-        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: bad size");
-    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
-    if (!isfinite(scale) || !(scale > 0.f))
-        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: scale must be finite and > 0");
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: misaligned pointer");
-    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: head_dim %d (built: 64, 128)", d);
-    if (page_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: page_size %d (built: 16)", page_size);
-    if (static_cast<long long>(max_pages_per_seq) * page_size > INT32_MAX)
-        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: sequences longer than 2^31 tokens");
+size_t attn_decode_kvcache_workspace_size(int B, int Nq, int Hq, int Hkv, int d, int page_size,
+                                          int max_pages_per_seq, int num_splits) {
     DecodePlan plan;
-    if (!make_decode_plan(B, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan))
-        return fail(ATTN_ERR_UNSUPPORTED, "attn_decode_paged: no plan for Hq/Hkv = %d", Hq / Hkv);
+    if (!make_decode_plan(B, Nq, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan)) return 0;
+    return plan.total_bytes;
+}
+
+namespace {
+
+// The checks and the launch shared by the paged-decode entry points.
+attn_status decode_call(const char* fn, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const int* block_table, int max_pages_per_seq, const int* seq_lens, void* out,
+                        float* lse, int B, int Nq, int Hq, int Hkv, int d, int page_size, int num_pages, float scale,
+                        int causal, int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse || !workspace)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if ((k_new == nullptr) != (v_new == nullptr)) return fail(ATTN_ERR_INVALID_ARG, "%s: give both k_new and v_new or neither", fn);
+    if (B < 0 || Nq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: bad size", fn);
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "%s: Hq %% Hkv != 0 (%d, %d)", fn, Hq, Hkv);
+    if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", fn);
+    if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "%s: head_dim %d (built: 64, 128)", fn, d);
+    if (page_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "%s: page_size %d (built: 16)", fn, page_size);
+    if (static_cast<long long>(max_pages_per_seq) * page_size > INT32_MAX)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: sequences longer than 2^31 tokens", fn);
+    if (static_cast<long long>(Hq / Hkv) * Nq > 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: (Hq/Hkv) * Nq = %lld query rows per K/V head (built: up to 128)", fn,
+                    static_cast<long long>(Hq / Hkv) * Nq);
+    DecodePlan plan;
+    if (!make_decode_plan(B, Nq, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan))
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: no plan for Hq/Hkv = %d, Nq = %d", fn, Hq / Hkv, Nq);
     if (workspace_bytes < plan.total_bytes)
-        return fail(ATTN_ERR_INVALID_ARG, "attn_decode_paged: workspace %zu bytes < %zu needed", workspace_bytes,
+        return fail(ATTN_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", fn, workspace_bytes,
                     plan.total_bytes);
     if (B == 0) return ATTN_OK;
     DecodeArgs a;
     a.q = q;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache_w = k_cache;
+    a.v_cache_w = v_cache;
     a.block_table = block_table;
     a.max_pages = max_pages_per_seq;
     a.seq_lens = seq_lens;
@@ -220,11 +238,35 @@ attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_
     a.d = d;
     a.page_size = page_size;
     a.num_pages = num_pages;
+    a.nq = Nq;
+    a.causal = causal;
     a.scale = scale;
     a.num_splits = num_splits;
     a.workspace = workspace;
     a.workspace_bytes = workspace_bytes;
     return launch_decode(a, plan, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+attn_status attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                              int max_pages_per_seq, const int* seq_lens, void* out, float* lse, int B, int Hq,
+                              int Hkv, int d, int page_size, int num_pages, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    // the caches are only read on this path (no append)
+    return decode_call("attn_decode_paged", q, nullptr, nullptr, const_cast<void*>(k_cache),
+                       const_cast<void*>(v_cache), block_table, max_pages_per_seq, seq_lens, out, lse, B, 1, Hq, Hkv,
+                       d, page_size, num_pages, scale, 0, num_splits, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_decode_kvcache(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                const int* block_table, int max_pages_per_seq, const int* seq_lens, void* out,
+                                float* lse, int B, int Nq, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                float scale, int causal, int num_splits, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+    return decode_call("attn_decode_kvcache", q, k_new, v_new, k_cache, v_cache, block_table, max_pages_per_seq,
+                       seq_lens, out, lse, B, Nq, Hq, Hkv, d, page_size, num_pages, scale, causal, num_splits,
+                       workspace, workspace_bytes, stream);
 }
 
 attn_status attn_get_device_status(void* stream) {

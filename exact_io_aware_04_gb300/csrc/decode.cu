@@ -17,6 +17,14 @@
 // ("FlashAttention-3 and PagedAttention", section "Why decode starves the
 // GPU").
 //
+// Several new queries per sequence (Nq > 1, "Deep Dive - FlashAttention",
+// sections "Causal 2.1 is the decode gotcha" and "Paged KV is a lookup, not a
+// cache manager"): the Nq x group query rows that share a K/V head form the
+// consumer tiles (row r = i * group + head-in-group), so the gathered page is
+// still read once for all of them; with causal, query i is position
+// len - Nq + i and its scores past that position are masked on the last pages.
+// append_kv_kernel writes the new tokens' K/V into their cache slots first.
+//
 // Slots at or beyond the sequence length are excluded by selection (their
 // score is replaced by -inf and their V entries by zero before any multiply),
 // so NaN bits in unused cache slots cannot reach the output.
@@ -41,12 +49,13 @@ constexpr float kRescaleThreshold = 8.0f;
 struct DecodeParams {
     CUtensorMap tm_k;  // 5-D view of the K pool: {64, slot, head, d/64, page}
     CUtensorMap tm_v;
-    const __nv_bfloat16* q;
+    const __nv_bfloat16* q;  // [B, nq, Hq, d]
     const int* block_table;
     const int* seq_lens;
-    float* part_o;     // [B, Hq, max_chunks, d]
-    float* part_lse;   // [B, Hq, max_chunks]
+    float* part_o;     // [B, Hq, nq, max_chunks, d]
+    float* part_lse;   // [B, Hq, nq, max_chunks]
     int B, Hq, Hkv, group, num_pages, max_pages;
+    int nq, causal;    // queries per sequence; bottom-right causal among them
     int pages_per_chunk, max_chunks, head_groups, heads_per_cta, m_tiles;
     float scale_log2;
     int validate;
@@ -169,24 +178,33 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
     const int cw = warp - 1;
     if (cw >= n_consumers) return;
     const int hh = cw / p.m_tiles;                  // K/V head inside the group
-    const int mt = cw - hh * p.m_tiles;             // 16-row tile of its query heads
+    const int mt = cw - hh * p.m_tiles;             // 16-row tile of its query rows
     const int g = hg * HG + hh;                     // global K/V head
-    const int rows = min(16, p.group - mt * 16);    // real query heads in this tile
-    const int h0 = g * p.group + mt * 16;           // first query head of the tile
+    const int R = p.group * p.nq;                   // query rows per K/V head
+    const int rows = min(16, R - mt * 16);          // real query rows in this tile
     const int r0 = lane >> 2, r1 = r0 + 8;          // accumulator rows of this lane
     const int cq = (lane & 3) * 2;                  // column pair inside an 8-wide block
+    // row r of the tile is query i = (16 mt + r) / group of query head g*group + (16 mt + r) % group
+    const int i0 = (mt * 16 + r0) / p.group, i1 = (mt * 16 + r1) / p.group;
+    const int h_r0 = g * p.group + (mt * 16 + r0 - i0 * p.group);
+    const int h_r1 = g * p.group + (mt * 16 + r1 - i1 * p.group);
+    // last key each row may see (inclusive): position len - nq + i under causal
+    const int lim0 = p.causal ? len - p.nq + i0 : len - 1;
+    const int lim1 = p.causal ? len - p.nq + i1 : len - 1;
+    const int first_limited = p.causal ? len - p.nq : len;  // pages reaching past this need the row limits
 
     // Q fragments (A operand), rows >= `rows` are zero
     uint32_t qa[KB][4];
     {
-        const __nv_bfloat16* qb = p.q + (static_cast<size_t>(b) * p.Hq + h0) * HD;
+        const __nv_bfloat16* qr0 = p.q + ((static_cast<size_t>(b) * p.nq + i0) * p.Hq + h_r0) * HD;
+        const __nv_bfloat16* qr1 = p.q + ((static_cast<size_t>(b) * p.nq + i1) * p.Hq + h_r1) * HD;
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb) {
             const int c0 = kb * 16 + cq;
-            qa[kb][0] = r0 < rows ? *reinterpret_cast<const uint32_t*>(qb + r0 * HD + c0) : 0u;
-            qa[kb][1] = r1 < rows ? *reinterpret_cast<const uint32_t*>(qb + r1 * HD + c0) : 0u;
-            qa[kb][2] = r0 < rows ? *reinterpret_cast<const uint32_t*>(qb + r0 * HD + c0 + 8) : 0u;
-            qa[kb][3] = r1 < rows ? *reinterpret_cast<const uint32_t*>(qb + r1 * HD + c0 + 8) : 0u;
+            qa[kb][0] = r0 < rows ? *reinterpret_cast<const uint32_t*>(qr0 + c0) : 0u;
+            qa[kb][1] = r1 < rows ? *reinterpret_cast<const uint32_t*>(qr1 + c0) : 0u;
+            qa[kb][2] = r0 < rows ? *reinterpret_cast<const uint32_t*>(qr0 + c0 + 8) : 0u;
+            qa[kb][3] = r1 < rows ? *reinterpret_cast<const uint32_t*>(qr1 + c0 + 8) : 0u;
         }
     }
     float o[NB][4];
@@ -228,6 +246,17 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
                 const int t0 = nt * 8 + cq;
                 if (t0 >= valid) { s[nt][0] = -INFINITY; s[nt][2] = -INFINITY; }
                 if (t0 + 1 >= valid) { s[nt][1] = -INFINITY; s[nt][3] = -INFINITY; }
+            }
+        }
+        const int pt = tok0 + it * kPage;  // position of the page's first token
+        if (pt + kPage - 1 > first_limited) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t0 = pt + nt * 8 + cq;
+                if (t0 > lim0) s[nt][0] = -INFINITY;
+                if (t0 + 1 > lim0) s[nt][1] = -INFINITY;
+                if (t0 > lim1) s[nt][2] = -INFINITY;
+                if (t0 + 1 > lim1) s[nt][3] = -INFINITY;
             }
         }
         // ---- row maxima (rows r0, r1), reduced over the 4 lanes of a quad
@@ -272,11 +301,20 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
             l_part[0] += pr[nt][0] + pr[nt][1];
             l_part[1] += pr[nt][2] + pr[nt][3];
         }
-        uint32_t pa[4];
+        // P as a bf16 pair hi + lo (lo = the rounding residual of hi): the
+        // weights then carry about 16 significant bits, so rows with few keys
+        // are not limited by an 8-bit P; two MMAs per fragment cost nothing
+        // on this HBM-bound path.
+        uint32_t pa[4], pl[4];
         pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
         pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
         pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
         pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float a = pr[c >> 1][(c & 1) * 2], bb = pr[c >> 1][(c & 1) * 2 + 1];
+            pl[c] = pack_bf16x2(a - bf16_lo(pa[c]), bb - bf16_hi(pa[c]));
+        }
 
         // ---- O += P V
         // B-fragment token rows of this lane: cq, cq+1 (b0) and 8+cq, 9+cq (b1)
@@ -297,6 +335,8 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
             }
             mma_16816(o[nb], pa, v00, v01);
             mma_16816(o[nb + 1], pa, v10, v11);
+            mma_16816(o[nb], pl, v00, v01);
+            mma_16816(o[nb + 1], pl, v10, v11);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&bar_empty[st]));
@@ -311,8 +351,8 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
     const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
     const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    const size_t slot0 = (static_cast<size_t>(b) * p.Hq + h0 + r0) * p.max_chunks + chunk;
-    const size_t slot1 = (static_cast<size_t>(b) * p.Hq + h0 + r1) * p.max_chunks + chunk;
+    const size_t slot0 = ((static_cast<size_t>(b) * p.Hq + h_r0) * p.nq + i0) * p.max_chunks + chunk;
+    const size_t slot1 = ((static_cast<size_t>(b) * p.Hq + h_r1) * p.nq + i1) * p.max_chunks + chunk;
     if (r0 < rows) {
         float* dst = p.part_o + slot0 * HD;
 #pragma unroll
@@ -333,12 +373,12 @@ struct CombineParams {
     const float* part_o;
     const float* part_lse;
     const int* seq_lens;
-    __nv_bfloat16* out;
-    float* lse;
-    int B, Hq, max_pages, pages_per_chunk, max_chunks;
+    __nv_bfloat16* out;  // [B, nq, Hq, d]
+    float* lse;          // [B, Hq, nq]
+    int B, Hq, nq, max_pages, pages_per_chunk, max_chunks;
 };
 
-// One warp per (sequence, query head): lse = log sum_i exp(lse_i), O = sum_i
+// One warp per (sequence, query head, query): lse = log sum_i exp(lse_i), O = sum_i
 // exp(lse_i - lse) O_i over the chunks the sequence actually has.  Lane l
 // owns d-elements [l*d/32, (l+1)*d/32) as one vector load per chunk; the
 // weights of 32 chunks at a time are computed once and broadcast by shuffle,
@@ -349,8 +389,10 @@ __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const CombineP
     using Vec = typename std::conditional<V == 4, float4, float2>::type;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= p.B * p.Hq) return;
-    const int b = row / p.Hq;
+    if (row >= p.B * p.Hq * p.nq) return;
+    const int b = row / (p.Hq * p.nq);
+    const int hq = (row - b * p.Hq * p.nq) / p.nq;
+    const int qi = row - (b * p.Hq + hq) * p.nq;
     const int len = min(max(__ldg(p.seq_lens + b), 0), p.max_pages * kPage);
     const int chunk_tokens = p.pages_per_chunk * kPage;
     const int n = (len + chunk_tokens - 1) / chunk_tokens;
@@ -362,7 +404,7 @@ __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const CombineP
     float acc[V];
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[c] = 0.f;
-    __nv_bfloat16* dst = p.out + static_cast<size_t>(row) * HD + lane * V;
+    __nv_bfloat16* dst = p.out + ((static_cast<size_t>(b) * p.nq + qi) * p.Hq + hq) * HD + lane * V;
     if (mx == -INFINITY) {  // no keys: O = 0, lse = -inf
         if (lane == 0) p.lse[row] = -INFINITY;
 #pragma unroll
@@ -396,6 +438,37 @@ __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const CombineP
         *reinterpret_cast<uint2*>(dst) = w2;
     } else {
         *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0], acc[1 % V]);
+    }
+}
+
+// In-place cache append: new row i of sequence b goes to position
+// len - nq + i, i.e. slot pos % 16 of page block_table[b][pos / 16].  One
+// block per (sequence, new token) copies its [Hkv, d] row with 16-byte stores.
+// Positions below zero or past the table, and page ids outside the pool, are
+// never written (with validation on they are reported as ATTN_ERR_BAD_INDEX).
+__global__ void __launch_bounds__(128) append_kv_kernel(const uint4* k_new, const uint4* v_new, uint4* k_cache,
+                                                        uint4* v_cache, const int* block_table, const int* seq_lens,
+                                                        int nq, int row_vecs, int max_pages, int num_pages,
+                                                        int validate, int* err) {
+    const int b = blockIdx.x / nq;
+    const int i = blockIdx.x - b * nq;
+    const int len = __ldg(seq_lens + b);
+    const int pos = len - nq + i;
+    bool bad = pos < 0 || pos >= max_pages * kPage;
+    int pg = -1;
+    if (!bad) {
+        pg = __ldg(block_table + static_cast<size_t>(b) * max_pages + pos / kPage);
+        bad = pg < 0 || pg >= num_pages;
+    }
+    if (bad) {
+        if (validate && threadIdx.x == 0) record_error(err, ATTN_ERR_BAD_INDEX);
+        return;
+    }
+    const size_t src = static_cast<size_t>(blockIdx.x) * row_vecs;
+    const size_t dst = (static_cast<size_t>(pg) * kPage + pos % kPage) * row_vecs;
+    for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+        k_cache[dst + c] = __ldg(k_new + src + c);
+        v_cache[dst + c] = __ldg(v_new + src + c);
     }
 }
 
@@ -442,7 +515,9 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     p.max_chunks = plan.max_chunks;
     p.head_groups = plan.head_groups;
     p.heads_per_cta = HG;
-    p.m_tiles = (p.group + 15) / 16;
+    p.nq = a.nq;
+    p.causal = a.causal ? 1 : 0;
+    p.m_tiles = (p.group * a.nq + 15) / 16;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.validate = validation_enabled() ? 1 : 0;
     p.drop_first_page = set_drop_page_load(0);  // consume the one-shot test switch
@@ -451,6 +526,17 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     if (p.validate)
         check_pages_kernel<<<a.B, 128, 0, stream>>>(a.block_table, a.seq_lens, a.max_pages, a.num_pages,
                                                     dev.err_word);
+    if (a.k_new != nullptr) {
+        append_kv_kernel<<<a.B * a.nq, 128, 0, stream>>>(
+            static_cast<const uint4*>(a.k_new), static_cast<const uint4*>(a.v_new), static_cast<uint4*>(a.k_cache_w),
+            static_cast<uint4*>(a.v_cache_w), a.block_table, a.seq_lens, a.nq, a.Hkv * HD / 8, a.max_pages,
+            a.num_pages, p.validate, dev.err_word);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error_message("append_kv launch: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+    }
     const int stage_bytes = 2 * kPage * HG * HD * 2;
     const int n_stages = std::min(8, kStageBudget / stage_bytes);
     const int smem = n_stages * stage_bytes + 1024;
@@ -480,10 +566,11 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     c.lse = a.lse;
     c.B = a.B;
     c.Hq = a.Hq;
+    c.nq = a.nq;
     c.max_pages = a.max_pages;
     c.pages_per_chunk = plan.pages_per_chunk;
     c.max_chunks = plan.max_chunks;
-    const int rows = a.B * a.Hq;
+    const int rows = a.B * a.Hq * a.nq;
     attn_decode_combine_kernel<HD><<<(rows + 7) / 8, 256, 0, stream>>>(c);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -501,12 +588,13 @@ std::atomic<int> g_drop_page_load{0};
 
 int set_drop_page_load(int enabled) { return g_drop_page_load.exchange(enabled ? 1 : 0); }
 
-bool make_decode_plan(int B, int Hq, int Hkv, int d, int page_size, int max_pages, int num_splits,
+bool make_decode_plan(int B, int nq, int Hq, int Hkv, int d, int page_size, int max_pages, int num_splits,
                       DecodePlan* plan) {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages <= 0 || num_splits < 0) return false;
+    if (B < 0 || nq <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_pages <= 0 || num_splits < 0) return false;
     if (page_size != kPage || (d != 64 && d != 128)) return false;
     const int group = Hq / Hkv;
-    const int m_tiles = (group + 15) / 16;
+    if (static_cast<long long>(group) * nq > 128) return false;
+    const int m_tiles = (group * nq + 15) / 16;
     if (m_tiles > 8) return false;
     // largest divisor of Hkv whose page box fits a 32 KB stage half and 8 consumer warps
     int hg = 1;
@@ -528,7 +616,7 @@ bool make_decode_plan(int B, int Hq, int Hkv, int d, int page_size, int max_page
     if (ppc < 1) ppc = 1;
     plan->pages_per_chunk = ppc;
     plan->max_chunks = (max_pages + ppc - 1) / ppc;
-    const size_t rows = static_cast<size_t>(B) * Hq * plan->max_chunks;
+    const size_t rows = static_cast<size_t>(B) * Hq * nq * plan->max_chunks;
     plan->partial_o_bytes = (rows * d * sizeof(float) + 255) / 256 * 256;
     plan->partial_lse_bytes = (rows * sizeof(float) + 255) / 256 * 256;
     plan->total_bytes = plan->partial_o_bytes + plan->partial_lse_bytes;

@@ -72,7 +72,7 @@ extern "C" attn_status attn_decode_paged_noalloc(const void* q, const void* k_ca
     // Same plan and checks as attn_decode_paged; the scratch must fit the array.
     DecodePlan plan;
     if (B >= 0 && Hq > 0 && Hkv > 0 && max_pages_per_seq > 0 && num_splits >= 0 &&
-        make_decode_plan(B, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan) &&
+        make_decode_plan(B, 1, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan) &&
         plan.total_bytes > kScratchBytes) {
         set_error_message(
             "attn_decode_paged_noalloc: these sizes need %zu bytes of scratch, more than the library's fixed "

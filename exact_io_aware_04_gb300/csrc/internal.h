@@ -47,14 +47,17 @@ struct FwdArgs {
 attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
 struct DecodeArgs {
-    const void* q;
+    const void* q;                  // [B, nq, Hq, d]
     const void *k_cache, *v_cache;
+    const void *k_new, *v_new;      // [B, nq, Hkv, d] appended before attending, or NULL
+    void *k_cache_w, *v_cache_w;    // writable views of the caches (used only with k_new)
     const int* block_table;
     int max_pages;
     const int* seq_lens;
     void* out;
     float* lse;
     int B, Hq, Hkv, d, page_size, num_pages;
+    int nq, causal;
     float scale;
     int num_splits;
     void* workspace;
@@ -69,7 +72,7 @@ struct DecodePlan {
     int head_groups;      // Hkv / heads_per_cta
     size_t partial_o_bytes, partial_lse_bytes, total_bytes;
 };
-bool make_decode_plan(int B, int Hq, int Hkv, int d, int page_size, int max_pages, int num_splits,
+bool make_decode_plan(int B, int nq, int Hq, int Hkv, int d, int page_size, int max_pages, int num_splits,
                       DecodePlan* plan);
 attn_status launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 

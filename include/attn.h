@@ -218,6 +218,60 @@ attn_status attn_decode_paged_noalloc(const void *q,
                                       void *stream);
 
 /*
+ * attn_decode_kvcache -- Nq new queries per sequence over the paged K/V cache,
+ * optionally appending the new tokens' K/V to the cache in place first.
+ *
+ * Operation: attn_decode_paged's split-KV pass and combine, generalised to
+ * several queries per sequence ("Deep Dive - FlashAttention", section "Paged
+ * KV is a lookup, not a cache manager": the call may update the cache in
+ * place; section "Causal 2.1 is the decode gotcha": the bottom-right corner).
+ * seq_lens[b] counts the sequence's tokens INCLUDING the Nq new ones; query i
+ * is position seq_lens[b] - Nq + i.  With causal = 1 it sees keys
+ * j <= seq_lens[b] - Nq + i (the bottom-right rule with Nq queries and
+ * seq_lens[b] keys); with causal = 0 it sees all seq_lens[b] keys.  The Nq
+ * queries of the query heads that share a K/V head are packed into the same
+ * tiles, so each gathered page is read once for all of them.
+ * Append (k_new and v_new not NULL): before any score is computed, new row i
+ * of sequence b is written to position seq_lens[b] - Nq + i, i.e. slot
+ * pos % page_size of page block_table[b][pos / page_size].  The caller
+ * reserves those pages in the block table beforehand.  Positions below zero,
+ * positions past the table and page ids outside [0, num_pages) are never
+ * written (with validation on they are reported as ATTN_ERR_BAD_INDEX).  Two
+ * sequences whose new positions map to the same slot race: the result is one
+ * of the writes, unspecified which.
+ *
+ * Layout:
+ *   q        [B, Nq, Hq, d] bf16          out [B, Nq, Hq, d] bf16 (written)
+ *   k_new, v_new [B, Nq, Hkv, d] bf16, or both NULL (no append)
+ *   k_cache, v_cache [num_pages, page_size, Hkv, d] bf16 (written by the append)
+ *   block_table, seq_lens, page_size, num_splits: as attn_decode_paged
+ *   lse      [B, Hq, Nq] fp32 (written)
+ *   workspace: at least attn_decode_kvcache_workspace_size(...) bytes,
+ *            256-byte aligned, otherwise as attn_decode_paged.
+ * Nq = 1 with no append computes what attn_decode_paged computes.
+ * Rejects (ATTN_ERR_INVALID_ARG): attn_decode_paged's cases, Nq <= 0, exactly
+ * one of k_new/v_new NULL, causal not 0 or 1.  (Hq / Hkv) * Nq > 128 returns
+ * ATTN_ERR_UNSUPPORTED.
+ */
+attn_status attn_decode_kvcache(const void *q, const void *k_new, const void *v_new,
+                                void *k_cache, void *v_cache,
+                                const int *block_table, int max_pages_per_seq,
+                                const int *seq_lens,
+                                void *out, float *lse,
+                                int B, int Nq, int Hq, int Hkv, int d, int page_size, int num_pages,
+                                float scale, int causal, int num_splits,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
+ * attn_decode_kvcache_workspace_size -- bytes of device scratch
+ * attn_decode_kvcache needs for these sizes (0 when the arguments are
+ * invalid).  Pure host arithmetic; needs no GPU.
+ */
+size_t attn_decode_kvcache_workspace_size(int B, int Nq, int Hq, int Hkv, int d, int page_size,
+                                          int max_pages_per_seq, int num_splits);
+
+/*
  * attn_get_device_status -- synchronises `stream`, then reads and clears the
  * device error word of the current device: ATTN_OK, ATTN_ERR_TIMEOUT or
  * ATTN_ERR_BAD_INDEX (the first error recorded since the last read), or

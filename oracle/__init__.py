@@ -198,12 +198,13 @@ def decode_multi_rows(q, k_cache, v_cache, block_table, seq_lens, *, scale, caus
     return out, lse
 
 
-def append_kv(k_cache, v_cache, block_table, seq_lens, k_new, v_new):
-    """The in-place cache update, on copies: new row i of sequence b goes to
-    position seq_lens[b] - Nq + i, i.e. page block_table[b][pos // page] at
-    slot pos % page.  Positions below zero, and page ids outside the pool, are
-    skipped.  k_new/v_new [B, Nq, Hkv, d].  Returns (k_cache', v_cache')."""
-    kc, vc = k_cache.clone(), v_cache.clone()
+def append_kv(k_cache, v_cache, block_table, seq_lens, k_new, v_new, inplace=False):
+    """The in-place cache update (on copies unless inplace): new row i of
+    sequence b goes to position seq_lens[b] - Nq + i, i.e. page
+    block_table[b][pos // page] at slot pos % page.  Positions below zero, and
+    page ids outside the pool, are skipped.  k_new/v_new [B, Nq, Hkv, d].
+    Returns (k_cache', v_cache')."""
+    kc, vc = (k_cache, v_cache) if inplace else (k_cache.clone(), v_cache.clone())
     B, Nq = int(k_new.shape[0]), int(k_new.shape[1])
     page, pool = int(kc.shape[1]), int(kc.shape[0])
     bt = block_table.cpu()

@@ -98,6 +98,27 @@ def test_decode_host_rejections(lib):
     assert dec(lib, B=0) == 0
 
 
+def kvc(lib, B=2, Nq=4, Hq=8, Hkv=2, causal=1, kn=FAKE, vn=FAKE, ws_bytes=1 << 30):
+    return lib.attn_decode_kvcache(FAKE, kn, vn, FAKE, FAKE, FAKE, 4, FAKE, FAKE, FAKE, B, Nq, Hq, Hkv, 128, 16,
+                                   10, 0.1, causal, 0, ctypes.c_void_p(0x100000), ws_bytes, None)
+
+
+def test_decode_kvcache_host_rejections(lib):
+    assert kvc(lib, Nq=0) == -1
+    assert kvc(lib, kn=None) == -1                    # only one of k_new / v_new
+    assert kvc(lib, causal=2) == -1
+    assert kvc(lib, Hq=7) == -1                       # Hq % Hkv
+    assert kvc(lib, Hq=64, Hkv=2, Nq=5) == -2         # 160 query rows per K/V head
+    assert kvc(lib, ws_bytes=16) == -1
+    assert kvc(lib, B=0) == 0
+    assert kvc(lib, B=0, kn=None, vn=None) == 0
+    # the workspace grows with Nq; Nq = 1 matches attn_decode_paged's
+    one = lib.attn_decode_kvcache_workspace_size(64, 1, 32, 8, 128, 16, 2048, 0)
+    assert one == lib.attn_decode_workspace_size(64, 32, 8, 128, 16, 2048, 0)
+    assert lib.attn_decode_kvcache_workspace_size(64, 4, 32, 8, 128, 16, 2048, 0) >= 4 * one - 1024
+    assert lib.attn_decode_kvcache_workspace_size(64, 0, 32, 8, 128, 16, 2048, 0) == 0
+
+
 def test_workspace_size(lib):
     f = lib.attn_decode_workspace_size
     assert f(2, 8, 2, 128, 16, 4, 0) > 0

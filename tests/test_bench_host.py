@@ -49,6 +49,13 @@ def test_decode_bytes():
     assert bench.decode_bytes(d) == kv + 2 * 2 * 8 * 128 * 2 + 4 * 2 * 8 + 4 * (2 + 2) + 4 * 2
 
 
+def test_kvcache_bytes():
+    p = workloads.make_kvcache_decode([17, 32], 3, 8, 2, 128, num_pages=8, seed=1, append=True)
+    kv = (17 + 32) * 2 * 128 * 2 * 2
+    new = 2 * (2 * 2 * 3 * 2 * 128 * 2)
+    assert bench.kvcache_bytes(p) == kv + new + 2 * 2 * 3 * 8 * 128 * 2 + 4 * 2 * 8 * 3 + 4 * (2 + 2) + 4 * 2
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
