@@ -27,6 +27,11 @@ Parity status of each function (what pins it, see ``tests/test_oracle.py``):
                   gathered keys.
   append_kv    -- pinned: brute-force gather of the written positions through
                   the block table; untouched slots keep their bytes.
+  backward     -- pinned: torch autograd through SDPA's fp64 MATH backend with
+                  an explicit keep mask; central finite differences of
+                  <G, O> on inputs whose perturbations are exact in bf16;
+                  sum_j dV_j = sum_i G_i over nonempty rows; sum_j dK_j = 0
+                  without a mask; empty rows pass no gradient.
 """
 from __future__ import annotations
 
@@ -73,6 +78,8 @@ def _load():
             lib.oracle_decode_rows.restype = I
             lib.oracle_decode_multi_rows.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, D, I, P, L, P, P, I]
             lib.oracle_decode_multi_rows.restype = I
+            lib.oracle_backward.argtypes = [P, P, P, P, I, I, I, I, I, I, D, I, I, I, P, P, P, L, P, P, P, I]
+            lib.oracle_backward.restype = I
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
             _lib = lib
@@ -232,4 +239,25 @@ def decode_kvcache(p, rows=None, threads: int = 0):
                           dtype=np.int32)
     return decode_multi_rows(p.q, kc, vc, p.block_table, p.seq_lens, scale=p.scale, causal=p.causal,
                              rows=rows, threads=threads)
+
+
+def backward(p, g, pairs=None, threads: int = 0):
+    """dQ, dK, dV (fp64 numpy, shaped like q, k, v) of L = <g, O> for a
+    workloads.Prefill problem; g is bf16 like q.  pairs: (b, kv head) pairs
+    to compute (default: all); rows outside them are zero."""
+    qb, kb, vb, gb = _bits(p.q), _bits(p.k), _bits(p.v), _bits(g)
+    if pairs is None:
+        pairs = [(b, h) for b in range(p.B) for h in range(p.Hkv)]
+    pr = _i32(pairs).reshape(-1, 2)
+    dq = np.zeros(tuple(p.q.shape), dtype=np.float64)
+    dk = np.zeros(tuple(p.k.shape), dtype=np.float64)
+    dv = np.zeros(tuple(p.v.shape), dtype=np.float64)
+    left, right = (int(x) for x in getattr(p, "window", (-1, -1)))
+    rc = _load().oracle_backward(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), p.B, p.Hq, p.Hkv, p.Nq, p.Nk,
+                                 int(p.d), float(p.scale), int(bool(p.causal)), left, right,
+                                 _ptr(_i32(p.cu_q)), _ptr(_i32(p.cu_k)), _ptr(pr), pr.shape[0],
+                                 _ptr(dq), _ptr(dk), _ptr(dv), threads if threads > 0 else num_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_backward rejected its arguments (status {rc})")
+    return dq, dk, dv
 

@@ -50,6 +50,16 @@
  *    queries and len keys ("Deep Dive - FlashAttention", sections "Causal 2.1
  *    is the decode gotcha" and "Paged KV is a lookup, not a cache manager").
  *
+ * Backward (oracle_backward), for one nonempty row i with G = dL/dO
+ * ("Deep Dive - FlashAttention", section "Backward recomputes tiles on
+ * purpose"; "FlashAttention: Part 1", section 3.6):
+ *   P_ij  = exp(s_ij - m) / l            over the allowed keys (else 0)
+ *   dV_j += P_ij G_i                     dP_ij = G_i . v_j
+ *   D_i   = sum_j P_ij dP_ij             (= G_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j      dK_j += scale * dS_ij q_i
+ * with the K/V gradients of a grouped head summed over its query heads.
+ *
  * Inputs are bf16 bit patterns (uint16); each is widened exactly to double.
  * Threads: POSIX threads over output rows; each row is computed by one thread
  * in the order written above, so results do not depend on the thread count.
@@ -423,3 +433,173 @@ int oracle_decode_multi_rows(const uint16_t *q, const uint16_t *k_cache, const u
     jb.max_keys = max_keys;
     return run_job(&jb, n_threads);
 }
+
+/* ---- backward by the definition ---- */
+typedef struct {
+    const uint16_t *q, *k, *v, *g;   /* g = dL/dO, laid out like q */
+    int B, Hq, Hkv, Nq, Nk, d, causal;
+    long win_left, win_right;
+    double scale;
+    const int32_t *cu_q, *cu_k;
+    const int32_t *pairs;            /* (b, kv head) pairs to compute */
+    long n_pairs;
+    double *dq, *dk, *dv;
+    long max_keys;
+    long next;
+    int status;
+} bwd_job;
+
+static void bwd_pair(bwd_job *jb, long r, double *sc, double *p, double *dp)
+{
+    const int b = jb->pairs[2 * r], g = jb->pairs[2 * r + 1];
+    const int d = jb->d, group = jb->Hq / jb->Hkv;
+    long q_first, k_first, nq, nk;
+    if (jb->cu_q) {
+        q_first = jb->cu_q[b];
+        nq = jb->cu_q[b + 1] - jb->cu_q[b];
+        k_first = jb->cu_k[b];
+        nk = jb->cu_k[b + 1] - jb->cu_k[b];
+    } else {
+        q_first = (long)b * jb->Nq;
+        nq = jb->Nq;
+        k_first = (long)b * jb->Nk;
+        nk = jb->Nk;
+    }
+    for (int h = g * group; h < (g + 1) * group; ++h) {
+        for (long i = 0; i < nq; ++i) {
+            const uint16_t *q_row = jb->q + ((q_first + i) * jb->Hq + h) * (long)d;
+            const uint16_t *g_row = jb->g + ((q_first + i) * jb->Hq + h) * (long)d;
+            double *dq_row = jb->dq + ((q_first + i) * jb->Hq + h) * (long)d;
+            double m = -INFINITY;
+            long n_allowed = 0;
+            for (long j = 0; j < nk; ++j) {
+                if (!key_allowed(i, j, nq, nk, jb->causal, jb->win_left, jb->win_right))
+                    continue;
+                const uint16_t *k_row = jb->k + ((k_first + j) * jb->Hkv + g) * (long)d;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c)
+                    dot += bf16_value(q_row[c]) * bf16_value(k_row[c]);
+                sc[j] = jb->scale * dot;
+                if (n_allowed == 0 || sc[j] > m)
+                    m = sc[j];
+                ++n_allowed;
+            }
+            for (int c = 0; c < d; ++c)
+                dq_row[c] = 0.0;
+            if (n_allowed == 0)
+                continue;   /* an empty row has O = 0 and passes no gradient */
+            double l = 0.0;
+            for (long j = 0; j < nk; ++j)
+                if (key_allowed(i, j, nq, nk, jb->causal, jb->win_left, jb->win_right))
+                    l += exp(sc[j] - m);
+            double D = 0.0;
+            for (long j = 0; j < nk; ++j) {
+                if (!key_allowed(i, j, nq, nk, jb->causal, jb->win_left, jb->win_right))
+                    continue;
+                const uint16_t *v_row = jb->v + ((k_first + j) * jb->Hkv + g) * (long)d;
+                p[j] = exp(sc[j] - m) / l;
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c)
+                    acc += bf16_value(g_row[c]) * bf16_value(v_row[c]);
+                dp[j] = acc;
+                D += p[j] * dp[j];
+            }
+            for (long j = 0; j < nk; ++j) {
+                if (!key_allowed(i, j, nq, nk, jb->causal, jb->win_left, jb->win_right))
+                    continue;
+                const double ds = p[j] * (dp[j] - D);
+                const uint16_t *k_row = jb->k + ((k_first + j) * jb->Hkv + g) * (long)d;
+                double *dk_row = jb->dk + ((k_first + j) * jb->Hkv + g) * (long)d;
+                double *dv_row = jb->dv + ((k_first + j) * jb->Hkv + g) * (long)d;
+                for (int c = 0; c < d; ++c) {
+                    dq_row[c] += jb->scale * ds * bf16_value(k_row[c]);
+                    dk_row[c] += jb->scale * ds * bf16_value(q_row[c]);
+                    dv_row[c] += p[j] * bf16_value(g_row[c]);
+                }
+            }
+        }
+    }
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *jb = (bwd_job *)arg;
+    size_t n = (size_t)(jb->max_keys > 0 ? jb->max_keys : 1);
+    double *buf = (double *)malloc(sizeof(double) * 3 * n);
+    if (!buf) {
+        __atomic_store_n(&jb->status, -2, __ATOMIC_SEQ_CST);
+        return NULL;
+    }
+    for (;;) {
+        long r = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (r >= jb->n_pairs)
+            break;
+        bwd_pair(jb, r, buf, buf + n, buf + 2 * n);
+    }
+    free(buf);
+    return NULL;
+}
+
+/*
+ * Gradients dQ, dK, dV of L = <G, O> for the (b, kv head) pairs listed
+ * (n_pairs pairs; each pair covers its group's query heads), dense or packed
+ * like oracle_prefill_rows_window.  g [T_q, Hq, d] bf16 bits.  dq [T_q, Hq, d],
+ * dk/dv [T_k, Hkv, d] fp64: the rows of the listed pairs are overwritten (dq)
+ * or accumulated into (dk, dv: the caller zero-fills them).
+ * Returns 0, or -1 for invalid arguments, -2 when out of memory.
+ */
+int oracle_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *g,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                    double scale, int causal, int win_left, int win_right,
+                    const int32_t *cu_q, const int32_t *cu_k,
+                    const int32_t *pairs, long n_pairs,
+                    double *dq, double *dk, double *dv, int n_threads)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || n_pairs < 0)
+        return -1;
+    if ((cu_q == NULL) != (cu_k == NULL))
+        return -1;
+    long max_keys = 1;
+    for (long r = 0; r < n_pairs; ++r) {
+        int b = pairs[2 * r], gg = pairs[2 * r + 1];
+        if (b < 0 || b >= B || gg < 0 || gg >= Hkv)
+            return -1;
+        long nk = cu_k ? (long)cu_k[b + 1] - cu_k[b] : Nk;
+        if (nk > max_keys)
+            max_keys = nk;
+    }
+    bwd_job jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k; jb.v = v; jb.g = g;
+    jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.Nq = Nq; jb.Nk = Nk; jb.d = d;
+    jb.causal = causal ? 1 : 0;
+    jb.win_left = win_left < 0 ? -1 : win_left;
+    jb.win_right = win_right < 0 ? -1 : win_right;
+    jb.scale = scale;
+    jb.cu_q = cu_q; jb.cu_k = cu_k;
+    jb.pairs = pairs; jb.n_pairs = n_pairs;
+    jb.dq = dq; jb.dk = dk; jb.dv = dv;
+    jb.max_keys = max_keys;
+    if (n_threads <= 0)
+        n_threads = 1;
+    if ((long)n_threads > n_pairs)
+        n_threads = n_pairs > 0 ? (int)n_pairs : 1;
+    if (n_threads > 1024)
+        n_threads = 1024;
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    if (!th)
+        return -2;
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &jb) != 0)
+            break;
+        ++started;
+    }
+    if (started == 0)
+        bwd_worker(&jb);
+    for (int t = 0; t < started; ++t)
+        pthread_join(th[t], NULL);
+    free(th);
+    return jb.status;
+}
+

@@ -563,3 +563,135 @@ def test_thread_count_does_not_change_results():
     a = oracle.prefill(p, threads=1)
     b = oracle.prefill(p, threads=7)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+def _sdpa_grads(p, g, keep):
+    """dq, dk, dv of <g, O> through SDPA's fp64 MATH backend with an explicit
+    keep mask (one dense sequence, q [nq, hq, d], k/v [nk, hkv, d])."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    import torch.nn.functional as F
+    rep = p.Hq // p.Hkv
+    q = p.q.double().permute(1, 0, 2)[None].requires_grad_(True)
+    k = p.k.double().permute(1, 0, 2)[None].requires_grad_(True)
+    v = p.v.double().permute(1, 0, 2)[None].requires_grad_(True)
+    with sdpa_kernel(SDPBackend.MATH):
+        out = F.scaled_dot_product_attention(q, k.repeat_interleave(rep, dim=1), v.repeat_interleave(rep, dim=1),
+                                             attn_mask=keep, is_causal=False, dropout_p=0.0, scale=p.scale)
+    has_key = keep.any(dim=-1)
+    gg = g.double().permute(1, 0, 2)[None] * has_key[None, None, :, None]   # SDPA's empty rows are NaN
+    out = torch.where(has_key[None, None, :, None], out, torch.zeros_like(out))
+    dq, dk, dv = torch.autograd.grad(out, (q, k, v), gg)
+    f = lambda x: x[0].permute(1, 0, 2).numpy()
+    return f(dq), f(dk), f(dv)
+
+
+def _keep(nq, nk, causal, window=(-1, -1)):
+    i = torch.arange(nq)[:, None]
+    j = torch.arange(nk)[None, :]
+    c = i + nk - nq
+    keep = torch.ones(nq, nk, dtype=torch.bool)
+    if causal:
+        keep &= j <= c
+    if window[0] >= 0:
+        keep &= j >= c - window[0]
+    if window[1] >= 0:
+        keep &= j <= c + window[1]
+    return keep
+
+
+@pytest.mark.parametrize("nq,nk,hq,hkv,d,causal,window", [
+    (2, 5, 2, 2, 3, True, (-1, -1)), (5, 2, 2, 2, 3, True, (-1, -1)), (4, 4, 2, 2, 3, True, (-1, -1)),
+    (7, 13, 6, 2, 8, True, (-1, -1)), (13, 7, 4, 1, 8, False, (-1, -1)), (20, 33, 4, 2, 16, True, (6, -1)),
+    (24, 24, 2, 2, 8, False, (3, 2)),
+])
+def test_backward_matches_sdpa_autograd_fp64(nq, nk, hq, hkv, d, causal, window):
+    p = workloads.make_prefill(1, hq, hkv, nq, nk, d, causal=causal, seed=nq * 31 + nk, window=window)
+    g = workloads.randn_bf16((nq, hq, d), seed=nq + 5 * nk)
+    dq, dk, dv = oracle.backward(p, g)
+    rq, rk, rv = _sdpa_grads(p, g, _keep(nq, nk, causal, window))
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert np.abs(got - ref).max() <= 1e-11 * max(1.0, np.abs(ref).max())
+
+
+def _exact_grid(shape, gen):
+    """Values k/4 in [-2, 2]: every x +- 1/64 and x +- 1/32 is exact in bf16."""
+    return (torch.randint(-8, 9, shape, generator=gen).float() / 4).to(torch.bfloat16)
+
+
+def test_backward_matches_finite_differences():
+    """Central differences of L = <G, O> along random directions, Richardson-
+    extrapolated from steps 1/64 and 1/32 (the perturbed inputs are exact in
+    bf16), against <U, grad>: independent of every backward formula."""
+    import dataclasses
+    gen = torch.Generator().manual_seed(11)
+    nq, nk, hq, hkv, d = 6, 9, 4, 2, 8
+    for causal in (True, False):
+        p = workloads.make_prefill(1, hq, hkv, nq, nk, d, causal=causal, seed=1)
+        p = dataclasses.replace(p, q=_exact_grid(p.q.shape, gen), k=_exact_grid(p.k.shape, gen),
+                                v=_exact_grid(p.v.shape, gen), scale=0.5)
+        g = _exact_grid(p.q.shape, gen)
+        grads = oracle.backward(p, g)
+        rows = oracle.all_rows(p)
+
+        def loss(pp):
+            o, _ = oracle.prefill(pp, rows)
+            gi = g.double().numpy()[rows[:, 2], rows[:, 1]]
+            return float((o * gi).sum())
+
+        for which, grad in zip(("q", "k", "v"), grads):
+            base = getattr(p, which)
+            u = torch.randint(-1, 2, base.shape, generator=gen).float()
+            est = []
+            for t in (1 / 64, 1 / 32):
+                plus = (base.float() + t * u).to(torch.bfloat16)
+                minus = (base.float() - t * u).to(torch.bfloat16)
+                assert torch.equal(plus.float(), base.float() + t * u)   # exact perturbation
+                lp = loss(dataclasses.replace(p, **{which: plus}))
+                lm = loss(dataclasses.replace(p, **{which: minus}))
+                est.append((lp - lm) / (2 * t))
+            fd = (4 * est[0] - est[1]) / 3
+            an = float((u.double().numpy() * grad).sum())
+            assert abs(fd - an) <= 2e-4 * max(1.0, abs(an)), (causal, which, fd, an)
+
+
+def test_backward_invariants():
+    """Adding c to every value shifts each nonempty row's O by c, so
+    sum_j dV_j = sum over nonempty rows of G_i (per K/V head, over its group);
+    without a mask, adding c to every key leaves O unchanged, so
+    sum_j dK_j = 0; rows with no key pass no gradient."""
+    for causal, nq, nk in ((True, 9, 5), (False, 7, 7), (True, 30, 40)):
+        p = workloads.make_prefill(1, 4, 2, nq, nk, 16, causal=causal, seed=nq + nk)
+        g = workloads.randn_bf16((nq, 4, 16), seed=3)
+        dq, dk, dv = oracle.backward(p, g)
+        keep = _keep(nq, nk, causal)
+        nonempty = keep.any(dim=-1).numpy()
+        gd = g.double().numpy()
+        for kvh in range(2):
+            heads = [kvh * 2, kvh * 2 + 1]
+            assert np.allclose(dv[:, kvh].sum(0), gd[nonempty][:, heads].sum((0, 1)), atol=1e-12)
+            if not causal:
+                assert np.allclose(dk[:, kvh].sum(0), 0.0, atol=1e-12)
+        assert (dq[~nonempty] == 0).all()
+
+
+def test_backward_varlen_equals_per_sequence_dense():
+    ql, kl = [5, 0, 17, 9], [7, 4, 17, 30]
+    p = workloads.make_varlen(ql, kl, 4, 2, 16, causal=True, seed=77)
+    g = workloads.randn_bf16((sum(ql), 4, 16), seed=78)
+    dq, dk, dv = oracle.backward(p, g)
+    cq = np.cumsum([0] + ql)
+    ck = np.cumsum([0] + kl)
+    for b in range(len(ql)):
+        sub = workloads.make_prefill(1, 4, 2, ql[b], kl[b], 16, causal=True, seed=1)
+        import dataclasses
+        sub = dataclasses.replace(sub, q=p.q[cq[b]:cq[b + 1]], k=p.k[ck[b]:ck[b + 1]], v=p.v[ck[b]:ck[b + 1]])
+        if ql[b] == 0:
+            assert (dk[ck[b]:ck[b + 1]] == 0).all() and (dv[ck[b]:ck[b + 1]] == 0).all()
+            continue
+        sq, sk, sv = oracle.backward(sub, g[cq[b]:cq[b + 1]])
+        assert np.array_equal(sq, dq[cq[b]:cq[b + 1]])
+        assert np.array_equal(sk, dk[ck[b]:ck[b + 1]]) and np.array_equal(sv, dv[ck[b]:ck[b + 1]])
+

@@ -31,6 +31,12 @@ MUTATIONS = {
                                                         "(((long)b * jb->Nq) * jb->Hq + h)"),
     "multi-query decode ignores causal": ("attend_row(q_row, &ks, h / group, i, jb->Nq, len, jb->causal,",
                                           "attend_row(q_row, &ks, h / group, i, jb->Nq, len, 0,"),
+    "backward drops the row term D": ("const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * dp[j];"),
+    "backward dK without the scale": ("dk_row[c] += jb->scale * ds * bf16_value(q_row[c]);",
+                                      "dk_row[c] += ds * bf16_value(q_row[c]);"),
+    "backward dV from dP": ("dv_row[c] += p[j] * bf16_value(g_row[c]);", "dv_row[c] += dp[j] * bf16_value(g_row[c]);"),
+    "backward dQ from values": ("dq_row[c] += jb->scale * ds * bf16_value(k_row[c]);",
+                                "dq_row[c] += jb->scale * ds * bf16_value(jb->v[((k_first + j) * jb->Hkv + g) * (long)d + c]);"),
 }
 
 
