@@ -14,7 +14,7 @@ outside the timed calls.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
                   [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|swa_causal|tiny|
-                              paged_decode|paged_decode_small|spec_decode]
+                              paged_decode|paged_decode_small|spec_decode|mha_causal_bwd|gqa_causal_bwd]
 
 --impl reference times the fp64 CPU oracle on the host cores (bounded row
 samples of the same workload, same metric and unit).  Under torchrun each rank
@@ -43,6 +43,7 @@ import torch  # noqa: E402
 import workloads  # noqa: E402
 
 PREFILL_WORKLOADS = ("mha_causal", "gqa_causal", "varlen_chunked", "swa_causal", "tiny")
+BWD_WORKLOADS = {"mha_causal_bwd": "mha_causal", "gqa_causal_bwd": "gqa_causal"}  # backward of a prefill workload
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -108,8 +109,15 @@ def is_kvcache(d) -> bool:
     return isinstance(d, workloads.KVCacheDecode)
 
 
+def backward_flops(p) -> float:
+    """Algorithmic FLOPs of one backward call: the five products of the
+    recomputation (S, dP, dV, dS^T Q, dS K), 2 * d per attended pair each."""
+    return 10.0 * p.d * attended_pairs(p)
+
+
 KERNEL_SOURCES = {
     "attn_fwd": ["exact_io_aware_04_gb300/csrc/fwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
+    "attn_bwd": ["exact_io_aware_04_gb300/csrc/bwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
     "attn_decode_paged": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
     "attn_decode_kvcache": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
 }
@@ -309,6 +317,31 @@ def appended_host_copy(p):
     return host
 
 
+def oracle_bwd_rate(p, g, target_s: float, seed: int):
+    """Times the oracle backward on seeded (sequence, K/V head) pairs, one per
+    host thread, over every row_stride-th query row; halves row_stride until
+    the sample takes about target_s.  Returns (flops/s, sample text, seconds,
+    threads); flops = 10 d x the keys of the rows processed."""
+    import oracle
+    threads = oracle.num_threads()
+    gen = torch.Generator().manual_seed(seed)
+    all_pairs = [(b, h) for b in range(p.B) for h in range(p.Hkv)]
+    n = min(len(all_pairs), max(1, threads))
+    idx = torch.randperm(len(all_pairs), generator=gen)[:n].tolist()
+    pairs = [all_pairs[i] for i in idx]
+    group = p.Hq // p.Hkv
+    stride = max(1, p.Nq // 8)
+    while True:
+        t0 = time.perf_counter()
+        oracle.backward(p, g, pairs=pairs, threads=threads, row_stride=stride)
+        dt = time.perf_counter() - t0
+        keys = sum(row_keys(p, b, i) for b, _ in pairs for i in range(0, p.seq_lens()[b][0], stride))
+        flops = 10.0 * p.d * keys * group
+        if dt >= target_s * 0.5 or stride == 1:
+            return flops / dt, f"{n} pairs, every {stride}-th row", dt, min(threads, n)
+        stride = max(1, int(stride / max(2.0, target_s / max(dt, 1e-3))))
+
+
 def oracle_decode_rate(d, target_s: float, seed: int):
     import numpy as np
     import oracle
@@ -351,9 +384,17 @@ def run_reference(args, world, rank):
     # the headline of the hot-path step is the prefill metric; the CPU arm
     # times that part (the decode pool would not fit a bounded CPU sample)
     name = "mha_causal" if args.workload == "hot_path" else args.workload
-    prefill, decode = make_workloads(name, "cpu")
     per_step = float(os.environ.get("ATTN_REFERENCE_STEP_SECONDS", "4.0"))
-    if prefill is not None:
+    if name in BWD_WORKLOADS:
+        prefill = getattr(workloads, BWD_WORKLOADS[name])()
+        decode = None
+        grad = workloads.randn_bf16(tuple(prefill.q.shape), seed=prefill.seed + 900)
+    else:
+        prefill, decode = make_workloads(name, "cpu")
+    if name in BWD_WORKLOADS:
+        rate_fn = lambda s: oracle_bwd_rate(prefill, grad, per_step, seed=s)[0]
+        unit, metric_scale = "TFLOP/s", 1e-12
+    elif prefill is not None:
         rate_fn = lambda s: oracle_sample_rate(prefill, per_step, seed=s)[0]
         unit, metric_scale = "TFLOP/s", 1e-12
     elif is_kvcache(decode):
@@ -369,13 +410,18 @@ def run_reference(args, world, rank):
     value = statistics.median(rates) * metric_scale
     import oracle
     cores = oracle.num_threads()
-    sample = (f"each step: seeded rows of the {prefill.name if prefill else decode.name} workload, "
+    wname = prefill.name if prefill else decode.name
+    metric = METRIC
+    if name in BWD_WORKLOADS:
+        wname += "_backward"
+        metric = BWD_METRIC
+    sample = (f"each step: seeded rows of the {wname} workload, "
               f"about {per_step:.0f} s of fp64 oracle work, rate = work/seconds")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": prefill.name if prefill else decode.name},
+        "config": {"workload": wname},
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -384,6 +430,7 @@ def run_reference(args, world, rank):
 
 
 METRIC = "fwd TFLOP/s & % bf16 tensor peak; split-KV decode GB/s & % HBM peak"
+BWD_METRIC = "bwd TFLOP/s (5 recomputation products per attended pair) & % bf16 tensor peak"
 
 
 def main(argv=None):
@@ -394,7 +441,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["libattn", "reference"], default="libattn")
     ap.add_argument("--workload", default="hot_path",
                     choices=["hot_path", "paged_decode", "paged_decode_small", "spec_decode"]
-                    + list(PREFILL_WORKLOADS))
+                    + list(PREFILL_WORKLOADS) + list(BWD_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
@@ -407,6 +454,8 @@ def main(argv=None):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, peaks_kind = load_peaks()
+    if args.workload in BWD_WORKLOADS:
+        return run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind)
 
     prefill, decode = make_workloads(args.workload, dev)
     # ---- device-resident inputs
@@ -553,6 +602,115 @@ def main(argv=None):
 
     if rank == 0 and world == 1 and args.cpu_baseline_seconds > 0:
         line["cpu_baseline"] = cpu_baseline(prefill, decode, args.cpu_baseline_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind):
+    """The backward of a prefill workload: attn_bwd (D, dK/dV, dQ kernels)
+    with q, k, v, the forward's out and lse and a seeded dO resident."""
+    p = getattr(workloads, BWD_WORKLOADS[args.workload])()
+    g_host = workloads.randn_bf16(tuple(p.q.shape), seed=p.seed + 900)
+    pg = p.to(dev)
+    shape_q = (p.B, p.Nq, p.Hq, p.d)
+    shape_k = (p.B, p.Nk, p.Hkv, p.d)
+    q, k, v = pg.q.view(shape_q), pg.k.view(shape_k), pg.v.view(shape_k)
+    out, lse = la.attn_fwd(q, k, v, causal=p.causal, scale=p.scale)
+    g = g_host.to(dev).view(shape_q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(la.lib().attn_bwd_workspace_size(p.B, p.Hq, p.Nq, 0), dtype=torch.uint8, device=dev)
+    kw = dict(causal=p.causal, scale=p.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+    flops = backward_flops(p)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        flush.fill_(1)
+        if ev is not None:
+            ev[0].record(stream)
+        la.attn_bwd(q, k, v, out, lse, g, **kw)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if la.attn_get_device_status() != 0:
+        raise RuntimeError("device error during warm-up")
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            step(events[i])
+        torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    st = la.attn_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {la.attn_status_string(st)} after the timed region")
+    ms = [e[0].elapsed_time(e[1]) for e in events]
+    tot = sum(ms)
+    t_max, units = reduce_max_sum(world, tot, flops * args.steps, dev)
+    value = units / (t_max * 1e-3) / 1e12
+    ach = flops / (tot / args.steps * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": ach / peaks["bf16_tflops"], "frac_nominal": ach / NOMINAL["bf16_tflops"],
+            "traffic": measured_traffic("attn_bwd", p.name), "peak_source": f"{peaks_kind} bf16 burst",
+            "ms_per_call_median": statistics.median(ms), "ms_per_call_p95": sorted(ms)[int(0.95 * (len(ms) - 1))],
+            "flops_per_call": flops, "flops_executed_per_call": 14.0 * p.d * attended_pairs(p),
+            "launches_per_call": 3, "kernel": "attn_bwd"}
+    line = {"metric": BWD_METRIC,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
+            "value": value, "unit": "TFLOP/s", "roofline": roof, "ms_per_step": tot / args.steps,
+            "gpu_launches": 3 * args.steps,
+            "config": {"workload": p.name + "_backward", "l2": "flushed between steps (256 MB write, outside the timed calls)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "prefill": {"B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Nq": p.Nq, "Nk": p.Nk, "d": p.d,
+                                   "causal": p.causal}},
+            "clocks": clocks.summary(), "wall_s_timed_region": t_wall}
+    # end to end: q, k, v, out, lse, dO from pinned host memory, dq/dk/dv back
+    src = [q, k, v, out, lse, g]
+    host_in = [t.cpu().pin_memory() for t in src]
+    dev_in = [torch.empty_like(t) for t in src]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        la.attn_bwd(*dev_in[:5], dev_in[5], **kw)
+        for h, d in zip(host_out, (dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    barrier(world)
+    n_e2e = min(args.steps, 20)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_max, e_units = reduce_max_sum(world, e0.elapsed_time(e1), flops * n_e2e, dev)
+    line["e2e"] = {"value": e_units / (e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+                   "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out), "steps": n_e2e,
+                   "note": "q, k, v, out, lse and dO copied from pinned host memory each step"}
+    if rank == 0 and world == 1 and args.cpu_baseline_seconds > 0:
+        try:
+            rate, what, dt, threads = oracle_bwd_rate(p, g_host, args.cpu_baseline_seconds, seed=4242)
+            line["cpu_baseline"] = {"value": rate * 1e-12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                    "sample": f"seeded (sequence, K/V head) pairs of {p.name}: {what}, "
+                                              f"in {dt:.1f} s"}
+        except Exception as e:
+            line["cpu_baseline"] = {"value": None, "unit": None, "cores": None, "kind": "oracle",
+                                    "sample": f"failed: {e}"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

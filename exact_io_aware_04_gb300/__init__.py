@@ -8,6 +8,7 @@ CUDA device, the calls raise.
 
     out, lse = attn_fwd(q, k, v, causal=True)                       # dense THD/BSHD
     out, lse = attn_fwd(q, k, v, causal=True, cu_seqlens_q=cq, cu_seqlens_k=ck)
+    dq, dk, dv = attn_bwd(q, k, v, out, lse, dout, causal=True)
     out, lse = attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens)
     out, lse = attn_decode_kvcache(q, k_cache, v_cache, block_table, seq_lens, k_new=kn, v_new=vn)
 """
@@ -19,6 +20,7 @@ from ._binding import (  # noqa: F401
     ATTN_ERR_UNSUPPORTED,
     ATTN_OK,
     AttnError,
+    attn_bwd,
     attn_decode_kvcache,
     attn_decode_kvcache_workspace_size,
     attn_decode_paged,

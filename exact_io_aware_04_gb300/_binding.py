@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged.restype = I
             L.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I, I]
             L.attn_decode_workspace_size.restype = Z
+            L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P, P, Z, P]
+            L.attn_bwd.restype = I
+            L.attn_bwd_workspace_size.argtypes = [I, I, I, I]
+            L.attn_bwd_workspace_size.restype = Z
             L.attn_decode_kvcache.argtypes = [P, P, P, P, P, P, I, P, P, P, I, I, I, I, I, I, I, F, I, I, P, Z, P]
             L.attn_decode_kvcache.restype = I
             L.attn_decode_kvcache_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -169,6 +173,54 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
                                      float(scale), 1 if causal else 0, left, right, _ptr(cu_seqlens_q),
                                      _ptr(cu_seqlens_k), _stream_handle(stream)))
     return out, lse
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, *, causal: bool, scale: Optional[float] = None, window: Optional[tuple] = None,
+             cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
+             dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None, stream=None):
+    """Backward of attn_fwd: returns (dq, dk, dv) for dout = dL/dout.  q, k, v,
+    causal, scale, window and cu_seqlens as given to attn_fwd; out and lse are
+    its outputs."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    if out.shape != q.shape or dout.shape != q.shape or k.shape != v.shape:
+        raise ValueError("out and dout must be shaped like q; k like v")
+    d = int(q.shape[-1])
+    Hq, Hkv = int(q.shape[-2]), int(k.shape[-2])
+    if cu_seqlens_q is not None or cu_seqlens_k is not None:
+        if cu_seqlens_q is None or cu_seqlens_k is None:
+            raise ValueError("give both cu_seqlens or neither")
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("packed mode takes q [T_q, Hq, d] and k/v [T_k, Hkv, d]")
+        B = int(cu_seqlens_q.numel()) - 1
+        Nq, Nk = int(q.shape[0]), int(k.shape[0])
+        packed = 1
+    else:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense mode takes q [B, Nq, Hq, d] and k/v [B, Nk, Hkv, d]")
+        B, Nq, Nk = int(q.shape[0]), int(q.shape[1]), int(k.shape[1])
+        packed = 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    left, right = (-1, -1) if window is None else (int(x) for x in window)
+    ws_bytes = int(lib().attn_bwd_workspace_size(B, Hq, Nq, packed))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, n, torch.bfloat16)
+    _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                          B, Hq, Hkv, Nq, Nk, d, float(scale), 1 if causal else 0, left, right,
+                          _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(workspace),
+                          int(workspace.numel() * workspace.element_size()), _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, d: int, page_size: int,

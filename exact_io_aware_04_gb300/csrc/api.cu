@@ -173,6 +173,68 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
                            cu_seqlens_k, stream);
 }
 
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int packed) {
+    if (B < 0 || Hq <= 0 || Nq < 0) return 0;
+    return bwd_workspace_bytes(B, Hq, Nq, packed != 0);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                     int causal, int window_left, int window_right, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !out || !dout || !lse || !dq || !workspace)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: NULL tensor pointer");
+    if ((!k || !v || !dk || !dv) && Nk > 0) return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: NULL k/v/dk/dv with keys present");
+    if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: give both cu_seqlens or neither");
+    if (B < 0 || Nq < 0 || Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: negative size");
+    if (Hq <= 0 || Hkv <= 0) return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: head counts must be positive");
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
+    if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: scale must be finite and > 0");
+    if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: causal must be 0 or 1");
+    if (window_left < -1 || window_right < -1)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: window sides must be >= 0, or -1 for unbounded");
+    if (Nk == 0) {  // no keys: K/V are never read and dK/dV are empty
+        k = v = q;
+        dk = dv = dq;
+    }
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: misaligned pointer");
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_bwd: head_dim %d (built: 64, 128)", d);
+    const bool varlen = cu_seqlens_q != nullptr;
+    if (!varlen && (static_cast<long long>(B) * Nq > INT32_MAX || static_cast<long long>(B) * Nk > INT32_MAX))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_bwd: more than 2^31 tokens");
+    if (workspace_bytes < bwd_workspace_bytes(B, Hq, Nq, varlen))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_bwd: workspace %zu bytes < %zu needed", workspace_bytes,
+                    bwd_workspace_bytes(B, Hq, Nq, varlen));
+    if (B == 0 || (Nq == 0 && Nk == 0)) return ATTN_OK;
+    BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.workspace = workspace;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.win_left = window_left;
+    a.win_right = window_right;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    return launch_bwd(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size, int max_pages_per_seq,
                                   int num_splits) {
     DecodePlan plan;

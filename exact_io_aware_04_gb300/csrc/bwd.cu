@@ -1,0 +1,984 @@
+// bwd.cu -- backward of exact attention on sm_103a, by recomputation.
+//
+// For a nonempty row i with G = dL/dO ("Deep Dive - FlashAttention", section
+// "Backward recomputes tiles on purpose"; "FlashAttention: Part 1", section
+// 3.6): P = exp(S - lse) is rebuilt tile by tile from the saved lse,
+//   dV = P^T G,  dP = G V^T,  D = rowsum(G o O),  dS = P o (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q,
+// and masked probabilities (and their gradients) are zero.  Three kernels:
+//
+//   attn_bwd_dot_kernel   D = rowsum(G o O) in fp32, one warp per row.
+//   attn_bwd_dkdv_kernel  one CTA per (sequence, K/V head, 128-key tile): K_j
+//                         and V_j stay in shared memory while the (Q_i, G_i)
+//                         tiles of every query head of the group stream past;
+//                         per step the tensor core runs S^T = K_j Q_i^T and
+//                         dP^T = V_j G_i^T, the softmax warps turn them into
+//                         P^T and dS^T (bf16, written back into tensor memory
+//                         over the fp32 tiles), and the tensor core
+//                         accumulates dV += P^T G_i and dK += dS^T Q_i with
+//                         the left operand read from tensor memory.
+//   attn_bwd_dq_kernel    one CTA per (sequence, query head, 128-row tile):
+//                         Q_i and G_i stay, (K_j, V_j) stream; S = Q_i K_j^T,
+//                         dP = G_i V_j^T, dS, and dQ += dS K_j.
+//
+// Computing dQ in its own pass (three products instead of one more in the
+// K/V pass) needs no atomic accumulation, so the result is deterministic, and
+// each pass fits its accumulators in the 512 tensor-memory columns of one SM.
+// The issue order overlaps the softmax work with the tensor core: in the K/V
+// pass the tensor core runs dV(s), S^T(s+1), dK(s), dP^T(s+1) while the
+// softmax warps produce P^T(s+1) and dS^T(s+1); in the dQ pass it runs
+// S(u+1), dQ(u), dP(u+1).
+#include <cuda_bf16.h>
+#include <math.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;  // rows of every tile (keys or queries)
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 208;  // warpgroups 0 and 1
+constexpr int kControlRegs = 88;   // warpgroup 2
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxWarps = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int HD>
+struct Tile {
+    static constexpr int kPanels = HD / 64;
+    static constexpr int kPanelBytes = kBM * 128;
+    static constexpr int kBytes = kPanels * kPanelBytes;
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 2-D [rows, heads*d] bf16, box 64 x 128, 128B swizzle
+    const float* lse;                      // dense [B, Hq, Nq]; packed [Hq, T_q]
+    const float* dvec;                     // D, same layout as lse
+    __nv_bfloat16 *dq, *dk, *dv;
+    const int *cu_q, *cu_k;
+    int B, Hq, Hkv, group, Nq, Nk;
+    int win_left, win_right;               // < 0 unbounded; causal is right = 0
+    int varlen;
+    float scale, scale_log2;
+    int* err;
+};
+
+struct Seq {
+    int q_base, k_base, nq, nk;
+};
+
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+__device__ __forceinline__ Seq seq_of(const BwdParams& p, int b) {
+    Seq s;
+    if (p.varlen) {
+        const int q0 = clampi(__ldg(p.cu_q + b), 0, p.Nq);
+        const int q1 = clampi(__ldg(p.cu_q + b + 1), q0, p.Nq);
+        const int k0 = clampi(__ldg(p.cu_k + b), 0, p.Nk);
+        const int k1 = clampi(__ldg(p.cu_k + b + 1), k0, p.Nk);
+        s.q_base = q0;
+        s.nq = q1 - q0;
+        s.k_base = k0;
+        s.nk = k1 - k0;
+    } else {
+        s.q_base = b * p.Nq;
+        s.nq = p.Nq;
+        s.k_base = b * p.Nk;
+        s.nk = p.Nk;
+    }
+    return s;
+}
+
+// Allowed keys of local query row i: [key_first, key_last] (inclusive, clamped
+// to [-1, nk]); the band of the forward pass.
+__device__ __forceinline__ int key_first(long long i, int nq, int nk, int left) {
+    if (left < 0) return 0;
+    const long long k = i + nk - nq - left;
+    return static_cast<int>(k < 0 ? 0 : (k > nk ? nk : k));
+}
+__device__ __forceinline__ int key_last(long long i, int nq, int nk, int right) {
+    if (right < 0) return nk - 1;
+    const long long k = i + nk - nq + right;
+    return static_cast<int>(k < -1 ? -1 : (k > nk - 1 ? nk - 1 : k));
+}
+// Query rows that see key j: [row_first, row_last] (inclusive, clamped to [-1, nq]).
+__device__ __forceinline__ int row_first(long long j, int nq, int nk, int right) {
+    if (right < 0) return 0;
+    const long long i = j - (nk - nq) - right;
+    return static_cast<int>(i < 0 ? 0 : (i > nq ? nq : i));
+}
+__device__ __forceinline__ int row_last(long long j, int nq, int nk, int left) {
+    if (left < 0) return nq - 1;
+    const long long i = j - (nk - nq) + left;
+    return static_cast<int>(i < -1 ? -1 : (i > nq - 1 ? nq - 1 : i));
+}
+
+__device__ __forceinline__ size_t lse_index(const BwdParams& p, int b, int h, const Seq& s, int i) {
+    return p.varlen ? static_cast<size_t>(h) * p.Nq + s.q_base + i
+                    : (static_cast<size_t>(b) * p.Hq + h) * p.Nq + i;
+}
+
+// Sequence b and tile t of item x of the packed-mode list: the tiles of
+// sequence b (of `rows_per_tile`-row tiles over its nq or nk rows) come after
+// those of sequences 0..b-1.  One warp scans cu_seqlens 32 sequences at a time.
+__device__ bool find_tile(const BwdParams& p, int x, bool over_keys, int& b_out, int& t_out) {
+    const int lane = threadIdx.x & 31;
+    int before = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int n = 0;
+        if (b < p.B) {
+            const Seq s = seq_of(p, b);
+            n = ((over_keys ? s.nk : s.nq) + kBM - 1) / kBM;
+        }
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        if (x < before + total) {
+            const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && x < before + incl);
+            const int l = __ffs(hit) - 1;
+            const int excl = __shfl_sync(0xffffffffu, incl - n, l);
+            b_out = b0 + l;
+            t_out = x - before - excl;
+            return true;
+        }
+        before += total;
+    }
+    return false;
+}
+
+__device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); }
+
+// S-type product: D[128 x 128] = A[128 x d] B[128 x d]^T, both K-major tiles.
+template <int HD>
+__device__ __forceinline__ void issue_nt(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBM, false);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * Tile<HD>::kPanelBytes + (kk & 3) * 32) >> 4);
+        mma_smem_smem(tmem_d, a_desc + off, b_desc + off, idesc, kk > 0);
+    }
+}
+
+// Accumulating product: D[128 x d] (+)= A[128 x 128](tensor memory, bf16) B[128 x d]
+// with B a row-major tile (MN-major operand).  A is written by two softmax
+// warpgroups, each over 64 of the 128 fp32 columns of a tile: each packs its
+// 64 bf16 values into the first 32 of ITS OWN columns (a warpgroup never
+// writes columns the other one still reads), so the K elements 64h .. 64h+63
+// sit at columns 64h .. 64h+31.
+template <int HD>
+__device__ __forceinline__ void issue_tn(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc, bool first) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, HD, true);
+#pragma unroll
+    for (int kk = 0; kk < kBM / 16; ++kk)
+        mma_tmem_smem(tmem_d, tmem_a + (kk >> 2) * 64 + (kk & 3) * 8,
+                      b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc, (!first || kk > 0) ? 1u : 0u);
+}
+
+// Stores 64 bf16 values (a row segment) from fp32 registers, times `mul`.
+__device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* x, float mul) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int c = 0; c < 64; c += 8) {
+        uint4 w;
+        w.x = pack_bf16x2(x[c + 0] * mul, x[c + 1] * mul);
+        w.y = pack_bf16x2(x[c + 2] * mul, x[c + 3] * mul);
+        w.z = pack_bf16x2(x[c + 4] * mul, x[c + 5] * mul);
+        w.w = pack_bf16x2(x[c + 6] * mul, x[c + 7] * mul);
+        d4[c >> 3] = w;
+    }
+}
+
+// Reads the tensor-memory accumulator of this thread's row, columns
+// [col, col + n), and writes it as bf16 (times mul) to dst.
+template <int N>
+__device__ __forceinline__ void drain_row(uint32_t taddr, __nv_bfloat16* dst, float mul, bool store) {
+#pragma unroll 1
+    for (int c = 0; c < N; c += 64) {
+        float x[64];
+        tmem_ld_32cols_f(taddr + c, x);
+        tmem_ld_32cols_f(taddr + c + 32, x + 32);
+        tmem_ld_wait_f(x);
+        tmem_ld_wait_f(x + 32);
+        if (store) store_row64(dst + c, x, mul);
+    }
+}
+// The 32-column variant for d = 64 split over two warpgroups.
+__device__ __forceinline__ void drain_row32(uint32_t taddr, __nv_bfloat16* dst, float mul, bool store) {
+    float x[32];
+    tmem_ld_32cols_f(taddr, x);
+    tmem_ld_wait_f(x);
+    if (store) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(x[c + 0] * mul, x[c + 1] * mul);
+            w.y = pack_bf16x2(x[c + 2] * mul, x[c + 3] * mul);
+            w.z = pack_bf16x2(x[c + 4] * mul, x[c + 5] * mul);
+            w.w = pack_bf16x2(x[c + 6] * mul, x[c + 7] * mul);
+            d4[c >> 3] = w;
+        }
+    }
+}
+
+template <int HD>
+__device__ __forceinline__ void drain_half(uint32_t taddr_row, int half, __nv_bfloat16* dst_row, float mul,
+                                           bool store) {
+    // each warpgroup drains HD/2 columns of its rows
+    if (HD == 128) drain_row<64>(taddr_row + half * 64, dst_row + half * 64, mul, store);
+    else drain_row32(taddr_row + half * 32, dst_row + half * 32, mul, store);
+}
+
+// ============================================================================ D = rowsum(G o O)
+__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const __nv_bfloat16* o, const __nv_bfloat16* g,
+                                                           float* dvec, int rows, int Hq, int Nq, int d,
+                                                           int varlen, int T_q) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // token-major row t * Hq + h
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int t = row / Hq, h = row - t * Hq;
+    const __nv_bfloat16* ob = o + static_cast<size_t>(row) * d;
+    const __nv_bfloat16* gb = g + static_cast<size_t>(row) * d;
+    float acc = 0.f;
+    for (int c = lane * 2; c < d; c += 64) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(ob + c);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(gb + c);
+        acc = fmaf(__bfloat162float(a.x), __bfloat162float(b.x), acc);
+        acc = fmaf(__bfloat162float(a.y), __bfloat162float(b.y), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+        const size_t idx = varlen ? static_cast<size_t>(h) * T_q + t
+                                  : (static_cast<size_t>(t / Nq) * Hq + h) * Nq + (t % Nq);
+        dvec[idx] = acc;
+    }
+}
+
+// ============================================================================ dK, dV
+template <int HD>
+struct KvCfg {
+    static constexpr int kStages = 2;
+    // Q_i, G_i, then lse * log2 e and D of the tile's rows (2 x 128 fp32, padded to 1 KB)
+    static constexpr int kStageBytes = 2 * Tile<HD>::kBytes + 1024;
+    // at least 120 KB so that one CTA (holding all 512 tensor-memory columns) runs per SM
+    static constexpr int kNeed = 2 * Tile<HD>::kBytes + kStages * kStageBytes + 1024;
+    static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;
+    // tensor memory columns
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + HD;
+};
+
+// barriers of the K/V pass
+enum : int { KV_FULL = 0, KV_STAGE_FULL = 1, KV_STAGE_EMPTY = 3, KV_S_FULL = 5, KV_DP_FULL, KV_P_READY, KV_DS_READY,
+             KV_ACC_FULL, KV_COUNT };
+
+struct KvItem {
+    int b, g, j;
+    Seq s;
+    int k0, keys;       // first key of the tile, valid keys in it
+    int qt_lo, nqt;     // query tiles [qt_lo, qt_lo + nqt) per query head
+    int steps;          // group * nqt
+};
+
+__device__ __forceinline__ bool kv_item(const BwdParams& p, KvItem& it) {
+    const int x = blockIdx.x;
+    it.g = blockIdx.y;
+    if (!p.varlen) {
+        const int nkt = (p.Nk + kBM - 1) / kBM;
+        const int t = x / p.B;
+        it.b = x - t * p.B;
+        // a bounded right edge gives the first key tiles the most query rows
+        it.j = p.win_right >= 0 ? t : nkt - 1 - t;
+    } else if (!find_tile(p, x, true, it.b, it.j)) {
+        return false;
+    }
+    it.s = seq_of(p, it.b);
+    it.k0 = it.j * kBM;
+    it.keys = clampi(it.s.nk - it.k0, 0, kBM);
+    it.qt_lo = 0;
+    it.nqt = 0;
+    if (it.keys > 0 && it.s.nq > 0) {
+        const int i_lo = row_first(it.k0, it.s.nq, it.s.nk, p.win_right);
+        const int i_hi = row_last(it.k0 + it.keys - 1, it.s.nq, it.s.nk, p.win_left);
+        if (i_hi >= i_lo) {
+            it.qt_lo = i_lo / kBM;
+            it.nqt = i_hi / kBM + 1 - it.qt_lo;
+        }
+    }
+    it.steps = p.group * it.nqt;
+    return it.keys > 0;
+}
+
+template <int HD>
+__device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, uint32_t smem0, uint32_t bar0) {
+    using T = Tile<HD>;
+    using C = KvCfg<HD>;
+    const int lane = threadIdx.x & 31;
+    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    float* vec_base = nullptr;
+    bool ok = true;
+    if (lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_do);
+        mbar_arrive_expect_tx(bar_at(bar0, KV_FULL), 2 * T::kBytes);
+#pragma unroll
+        for (int pn = 0; pn < T::kPanels; ++pn) {
+            tma_load_2d(smem0 + pn * T::kPanelBytes, &p.tm_k, bar_at(bar0, KV_FULL), it.g * HD + pn * 64,
+                        it.s.k_base + it.k0);
+            tma_load_2d(smem0 + T::kBytes + pn * T::kPanelBytes, &p.tm_v, bar_at(bar0, KV_FULL),
+                        it.g * HD + pn * 64, it.s.k_base + it.k0);
+        }
+    }
+    for (int s = 0; s < it.steps && ok; ++s) {
+        const int st = s % C::kStages;
+        const int h = it.g * p.group + s / it.nqt;
+        const int qt = it.qt_lo + s % it.nqt;
+        const uint32_t base = stage0 + st * C::kStageBytes;
+        if (s >= C::kStages)
+            ok = __shfl_sync(0xffffffffu,
+                             lane == 0 ? mbar_wait(bar_at(bar0, KV_STAGE_EMPTY + st), ((s / C::kStages) - 1) & 1,
+                                                   p.err)
+                                       : true,
+                             0);
+        if (!ok) break;
+        const uint32_t full = bar_at(bar0, KV_STAGE_FULL + st);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(full, 2 * T::kBytes);
+#pragma unroll
+            for (int pn = 0; pn < T::kPanels; ++pn) {
+                tma_load_2d(base + pn * T::kPanelBytes, &p.tm_q, full, h * HD + pn * 64,
+                            it.s.q_base + qt * kBM);
+                tma_load_2d(base + T::kBytes + pn * T::kPanelBytes, &p.tm_do, full, h * HD + pn * 64,
+                            it.s.q_base + qt * kBM);
+            }
+        }
+        // lse (times log2 e) and D of the tile's rows; rows past the sequence get 0
+        vec_base = reinterpret_cast<float*>(__cvta_shared_to_generic(base + 2 * T::kBytes));
+        for (int r = lane; r < kBM; r += 32) {
+            const int i = qt * kBM + r;
+            float l2 = 0.f, dd = 0.f;
+            if (i < it.s.nq) {
+                const size_t li = lse_index(p, it.b, h, it.s, i);
+                l2 = __ldg(p.lse + li) * kLog2e;
+                dd = __ldg(p.dvec + li);
+            }
+            vec_base[r] = l2;
+            vec_base[kBM + r] = dd;
+        }
+        mbar_arrive(full);  // each lane releases its own stores
+    }
+    // drain: every copy issued has landed before the CTA may exit
+    if (lane == 0) {
+        mbar_wait(bar_at(bar0, KV_FULL), 0, p.err);
+        for (int s = (it.steps > C::kStages ? it.steps - C::kStages : 0); s < it.steps; ++s)
+            mbar_wait(bar_at(bar0, KV_STAGE_FULL + s % C::kStages), (s / C::kStages) & 1, p.err);
+    }
+    __syncwarp();
+}
+
+template <int HD>
+__device__ __noinline__ void kv_mma(const BwdParams& p, const KvItem& it, uint32_t smem0, uint32_t bar0,
+                                    uint32_t tmem) {
+    using T = Tile<HD>;
+    using C = KvCfg<HD>;
+    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    const uint64_t dk_desc = smem_desc_sw128(smem0, 16, 1024);               // K_j, K-major
+    const uint64_t dv_desc = smem_desc_sw128(smem0 + T::kBytes, 16, 1024);   // V_j, K-major
+    constexpr uint64_t kStageDesc = C::kStageBytes >> 4;
+    const uint64_t dq_k0 = smem_desc_sw128(stage0, 16, 1024);                      // Q_i as the B of S^T
+    const uint64_t dg_k0 = smem_desc_sw128(stage0 + T::kBytes, 16, 1024);          // G_i as the B of dP^T
+    const uint64_t dg_mn0 = smem_desc_sw128(stage0 + T::kBytes, T::kPanelBytes, 1024);  // G_i row-major B
+    const uint64_t dq_mn0 = smem_desc_sw128(stage0, T::kPanelBytes, 1024);               // Q_i row-major B
+    const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP;
+    const uint32_t t_dv = tmem + C::kColDV, t_dk = tmem + C::kColDK;
+    bool ok = mbar_wait(bar_at(bar0, KV_FULL), 0, p.err);
+    const int n = it.steps;
+    if (ok && n > 0) {
+        ok = mbar_wait(bar_at(bar0, KV_STAGE_FULL + 0), 0, p.err);
+        if (ok) {
+            tc_fence_after_sync();
+            issue_nt<HD>(t_s, dk_desc, dq_k0);
+            tc_commit(bar_at(bar0, KV_S_FULL));
+            issue_nt<HD>(t_dp, dv_desc, dg_k0);
+            tc_commit(bar_at(bar0, KV_DP_FULL));
+        }
+    }
+    for (int s = 0; s < n && ok; ++s) {
+        const int st = s % C::kStages;
+        ok = mbar_wait(bar_at(bar0, KV_P_READY), s & 1, p.err);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_tn<HD>(t_dv, t_s, dg_mn0 + st * kStageDesc, s == 0);  // dV += P^T G_i
+        const bool more = s + 1 < n;
+        const int st1 = (s + 1) % C::kStages;
+        if (more) {
+            ok = mbar_wait(bar_at(bar0, KV_STAGE_FULL + st1), ((s + 1) / C::kStages) & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_nt<HD>(t_s, dk_desc, dq_k0 + st1 * kStageDesc);  // S^T(s+1)
+            tc_commit(bar_at(bar0, KV_S_FULL));
+        }
+        ok = mbar_wait(bar_at(bar0, KV_DS_READY), s & 1, p.err);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_tn<HD>(t_dk, t_dp, dq_mn0 + st * kStageDesc, s == 0);  // dK += dS^T Q_i
+        tc_commit(bar_at(bar0, KV_STAGE_EMPTY + st));
+        if (more) {
+            issue_nt<HD>(t_dp, dv_desc, dg_k0 + st1 * kStageDesc);  // dP^T(s+1)
+            tc_commit(bar_at(bar0, KV_DP_FULL));
+        }
+    }
+    // all products done (or abandoned): the accumulators may be read
+    tc_commit(bar_at(bar0, KV_ACC_FULL));
+}
+
+template <int HD>
+__device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, uint32_t smem0, uint32_t bar0,
+                                        uint32_t tmem) {
+    using T = Tile<HD>;
+    using C = KvCfg<HD>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int half = warp >> 2;                // query columns [64 half, 64 half + 64)
+    const int r = (warp & 3) * 32 + lane;      // key row == tensor-memory lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    const int key = it.k0 + r;
+    const bool key_valid = r < it.keys;
+    // the query rows that see this key (none for rows past the sequence)
+    const int qmin = key_valid ? row_first(key, it.s.nq, it.s.nk, p.win_right) : 1;
+    const int qmax = key_valid ? row_last(key, it.s.nq, it.s.nk, p.win_left) : 0;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int s = 0; s < it.steps && ok; ++s) {
+        const int st = s % C::kStages;
+        const int qt = it.qt_lo + s % it.nqt;
+        const int c0 = qt * kBM + half * 64;  // first query of this thread's columns
+        const float* vec = reinterpret_cast<const float*>(__cvta_shared_to_generic(stage0 + st * C::kStageBytes +
+                                                                                   2 * T::kBytes));
+        // acquire the stage's vectors (written by the producer lanes before
+        // they arrived on its full barrier; the stage is not refilled before
+        // this step's dK product has read it), then S^T(s)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, KV_STAGE_FULL + st), (s / C::kStages) & 1, p.err) &&
+                                         mbar_wait(bar_at(bar0, KV_S_FULL), s & 1, p.err));
+        if (!ok) break;
+        tc_fence_after_sync();
+        float x[64];
+        tmem_ld_32cols_f(t_s + half * 64, x);
+        tmem_ld_32cols_f(t_s + half * 64 + 32, x + 32);
+        tmem_ld_wait_f(x);
+        tmem_ld_wait_f(x + 32);
+        const int lo = qmin - c0, hi = qmax - c0;  // allowed columns [lo, hi]
+        const float* l2 = vec + half * 64;
+        float pr[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            const float e = fast_exp2(fmaf(x[c], sl2, -l2[c]));
+            pr[c] = (c < lo || c > hi) ? 0.f : e;
+        }
+        {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) pk[c >> 1] = pack_bf16x2(pr[c], pr[c + 1]);
+            tmem_st_32cols(t_s + half * 64, pk);  // over this warpgroup's own S^T columns
+            tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(bar0, KV_P_READY));
+
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, KV_DP_FULL), s & 1, p.err));
+        if (!ok) break;
+        tc_fence_after_sync();
+        tmem_ld_32cols_f(t_dp + half * 64, x);
+        tmem_ld_32cols_f(t_dp + half * 64 + 32, x + 32);
+        tmem_ld_wait_f(x);
+        tmem_ld_wait_f(x + 32);
+        const float* dd = vec + kBM + half * 64;
+        {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2)
+                pk[c >> 1] = pack_bf16x2(pr[c] * (x[c] - dd[c]), pr[c + 1] * (x[c + 1] - dd[c + 1]));
+            tmem_st_32cols(t_dp + half * 64, pk);  // over this warpgroup's own dP^T columns
+            tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(bar0, KV_DS_READY));
+    }
+    // epilogue: dV and dK (times scale) of this key row, HD/2 columns per warpgroup
+    __nv_bfloat16* dk_row = p.dk + (static_cast<size_t>(it.s.k_base + key) * p.Hkv + it.g) * HD;
+    __nv_bfloat16* dv_row = p.dv + (static_cast<size_t>(it.s.k_base + key) * p.Hkv + it.g) * HD;
+    if (it.steps == 0) {  // no query sees these keys: zero gradients
+        if (key_valid) {
+            uint4* a = reinterpret_cast<uint4*>(dk_row + half * (HD / 2));
+            uint4* b = reinterpret_cast<uint4*>(dv_row + half * (HD / 2));
+            for (int c = 0; c < HD / 16; ++c) a[c] = b[c] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, KV_ACC_FULL), 0, p.err)) && ok;
+    if (!ok) return;
+    tc_fence_after_sync();
+    drain_half<HD>(tmem + lane_off + C::kColDV, half, dv_row, 1.f, key_valid);
+    drain_half<HD>(tmem + lane_off + C::kColDK, half, dk_row, p.scale, key_valid);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_dyn[];
+    __shared__ __align__(8) uint64_t bars[KV_COUNT];
+    __shared__ uint32_t tmem_slot;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    KvItem it;
+    const bool live = kv_item(p, it);  // uniform over the CTA
+    if (!live) return;
+    const uint32_t smem0 = (smem_addr(smem_dyn) + 1023u) & ~1023u;
+    const uint32_t bar0 = smem_addr(bars);
+    if (threadIdx.x == 0) {
+        mbar_init(bar_at(bar0, KV_FULL), 1);
+        for (int s = 0; s < KvCfg<HD>::kStages; ++s) {
+            mbar_init(bar_at(bar0, KV_STAGE_FULL + s), 1 + 32);  // expect_tx + 32 lanes' vector stores
+            mbar_init(bar_at(bar0, KV_STAGE_EMPTY + s), 1);
+        }
+        mbar_init(bar_at(bar0, KV_S_FULL), 1);
+        mbar_init(bar_at(bar0, KV_DP_FULL), 1);
+        mbar_init(bar_at(bar0, KV_P_READY), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, KV_DS_READY), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, KV_ACC_FULL), 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(&tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    if (warp >= 8) {
+        regs_decrease<kControlRegs>();
+        if (warp == kProducerWarp) kv_producer<HD>(p, it, smem0, bar0);
+        if (warp == kMmaWarp && lane == 0) kv_mma<HD>(p, it, smem0, bar0, tmem);
+        __syncwarp();
+    } else {
+        regs_increase<kSoftmaxRegs>();
+        kv_softmax<HD>(p, it, smem0, bar0, tmem);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================ dQ
+template <int HD>
+struct QCfg {
+    static constexpr int kStages = HD == 128 ? 2 : 4;
+    static constexpr int kStageBytes = 2 * Tile<HD>::kBytes;  // K_j, V_j
+    static constexpr int kNeed = 2 * Tile<HD>::kBytes + kStages * kStageBytes + 1024;
+    static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;  // one CTA per SM
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+};
+
+enum : int { Q_FULL = 0, Q_STAGE_FULL = 1, Q_STAGE_EMPTY = 5, Q_S_FULL = 9, Q_DP_FULL, Q_S_FREE, Q_DS_READY,
+             Q_ACC_FULL, Q_COUNT };
+
+struct QItem {
+    int b, h, i;
+    Seq s;
+    int q0, rows;   // first row of the tile, valid rows
+    int lo, n;      // K/V tiles [lo, lo + n)
+};
+
+__device__ __forceinline__ bool q_item(const BwdParams& p, QItem& it) {
+    const int x = blockIdx.x;
+    it.h = blockIdx.y;
+    if (!p.varlen) {
+        const int nqt = (p.Nq + kBM - 1) / kBM;
+        const int t = x / p.B;
+        it.b = x - t * p.B;
+        // a bounded right edge gives the last query tiles the most keys
+        it.i = p.win_right >= 0 ? nqt - 1 - t : t;
+    } else if (!find_tile(p, x, false, it.b, it.i)) {
+        return false;
+    }
+    it.s = seq_of(p, it.b);
+    it.q0 = it.i * kBM;
+    it.rows = clampi(it.s.nq - it.q0, 0, kBM);
+    it.lo = 0;
+    it.n = 0;
+    if (it.rows > 0 && it.s.nk > 0) {
+        const int kmin = key_first(it.q0, it.s.nq, it.s.nk, p.win_left);
+        const int kmax = key_last(static_cast<long long>(it.q0) + it.rows - 1, it.s.nq, it.s.nk, p.win_right);
+        if (kmax >= kmin) {
+            it.lo = kmin / kBM;
+            it.n = kmax / kBM + 1 - it.lo;
+        }
+    }
+    return it.rows > 0;
+}
+
+template <int HD>
+__device__ __noinline__ void q_producer(const BwdParams& p, const QItem& it, uint32_t smem0, uint32_t bar0) {
+    using T = Tile<HD>;
+    using C = QCfg<HD>;
+    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    const int g = it.h / p.group;
+    bool ok = true;
+    mbar_arrive_expect_tx(bar_at(bar0, Q_FULL), 2 * T::kBytes);
+#pragma unroll
+    for (int pn = 0; pn < T::kPanels; ++pn) {
+        tma_load_2d(smem0 + pn * T::kPanelBytes, &p.tm_q, bar_at(bar0, Q_FULL), it.h * HD + pn * 64,
+                    it.s.q_base + it.q0);
+        tma_load_2d(smem0 + T::kBytes + pn * T::kPanelBytes, &p.tm_do, bar_at(bar0, Q_FULL), it.h * HD + pn * 64,
+                    it.s.q_base + it.q0);
+    }
+    for (int u = 0; u < it.n && ok; ++u) {
+        const int st = u % C::kStages;
+        if (u >= C::kStages) ok = mbar_wait(bar_at(bar0, Q_STAGE_EMPTY + st), ((u / C::kStages) - 1) & 1, p.err);
+        if (!ok) break;
+        const uint32_t base = stage0 + st * C::kStageBytes;
+        const uint32_t full = bar_at(bar0, Q_STAGE_FULL + st);
+        mbar_arrive_expect_tx(full, 2 * T::kBytes);
+        const int y = it.s.k_base + (it.lo + u) * kBM;
+#pragma unroll
+        for (int pn = 0; pn < T::kPanels; ++pn) {
+            tma_load_2d(base + pn * T::kPanelBytes, &p.tm_k, full, g * HD + pn * 64, y);
+            tma_load_2d(base + T::kBytes + pn * T::kPanelBytes, &p.tm_v, full, g * HD + pn * 64, y);
+        }
+    }
+    mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
+    for (int u = (it.n > C::kStages ? it.n - C::kStages : 0); u < it.n; ++u)
+        mbar_wait(bar_at(bar0, Q_STAGE_FULL + u % C::kStages), (u / C::kStages) & 1, p.err);
+}
+
+template <int HD>
+__device__ __noinline__ void q_mma(const BwdParams& p, const QItem& it, uint32_t smem0, uint32_t bar0,
+                                   uint32_t tmem) {
+    using T = Tile<HD>;
+    using C = QCfg<HD>;
+    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    const uint64_t d_q = smem_desc_sw128(smem0, 16, 1024);               // Q_i, K-major
+    const uint64_t d_g = smem_desc_sw128(smem0 + T::kBytes, 16, 1024);   // G_i, K-major
+    constexpr uint64_t kStageDesc = C::kStageBytes >> 4;
+    const uint64_t d_k0 = smem_desc_sw128(stage0, 16, 1024);                       // K_j as the B of S
+    const uint64_t d_v0 = smem_desc_sw128(stage0 + T::kBytes, 16, 1024);           // V_j as the B of dP
+    const uint64_t d_kmn0 = smem_desc_sw128(stage0, T::kPanelBytes, 1024);         // K_j row-major B
+    const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP, t_dq = tmem + C::kColDQ;
+    const int n = it.n;
+    bool ok = mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
+    if (ok && n > 0) {
+        ok = mbar_wait(bar_at(bar0, Q_STAGE_FULL + 0), 0, p.err);
+        if (ok) {
+            tc_fence_after_sync();
+            issue_nt<HD>(t_s, d_q, d_k0);
+            tc_commit(bar_at(bar0, Q_S_FULL));
+            issue_nt<HD>(t_dp, d_g, d_v0);
+            tc_commit(bar_at(bar0, Q_DP_FULL));
+        }
+    }
+    for (int u = 0; u < n && ok; ++u) {
+        const int st = u % C::kStages;
+        const bool more = u + 1 < n;
+        const int st1 = (u + 1) % C::kStages;
+        if (more) {
+            ok = mbar_wait(bar_at(bar0, Q_S_FREE), u & 1, p.err) &&
+                 mbar_wait(bar_at(bar0, Q_STAGE_FULL + st1), ((u + 1) / C::kStages) & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_nt<HD>(t_s, d_q, d_k0 + st1 * kStageDesc);  // S(u+1)
+            tc_commit(bar_at(bar0, Q_S_FULL));
+        }
+        ok = mbar_wait(bar_at(bar0, Q_DS_READY), u & 1, p.err);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_tn<HD>(t_dq, t_dp, d_kmn0 + st * kStageDesc, u == 0);  // dQ += dS K_j
+        tc_commit(bar_at(bar0, Q_STAGE_EMPTY + st));
+        if (more) {
+            issue_nt<HD>(t_dp, d_g, d_v0 + st1 * kStageDesc);  // dP(u+1)
+            tc_commit(bar_at(bar0, Q_DP_FULL));
+        }
+    }
+    tc_commit(bar_at(bar0, Q_ACC_FULL));
+}
+
+template <int HD>
+__device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint32_t bar0, uint32_t tmem) {
+    using C = QCfg<HD>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int half = warp >> 2;                // key columns [64 half, 64 half + 64)
+    const int r = (warp & 3) * 32 + lane;      // query row == tensor-memory lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const int i = it.q0 + r;
+    const bool row_valid = r < it.rows;
+    const int nq = it.s.nq, nk = it.s.nk;
+    const int kmin = row_valid ? key_first(i, nq, nk, p.win_left) : 1;
+    const int kmax = row_valid ? key_last(i, nq, nk, p.win_right) : 0;
+    float l2 = 0.f, dd = 0.f;
+    if (row_valid) {
+        const size_t li = lse_index(p, it.b, it.h, it.s, i);
+        l2 = __ldg(p.lse + li) * kLog2e;
+        dd = __ldg(p.dvec + li);
+    }
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int u = 0; u < it.n && ok; ++u) {
+        const int k0 = (it.lo + u) * kBM + half * 64;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_S_FULL), u & 1, p.err));
+        if (!ok) break;
+        tc_fence_after_sync();
+        float x[64];
+        tmem_ld_32cols_f(t_s + half * 64, x);
+        tmem_ld_32cols_f(t_s + half * 64 + 32, x + 32);
+        tmem_ld_wait_f(x);
+        tmem_ld_wait_f(x + 32);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(bar0, Q_S_FREE));  // S may be overwritten
+        const int lo = kmin - k0, hi = kmax - k0;
+        float pr[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            const float e = fast_exp2(fmaf(x[c], sl2, -l2));
+            pr[c] = (c < lo || c > hi) ? 0.f : e;
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_DP_FULL), u & 1, p.err));
+        if (!ok) break;
+        tc_fence_after_sync();
+        tmem_ld_32cols_f(t_dp + half * 64, x);
+        tmem_ld_32cols_f(t_dp + half * 64 + 32, x + 32);
+        tmem_ld_wait_f(x);
+        tmem_ld_wait_f(x + 32);
+        {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) pk[c >> 1] = pack_bf16x2(pr[c] * (x[c] - dd), pr[c + 1] * (x[c + 1] - dd));
+            tmem_st_32cols(t_dp + half * 64, pk);  // over this warpgroup's own dP columns
+            tmem_st_wait();
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_at(bar0, Q_DS_READY));
+    }
+    __nv_bfloat16* dq_row = p.dq + (static_cast<size_t>(it.s.q_base + i) * p.Hq + it.h) * HD;
+    if (it.n == 0) {  // no key: zero gradient
+        if (row_valid) {
+            uint4* a = reinterpret_cast<uint4*>(dq_row + half * (HD / 2));
+            for (int c = 0; c < HD / 16; ++c) a[c] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_ACC_FULL), 0, p.err)) && ok;
+    if (!ok) return;
+    tc_fence_after_sync();
+    drain_half<HD>(tmem + lane_off + C::kColDQ, half, dq_row, p.scale, row_valid);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_dyn[];
+    __shared__ __align__(8) uint64_t bars[Q_COUNT];
+    __shared__ uint32_t tmem_slot;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    QItem it;
+    if (!q_item(p, it)) return;  // uniform over the CTA
+    const uint32_t smem0 = (smem_addr(smem_dyn) + 1023u) & ~1023u;
+    const uint32_t bar0 = smem_addr(bars);
+    if (threadIdx.x == 0) {
+        mbar_init(bar_at(bar0, Q_FULL), 1);
+        for (int s = 0; s < QCfg<HD>::kStages; ++s) {
+            mbar_init(bar_at(bar0, Q_STAGE_FULL + s), 1);
+            mbar_init(bar_at(bar0, Q_STAGE_EMPTY + s), 1);
+        }
+        mbar_init(bar_at(bar0, Q_S_FULL), 1);
+        mbar_init(bar_at(bar0, Q_DP_FULL), 1);
+        mbar_init(bar_at(bar0, Q_S_FREE), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, Q_DS_READY), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, Q_ACC_FULL), 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(&tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_do);
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+    if (warp >= 8) {
+        regs_decrease<kControlRegs>();
+        if (warp == kProducerWarp && lane == 0) q_producer<HD>(p, it, smem0, bar0);
+        if (warp == kMmaWarp && lane == 0) q_mma<HD>(p, it, smem0, bar0, tmem);
+        __syncwarp();
+    } else {
+        regs_increase<kSoftmaxRegs>();
+        q_softmax<HD>(p, it, bar0, tmem);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// ============================================================================ host
+template <typename K>
+attn_status prepare_kernel(K kernel, int smem_bytes, bool& done) {
+    if (done) return ATTN_OK;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) {
+        set_error_message("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) {
+        set_error_message("cudaFuncGetAttributes: %s", cudaGetErrorString(e));
+        return ATTN_ERR_CUDA;
+    }
+    if (fa.numRegs * kThreads < 2 * 128 * kSoftmaxRegs + 128 * kControlRegs) {
+        set_error_message("attn_bwd kernel built with %d registers/thread; the warpgroup split needs %d",
+                          fa.numRegs, kLaunchRegs);
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    done = true;
+    return ATTN_OK;
+}
+
+template <int HD>
+attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+    BwdParams p;
+    memset(&p, 0, sizeof(p));
+    const bool varlen = a.cu_q != nullptr;
+    const uint64_t t_q = varlen ? static_cast<uint64_t>(a.Nq) : static_cast<uint64_t>(a.B) * a.Nq;
+    uint64_t t_k = varlen ? static_cast<uint64_t>(a.Nk) : static_cast<uint64_t>(a.B) * a.Nk;
+    const uint32_t box[2] = {64, kBM};
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hq) * HD, t_q};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hq) * HD * 2};
+        attn_status st = encode_tma_bf16(&p.tm_q, a.q, 2, dims, strides, box, true);
+        if (st == ATTN_OK) st = encode_tma_bf16(&p.tm_do, a.dout, 2, dims, strides, box, true);
+        if (st != ATTN_OK) return st;
+    }
+    {
+        const bool no_keys = t_k == 0;
+        if (no_keys) t_k = 1;  // never read; a zero extent is not encodable
+        const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, t_k};
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
+        attn_status st = encode_tma_bf16(&p.tm_k, no_keys ? a.q : a.k, 2, dims, strides, box, true);
+        if (st == ATTN_OK) st = encode_tma_bf16(&p.tm_v, no_keys ? a.q : a.v, 2, dims, strides, box, true);
+        if (st != ATTN_OK) return st;
+    }
+    p.lse = a.lse;
+    p.dvec = static_cast<float*>(a.workspace);
+    p.dq = static_cast<__nv_bfloat16*>(a.dq);
+    p.dk = static_cast<__nv_bfloat16*>(a.dk);
+    p.dv = static_cast<__nv_bfloat16*>(a.dv);
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = a.Hq / a.Hkv;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.win_left = a.win_left < 0 ? -1 : a.win_left;
+    p.win_right = a.causal ? 0 : (a.win_right < 0 ? -1 : a.win_right);
+    p.varlen = varlen ? 1 : 0;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * kLog2e;
+    p.err = dev.err_word;
+
+    // D = rowsum(G o O)
+    const long long rows = static_cast<long long>(t_q) * a.Hq;
+    if (rows > 0) {
+        attn_bwd_dot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout),
+            static_cast<float*>(a.workspace),
+            static_cast<int>(rows), a.Hq, varlen ? 1 : a.Nq, HD, varlen ? 1 : 0, static_cast<int>(t_q));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error_message("attn_bwd_dot launch: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+    }
+    static bool ready_kv[2] = {false, false}, ready_q[2] = {false, false};
+    attn_status st = prepare_kernel(attn_bwd_dkdv_kernel<HD>, KvCfg<HD>::kSmemBytes, ready_kv[HD == 128]);
+    if (st == ATTN_OK) st = prepare_kernel(attn_bwd_dq_kernel<HD>, QCfg<HD>::kSmemBytes, ready_q[HD == 128]);
+    if (st != ATTN_OK) return st;
+    // grids: dense = (tiles x B, heads); packed = an upper bound on the
+    // (sequence, tile) entries, the surplus CTAs return at once
+    const long long kv_x = varlen ? static_cast<long long>(a.Nk) / kBM + a.B
+                                  : static_cast<long long>((a.Nk + kBM - 1) / kBM) * a.B;
+    const long long q_x = varlen ? static_cast<long long>(a.Nq) / kBM + a.B
+                                 : static_cast<long long>((a.Nq + kBM - 1) / kBM) * a.B;
+    if (kv_x > 0x7fffffffLL || q_x > 0x7fffffffLL) {
+        set_error_message("attn_bwd: too many tiles");
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    if (kv_x > 0) {
+        attn_bwd_dkdv_kernel<HD><<<dim3(static_cast<unsigned>(kv_x), a.Hkv), kThreads, KvCfg<HD>::kSmemBytes,
+                                   stream>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error_message("attn_bwd_dkdv launch: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+    }
+    if (q_x > 0) {
+        attn_bwd_dq_kernel<HD><<<dim3(static_cast<unsigned>(q_x), a.Hq), kThreads, QCfg<HD>::kSmemBytes,
+                                 stream>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) {
+            set_error_message("attn_bwd_dq launch: %s", cudaGetErrorString(e));
+            return ATTN_ERR_CUDA;
+        }
+    }
+    return ATTN_OK;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int Hq, int Nq, bool varlen) {
+    const size_t t_q = varlen ? static_cast<size_t>(Nq) : static_cast<size_t>(B) * Nq;
+    return (t_q * Hq * sizeof(float) + 255) / 256 * 256;
+}
+
+attn_status launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+    DeviceInfo dev;
+    attn_status st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    if (a.d == 128) return launch_typed<128>(a, dev, stream);
+    if (a.d == 64) return launch_typed<64>(a, dev, stream);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace attn

@@ -46,6 +46,20 @@ struct FwdArgs {
 };
 attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
+struct BwdArgs {
+    const void *q, *k, *v, *out, *dout;  // out = the forward output O, dout = dL/dO
+    const float* lse;                    // the forward lse (natural log)
+    void *dq, *dk, *dv;
+    void* workspace;                     // D = rowsum(dout o out), fp32 in the lse layout
+    int B, Hq, Hkv, Nq, Nk, d;
+    float scale;
+    int causal;
+    int win_left, win_right;
+    const int *cu_q, *cu_k;
+};
+size_t bwd_workspace_bytes(int B, int Hq, int Nq, bool varlen);
+attn_status launch_bwd(const BwdArgs& a, cudaStream_t stream);
+
 struct DecodeArgs {
     const void* q;                  // [B, nq, Hq, d]
     const void *k_cache, *v_cache;

@@ -122,6 +122,49 @@ attn_status attn_fwd_window(const void *q, const void *k, const void *v,
                             void *stream);
 
 /*
+ * attn_bwd -- gradients dQ, dK, dV of a loss L through attn_fwd /
+ * attn_fwd_window, given G = dL/dO, by recomputation.
+ *
+ * Operation: "Deep Dive - FlashAttention", section "Backward recomputes tiles
+ * on purpose", and "FlashAttention: Part 1", section 3.6.  The forward saved
+ * only O and lse; each probability tile is rebuilt as P = exp(S - lse) with
+ * the forward's mask, and for every nonempty row
+ *     dV = P^T G,   dP = G V^T,   D = rowsum(G o O),   dS = P o (dP - D),
+ *     dQ = scale * dS K,   dK = scale * dS^T Q,
+ * masked probabilities and their gradients being zero.  With grouped heads
+ * the K/V gradients of a K/V head are summed over its Hq / Hkv query heads.
+ * Three kernels: D, then dK/dV with K/V tiles resident, then dQ with query
+ * tiles resident (no atomic accumulation: the result is deterministic).
+ *
+ * Arguments: q, k, v, B, Hq, Hkv, Nq, Nk, d, scale, causal, window_left,
+ * window_right, cu_seqlens_q, cu_seqlens_k exactly as given to the forward
+ * call; out and lse are the forward's outputs; dout = G, laid out like out.
+ *   dq [T_q, Hq, d], dk and dv [T_k, Hkv, d], bf16 (written; every row is
+ *   written, rows no query attends get 0).
+ *   workspace: caller-owned device scratch of attn_bwd_workspace_size(B, Hq,
+ *   Nq, packed) bytes, 256-byte aligned; it holds D (fp32) between the
+ *   kernels, needs no initialisation and is meaningless afterwards.
+ * k, v, dk, dv may be NULL only when Nk == 0.
+ * Rejects (ATTN_ERR_INVALID_ARG): the forward's cases, NULL out/dout/dq/
+ * workspace, a workspace that is too small or not 256-byte aligned.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v,
+                     const void *out, const void *dout, const float *lse,
+                     void *dq, void *dk, void *dv,
+                     int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                     float scale, int causal, int window_left, int window_right,
+                     const int *cu_seqlens_q, const int *cu_seqlens_k,
+                     void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: 4 * Hq * T_q
+ * rounded up to 256, with T_q = B * Nq (packed = 0) or Nq (packed = 1, Nq the
+ * total query rows).  0 for invalid arguments.  Pure host arithmetic.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int packed);
+
+/*
  * attn_decode_paged -- one new query per sequence over a paged K/V cache,
  * split along the keys (split-KV) with a log-sum-exp combine.
  *

@@ -78,7 +78,7 @@ def _load():
             lib.oracle_decode_rows.restype = I
             lib.oracle_decode_multi_rows.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, D, I, P, L, P, P, I]
             lib.oracle_decode_multi_rows.restype = I
-            lib.oracle_backward.argtypes = [P, P, P, P, I, I, I, I, I, I, D, I, I, I, P, P, P, L, P, P, P, I]
+            lib.oracle_backward.argtypes = [P, P, P, P, I, I, I, I, I, I, D, I, I, I, P, P, P, L, L, P, P, P, I]
             lib.oracle_backward.restype = I
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
@@ -241,10 +241,11 @@ def decode_kvcache(p, rows=None, threads: int = 0):
                              rows=rows, threads=threads)
 
 
-def backward(p, g, pairs=None, threads: int = 0):
+def backward(p, g, pairs=None, threads: int = 0, row_stride: int = 1):
     """dQ, dK, dV (fp64 numpy, shaped like q, k, v) of L = <g, O> for a
     workloads.Prefill problem; g is bf16 like q.  pairs: (b, kv head) pairs
-    to compute (default: all); rows outside them are zero."""
+    to compute (default: all); rows outside them are zero.  row_stride > 1
+    processes every row_stride-th query row only (a timing sample)."""
     qb, kb, vb, gb = _bits(p.q), _bits(p.k), _bits(p.v), _bits(g)
     if pairs is None:
         pairs = [(b, h) for b in range(p.B) for h in range(p.Hkv)]
@@ -255,7 +256,7 @@ def backward(p, g, pairs=None, threads: int = 0):
     left, right = (int(x) for x in getattr(p, "window", (-1, -1)))
     rc = _load().oracle_backward(_ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), p.B, p.Hq, p.Hkv, p.Nq, p.Nk,
                                  int(p.d), float(p.scale), int(bool(p.causal)), left, right,
-                                 _ptr(_i32(p.cu_q)), _ptr(_i32(p.cu_k)), _ptr(pr), pr.shape[0],
+                                 _ptr(_i32(p.cu_q)), _ptr(_i32(p.cu_k)), _ptr(pr), pr.shape[0], int(row_stride),
                                  _ptr(dq), _ptr(dk), _ptr(dv), threads if threads > 0 else num_threads())
     if rc != 0:
         raise ValueError(f"oracle_backward rejected its arguments (status {rc})")

@@ -443,6 +443,7 @@ typedef struct {
     const int32_t *cu_q, *cu_k;
     const int32_t *pairs;            /* (b, kv head) pairs to compute */
     long n_pairs;
+    long row_stride;                 /* 1: every row; k: rows i = 0, k, 2k, ... (a timing sample) */
     double *dq, *dk, *dv;
     long max_keys;
     long next;
@@ -466,7 +467,7 @@ static void bwd_pair(bwd_job *jb, long r, double *sc, double *p, double *dp)
         nk = jb->Nk;
     }
     for (int h = g * group; h < (g + 1) * group; ++h) {
-        for (long i = 0; i < nq; ++i) {
+        for (long i = 0; i < nq; i += jb->row_stride) {
             const uint16_t *q_row = jb->q + ((q_first + i) * jb->Hq + h) * (long)d;
             const uint16_t *g_row = jb->g + ((q_first + i) * jb->Hq + h) * (long)d;
             double *dq_row = jb->dq + ((q_first + i) * jb->Hq + h) * (long)d;
@@ -545,16 +546,20 @@ static void *bwd_worker(void *arg)
  * (n_pairs pairs; each pair covers its group's query heads), dense or packed
  * like oracle_prefill_rows_window.  g [T_q, Hq, d] bf16 bits.  dq [T_q, Hq, d],
  * dk/dv [T_k, Hkv, d] fp64: the rows of the listed pairs are overwritten (dq)
- * or accumulated into (dk, dv: the caller zero-fills them).
+ * or accumulated into (dk, dv: the caller zero-fills them).  row_stride > 1
+ * takes only rows 0, row_stride, 2 row_stride, ... of each sequence (their
+ * contributions; a timing sample, not a gradient).
  * Returns 0, or -1 for invalid arguments, -2 when out of memory.
  */
 int oracle_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *g,
                     int B, int Hq, int Hkv, int Nq, int Nk, int d,
                     double scale, int causal, int win_left, int win_right,
                     const int32_t *cu_q, const int32_t *cu_k,
-                    const int32_t *pairs, long n_pairs,
+                    const int32_t *pairs, long n_pairs, long row_stride,
                     double *dq, double *dk, double *dv, int n_threads)
 {
+    if (row_stride < 1)
+        return -1;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || n_pairs < 0)
         return -1;
     if ((cu_q == NULL) != (cu_k == NULL))
@@ -578,6 +583,7 @@ int oracle_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v, con
     jb.scale = scale;
     jb.cu_q = cu_q; jb.cu_k = cu_k;
     jb.pairs = pairs; jb.n_pairs = n_pairs;
+    jb.row_stride = row_stride;
     jb.dq = dq; jb.dk = dk; jb.dv = dv;
     jb.max_keys = max_keys;
     if (n_threads <= 0)

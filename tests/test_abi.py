@@ -98,6 +98,27 @@ def test_decode_host_rejections(lib):
     assert dec(lib, B=0) == 0
 
 
+def bwd(lib, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, causal=1, wl=-1, wr=-1, ws=ctypes.c_void_p(0x100000),
+        ws_bytes=1 << 20, dout=FAKE):
+    return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, dout, FAKE, FAKE, FAKE, FAKE, B, Hq, Hkv, Nq, Nk, d, 0.1, causal,
+                        wl, wr, None, None, ws, ws_bytes, None)
+
+
+def test_bwd_host_rejections(lib):
+    assert bwd(lib, dout=None) == -1
+    assert bwd(lib, Hq=5) == -1
+    assert bwd(lib, causal=3) == -1
+    assert bwd(lib, wl=-2) == -1
+    assert bwd(lib, ws=None) == -1
+    assert bwd(lib, ws=ctypes.c_void_p(0x100010)) == -1      # workspace not 256-byte aligned
+    assert bwd(lib, ws_bytes=16, Nq=4096) == -1              # workspace too small
+    assert bwd(lib, d=96) == -2
+    assert bwd(lib, B=0) == 0
+    assert lib.attn_bwd_workspace_size(4, 16, 4096, 0) == 4 * 16 * 4096 * 4
+    assert lib.attn_bwd_workspace_size(1, 3, 5, 1) == 256
+    assert lib.attn_bwd_workspace_size(1, 0, 5, 0) == 0
+
+
 def kvc(lib, B=2, Nq=4, Hq=8, Hkv=2, causal=1, kn=FAKE, vn=FAKE, ws_bytes=1 << 30):
     return lib.attn_decode_kvcache(FAKE, kn, vn, FAKE, FAKE, FAKE, 4, FAKE, FAKE, FAKE, B, Nq, Hq, Hkv, 128, 16,
                                    10, 0.1, causal, 0, ctypes.c_void_p(0x100000), ws_bytes, None)

@@ -49,6 +49,11 @@ def test_decode_bytes():
     assert bench.decode_bytes(d) == kv + 2 * 2 * 8 * 128 * 2 + 4 * 2 * 8 + 4 * (2 + 2) + 4 * 2
 
 
+def test_backward_flops():
+    p = workloads.make_prefill(4, 16, 16, 4096, 4096, 128, causal=True, seed=1)
+    assert bench.backward_flops(p) == 2.5 * bench.prefill_flops(p)
+
+
 def test_kvcache_bytes():
     p = workloads.make_kvcache_decode([17, 32], 3, 8, 2, 128, num_pages=8, seed=1, append=True)
     kv = (17 + 32) * 2 * 128 * 2 * 2
