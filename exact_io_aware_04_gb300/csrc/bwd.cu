@@ -7,7 +7,7 @@
 //   dQ = scale dS K,  dK = scale dS^T Q,
 // and masked probabilities (and their gradients) are zero.  Three kernels:
 //
-//   attn_bwd_dot_kernel   D = rowsum(G o O) in fp32, one warp per row.
+//   attn_bwd_dot_kernel   D = rowsum(G o O) in fp32, d/8 threads per row.
 //   attn_bwd_dkdv_kernel  one CTA per (sequence, K/V head, 128-key tile): K_j
 //                         and V_j stay in shared memory while the (Q_i, G_i)
 //                         tiles of every query head of the group stream past;
@@ -60,7 +60,11 @@ struct Tile {
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 2-D [rows, heads*d] bf16, box 64 x 128, 128B swizzle
     const float* lse;                      // dense [B, Hq, Nq]; packed [Hq, T_q]
-    const float* dvec;                     // D, same layout as lse
+    // workspace: lse * log2 e and D, each [Hq][ws_row] fp32; sequence b's
+    // rows start at ws_offset(b), so every 128-row tile starts 16-byte aligned
+    const float* lse2;
+    const float* dvec;
+    long long ws_row;
     __nv_bfloat16 *dq, *dk, *dv;
     const int *cu_q, *cu_k;
     int B, Hq, Hkv, group, Nq, Nk;
@@ -125,6 +129,17 @@ __device__ __forceinline__ size_t lse_index(const BwdParams& p, int b, int h, co
                     : (static_cast<size_t>(b) * p.Hq + h) * p.Nq + i;
 }
 
+// First workspace element of sequence b (first query row q_base): 16-byte
+// aligned, and far enough from sequence b-1's rows.
+__host__ __device__ __forceinline__ long long ws_offset(int b, long long q_base) {
+    return 4 * ((q_base + 3) / 4) + 4LL * b;
+}
+// Row length of one head in the workspace: every sequence's offset plus a full
+// 128-row tile past the last row (a multiple of 4 floats).
+__host__ __device__ __forceinline__ long long bwd_ws_row(int B, long long t_q) {
+    return ws_offset(B, t_q) + kBM + 4;
+}
+
 // Sequence b and tile t of item x of the packed-mode list: the tiles of
 // sequence b (of `rows_per_tile`-row tiles over its nq or nk rows) come after
 // those of sequences 0..b-1.  One warp scans cu_seqlens 32 sequences at a time.
@@ -159,6 +174,15 @@ __device__ bool find_tile(const BwdParams& p, int x, bool over_keys, int& b_out,
 }
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); }
+
+// 64 consecutive fp32 values at shared address `saddr` (16-byte aligned), as 16 vector loads.
+__device__ __forceinline__ void lds_64(uint32_t saddr, float* r) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(r[4 * i]), "=f"(r[4 * i + 1]), "=f"(r[4 * i + 2]), "=f"(r[4 * i + 3])
+                     : "r"(saddr + 16u * i));
+}
 
 // S-type product: D[128 x 128] = A[128 x d] B[128 x d]^T, both K-major tiles.
 template <int HD>
@@ -242,28 +266,52 @@ __device__ __forceinline__ void drain_half(uint32_t taddr_row, int half, __nv_bf
 }
 
 // ============================================================================ D = rowsum(G o O)
-__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const __nv_bfloat16* o, const __nv_bfloat16* g,
-                                                           float* dvec, int rows, int Hq, int Nq, int d,
-                                                           int varlen, int T_q) {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);  // token-major row t * Hq + h
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const int t = row / Hq, h = row - t * Hq;
-    const __nv_bfloat16* ob = o + static_cast<size_t>(row) * d;
-    const __nv_bfloat16* gb = g + static_cast<size_t>(row) * d;
+// d/8 threads per row, each with one 16-byte load of O and of G; the rows of
+// a warp are consecutive, so a warp reads contiguous memory.  Every lane of a
+// warp runs the same iterations (rows past the end contribute nothing), so
+// the shuffle reduction always has the full warp.  Also writes lse * log2 e,
+// both into the padded workspace layout the K/V pass copies tile by tile.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const BwdParams p, const __nv_bfloat16* o,
+                                                           const __nv_bfloat16* g, float* lse2, float* dvec,
+                                                           long long rows) {
+    constexpr int kTpr = HD / 8;              // threads per row
+    constexpr int kRowsPerBlock = 256 / kTpr;
+    const int sub = threadIdx.x % kTpr;
+    const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kTpr;
     float acc = 0.f;
-    for (int c = lane * 2; c < d; c += 64) {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(ob + c);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(gb + c);
-        acc = fmaf(__bfloat162float(a.x), __bfloat162float(b.x), acc);
-        acc = fmaf(__bfloat162float(a.y), __bfloat162float(b.y), acc);
+    if (row < rows) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * HD) + sub);
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(g + row * HD) + sub);
+        const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+        const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(bf16_lo(aw[i]), bf16_lo(bw[i]), acc);
+            acc = fmaf(bf16_hi(aw[i]), bf16_hi(bw[i]), acc);
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        const size_t idx = varlen ? static_cast<size_t>(h) * T_q + t
-                                  : (static_cast<size_t>(t / Nq) * Hq + h) * Nq + (t % Nq);
-        dvec[idx] = acc;
+    for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && sub == 0) {
+        const int t = static_cast<int>(row / p.Hq);   // token
+        const int h = static_cast<int>(row - static_cast<long long>(t) * p.Hq);
+        int b;
+        if (!p.varlen) {
+            b = t / p.Nq;
+        } else {  // the sequence holding token t: last b with cu_q[b] <= t
+            int lo = 0, hi = p.B;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid;
+            }
+            b = lo;
+        }
+        const Seq s = seq_of(p, b);
+        const int i = t - s.q_base;
+        const long long w = static_cast<long long>(h) * p.ws_row + ws_offset(b, s.q_base) + i;
+        lse2[w] = __ldg(p.lse + lse_index(p, b, h, s, i)) * kLog2e;
+        dvec[w] = acc;
     }
 }
 
@@ -327,7 +375,6 @@ __device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, u
     using C = KvCfg<HD>;
     const int lane = threadIdx.x & 31;
     const uint32_t stage0 = smem0 + 2 * T::kBytes;
-    float* vec_base = nullptr;
     bool ok = true;
     if (lane == 0) {
         tma_prefetch_map(&p.tm_q);
@@ -355,7 +402,7 @@ __device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, u
         if (!ok) break;
         const uint32_t full = bar_at(bar0, KV_STAGE_FULL + st);
         if (lane == 0) {
-            mbar_arrive_expect_tx(full, 2 * T::kBytes);
+            mbar_arrive_expect_tx(full, 2 * T::kBytes + 2 * kBM * 4);
 #pragma unroll
             for (int pn = 0; pn < T::kPanels; ++pn) {
                 tma_load_2d(base + pn * T::kPanelBytes, &p.tm_q, full, h * HD + pn * 64,
@@ -363,21 +410,12 @@ __device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, u
                 tma_load_2d(base + T::kBytes + pn * T::kPanelBytes, &p.tm_do, full, h * HD + pn * 64,
                             it.s.q_base + qt * kBM);
             }
+            // lse * log2 e and D of the tile's rows (rows past the sequence
+            // hold other values: every use of them is masked by a select)
+            const long long w = static_cast<long long>(h) * p.ws_row + ws_offset(it.b, it.s.q_base) + qt * kBM;
+            bulk_load(base + 2 * T::kBytes, p.lse2 + w, kBM * 4, full);
+            bulk_load(base + 2 * T::kBytes + kBM * 4, p.dvec + w, kBM * 4, full);
         }
-        // lse (times log2 e) and D of the tile's rows; rows past the sequence get 0
-        vec_base = reinterpret_cast<float*>(__cvta_shared_to_generic(base + 2 * T::kBytes));
-        for (int r = lane; r < kBM; r += 32) {
-            const int i = qt * kBM + r;
-            float l2 = 0.f, dd = 0.f;
-            if (i < it.s.nq) {
-                const size_t li = lse_index(p, it.b, h, it.s, i);
-                l2 = __ldg(p.lse + li) * kLog2e;
-                dd = __ldg(p.dvec + li);
-            }
-            vec_base[r] = l2;
-            vec_base[kBM + r] = dd;
-        }
-        mbar_arrive(full);  // each lane releases its own stores
     }
     // drain: every copy issued has landed before the CTA may exit
     if (lane == 0) {
@@ -467,8 +505,7 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
         const int st = s % C::kStages;
         const int qt = it.qt_lo + s % it.nqt;
         const int c0 = qt * kBM + half * 64;  // first query of this thread's columns
-        const float* vec = reinterpret_cast<const float*>(__cvta_shared_to_generic(stage0 + st * C::kStageBytes +
-                                                                                   2 * T::kBytes));
+        const uint32_t vec = stage0 + st * C::kStageBytes + 2 * T::kBytes;  // lse*log2e [128], then D [128]
         // acquire the stage's vectors (written by the producer lanes before
         // they arrived on its full barrier; the stage is not refilled before
         // this step's dK product has read it), then S^T(s)
@@ -482,12 +519,17 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
         tmem_ld_wait_f(x);
         tmem_ld_wait_f(x + 32);
         const int lo = qmin - c0, hi = qmax - c0;  // allowed columns [lo, hi]
-        const float* l2 = vec + half * 64;
         float pr[64];
+        lds_64(vec + half * 64 * 4, pr);  // lse*log2e of this thread's 64 query columns
+        if (lo <= 0 && hi >= 63) {        // every column allowed (the common case)
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const float e = fast_exp2(fmaf(x[c], sl2, -l2[c]));
-            pr[c] = (c < lo || c > hi) ? 0.f : e;
+            for (int c = 0; c < 64; ++c) pr[c] = fast_exp2(fmaf(x[c], sl2, -pr[c]));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float e = fast_exp2(fmaf(x[c], sl2, -pr[c]));
+                pr[c] = (c < lo || c > hi) ? 0.f : e;
+            }
         }
         {
             uint32_t pk[32];
@@ -507,8 +549,13 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
         tmem_ld_32cols_f(t_dp + half * 64 + 32, x + 32);
         tmem_ld_wait_f(x);
         tmem_ld_wait_f(x + 32);
-        const float* dd = vec + kBM + half * 64;
         {
+            float dd[64];
+            lds_64(vec + (kBM + half * 64) * 4, dd);  // D of this thread's 64 query columns
+            if (!(lo <= 0 && hi >= 63)) {  // masked columns: D may be any bits there
+#pragma unroll
+                for (int c = 0; c < 64; ++c) dd[c] = (c < lo || c > hi) ? x[c] : dd[c];
+            }
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 64; c += 2)
@@ -553,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     if (threadIdx.x == 0) {
         mbar_init(bar_at(bar0, KV_FULL), 1);
         for (int s = 0; s < KvCfg<HD>::kStages; ++s) {
-            mbar_init(bar_at(bar0, KV_STAGE_FULL + s), 1 + 32);  // expect_tx + 32 lanes' vector stores
+            mbar_init(bar_at(bar0, KV_STAGE_FULL + s), 1);
             mbar_init(bar_at(bar0, KV_STAGE_EMPTY + s), 1);
         }
         mbar_init(bar_at(bar0, KV_S_FULL), 1);
@@ -738,9 +785,9 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
     const int kmax = row_valid ? key_last(i, nq, nk, p.win_right) : 0;
     float l2 = 0.f, dd = 0.f;
     if (row_valid) {
-        const size_t li = lse_index(p, it.b, it.h, it.s, i);
-        l2 = __ldg(p.lse + li) * kLog2e;
-        dd = __ldg(p.dvec + li);
+        const long long w = static_cast<long long>(it.h) * p.ws_row + ws_offset(it.b, it.s.q_base) + i;
+        l2 = __ldg(p.lse2 + w);
+        dd = __ldg(p.dvec + w);
     }
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -759,10 +806,15 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
         if (lane == 0) mbar_arrive(bar_at(bar0, Q_S_FREE));  // S may be overwritten
         const int lo = kmin - k0, hi = kmax - k0;
         float pr[64];
+        if (lo <= 0 && hi >= 63) {  // every column allowed (the common case)
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const float e = fast_exp2(fmaf(x[c], sl2, -l2));
-            pr[c] = (c < lo || c > hi) ? 0.f : e;
+            for (int c = 0; c < 64; ++c) pr[c] = fast_exp2(fmaf(x[c], sl2, -l2));
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float e = fast_exp2(fmaf(x[c], sl2, -l2));
+                pr[c] = (c < lo || c > hi) ? 0.f : e;
+            }
         }
         ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_DP_FULL), u & 1, p.err));
         if (!ok) break;
@@ -898,7 +950,9 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         if (st != ATTN_OK) return st;
     }
     p.lse = a.lse;
-    p.dvec = static_cast<float*>(a.workspace);
+    p.ws_row = bwd_ws_row(a.B, varlen ? a.Nq : static_cast<long long>(a.B) * a.Nq);
+    p.lse2 = static_cast<float*>(a.workspace);
+    p.dvec = static_cast<float*>(a.workspace) + p.ws_row * a.Hq;
     p.dq = static_cast<__nv_bfloat16*>(a.dq);
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
@@ -920,10 +974,11 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     // D = rowsum(G o O)
     const long long rows = static_cast<long long>(t_q) * a.Hq;
     if (rows > 0) {
-        attn_bwd_dot_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.dout),
-            static_cast<float*>(a.workspace),
-            static_cast<int>(rows), a.Hq, varlen ? 1 : a.Nq, HD, varlen ? 1 : 0, static_cast<int>(t_q));
+        constexpr int kRowsPerBlock = 256 / (HD / 8);
+        attn_bwd_dot_kernel<HD><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0,
+                                  stream>>>(p, static_cast<const __nv_bfloat16*>(a.out),
+                                            static_cast<const __nv_bfloat16*>(a.dout), const_cast<float*>(p.lse2),
+                                            const_cast<float*>(p.dvec), rows);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error_message("attn_bwd_dot launch: %s", cudaGetErrorString(e));
@@ -968,8 +1023,8 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
 }  // namespace
 
 size_t bwd_workspace_bytes(int B, int Hq, int Nq, bool varlen) {
-    const size_t t_q = varlen ? static_cast<size_t>(Nq) : static_cast<size_t>(B) * Nq;
-    return (t_q * Hq * sizeof(float) + 255) / 256 * 256;
+    const long long t_q = varlen ? static_cast<long long>(Nq) : static_cast<long long>(B) * Nq;
+    return (static_cast<size_t>(2 * Hq) * bwd_ws_row(B, t_q) * sizeof(float) + 255) / 256 * 256;
 }
 
 attn_status launch_bwd(const BwdArgs& a, cudaStream_t stream) {

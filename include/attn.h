@@ -142,8 +142,8 @@ attn_status attn_fwd_window(const void *q, const void *k, const void *v,
  *   dq [T_q, Hq, d], dk and dv [T_k, Hkv, d], bf16 (written; every row is
  *   written, rows no query attends get 0).
  *   workspace: caller-owned device scratch of attn_bwd_workspace_size(B, Hq,
- *   Nq, packed) bytes, 256-byte aligned; it holds D (fp32) between the
- *   kernels, needs no initialisation and is meaningless afterwards.
+ *   Nq, packed) bytes, 256-byte aligned; it holds D and lse * log2(e) (fp32)
+ *   between the kernels, needs no initialisation and is meaningless afterwards.
  * k, v, dk, dv may be NULL only when Nk == 0.
  * Rejects (ATTN_ERR_INVALID_ARG): the forward's cases, NULL out/dout/dq/
  * workspace, a workspace that is too small or not 256-byte aligned.
@@ -158,9 +158,12 @@ attn_status attn_bwd(const void *q, const void *k, const void *v,
                      void *stream);
 
 /*
- * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: 4 * Hq * T_q
- * rounded up to 256, with T_q = B * Nq (packed = 0) or Nq (packed = 1, Nq the
- * total query rows).  0 for invalid arguments.  Pure host arithmetic.
+ * attn_bwd_workspace_size -- bytes of scratch attn_bwd needs: lse * log2(e)
+ * and D for every query row and head, each per head in a row of
+ * 4*ceil(T_q/4) + 4*B + 132 floats (every sequence's rows start 16-byte
+ * aligned so that 128-row tiles are copied in one transfer), rounded up to 256
+ * bytes; T_q = B * Nq (packed = 0) or Nq (packed = 1, Nq the total query
+ * rows).  0 for invalid arguments.  Pure host arithmetic.
  */
 size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int packed);
 

@@ -114,8 +114,9 @@ def test_bwd_host_rejections(lib):
     assert bwd(lib, ws_bytes=16, Nq=4096) == -1              # workspace too small
     assert bwd(lib, d=96) == -2
     assert bwd(lib, B=0) == 0
-    assert lib.attn_bwd_workspace_size(4, 16, 4096, 0) == 4 * 16 * 4096 * 4
-    assert lib.attn_bwd_workspace_size(1, 3, 5, 1) == 256
+    # per head: 4*ceil(T_q/4) + 4*B + 132 floats, for lse*log2(e) and for D
+    assert lib.attn_bwd_workspace_size(4, 16, 4096, 0) == 2 * 16 * (16384 + 16 + 132) * 4
+    assert lib.attn_bwd_workspace_size(1, 3, 5, 1) == 3584   # 2*3*(8+4+132)*4 = 3456, rounded to 256
     assert lib.attn_bwd_workspace_size(1, 0, 5, 0) == 0
 
 
