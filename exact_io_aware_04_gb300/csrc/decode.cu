@@ -378,18 +378,24 @@ struct CombineParams {
     int B, Hq, nq, max_pages, pages_per_chunk, max_chunks;
 };
 
-// One warp per (sequence, query head, query): lse = log sum_i exp(lse_i), O = sum_i
-// exp(lse_i - lse) O_i over the chunks the sequence actually has.  Lane l
-// owns d-elements [l*d/32, (l+1)*d/32) as one vector load per chunk; the
-// weights of 32 chunks at a time are computed once and broadcast by shuffle,
-// so the partial-output loads of consecutive chunks are independent.
+// One block of kCombineWarps warps per (sequence, query head, query) row:
+// lse = log sum_i exp(lse_i), O = sum_i exp(lse_i - lse) O_i over the chunks
+// the sequence actually has.  Warp w takes chunks w, w + kCombineWarps, ...;
+// lane l of a warp owns d-elements [l*d/32, (l+1)*d/32) as one vector load per chunk.
+// The maximum and the normaliser are reduced across the block first, then
+// every warp accumulates its chunks and the warps' sums are added in shared
+// memory.  Several warps per row keep enough loads in flight to stream the
+// partials at memory speed; the chunks are dealt round-robin to the warps.
+constexpr int kCombineWarps = 4;
+
 template <int HD>
-__global__ void __launch_bounds__(256) attn_decode_combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(32 * kCombineWarps) attn_decode_combine_kernel(const CombineParams p) {
     constexpr int V = HD / 32;  // floats per lane
     using Vec = typename std::conditional<V == 4, float4, float2>::type;
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= p.B * p.Hq * p.nq) return;
+    __shared__ float red[kCombineWarps];
+    __shared__ float acc_s[kCombineWarps][HD];
+    const int row = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = row / (p.Hq * p.nq);
     const int hq = (row - b * p.Hq * p.nq) / p.nq;
     const int qi = row - (b * p.Hq + hq) * p.nq;
@@ -397,48 +403,66 @@ __global__ void __launch_bounds__(256) attn_decode_combine_kernel(const CombineP
     const int chunk_tokens = p.pages_per_chunk * kPage;
     const int n = (len + chunk_tokens - 1) / chunk_tokens;
     const float* lse_s = p.part_lse + static_cast<size_t>(row) * p.max_chunks;
+    // row maximum of the chunk lse
     float mx = -INFINITY;
-    for (int i = lane; i < n; i += 32) mx = fmaxf(mx, __ldg(lse_s + i));
+    for (int i = threadIdx.x; i < n; i += 32 * kCombineWarps) mx = fmaxf(mx, __ldg(lse_s + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, red[w]);
+    __nv_bfloat16* dst = p.out + ((static_cast<size_t>(b) * p.nq + qi) * p.Hq + hq) * HD;
+    if (mx == -INFINITY) {  // no keys: O = 0, lse = -inf
+        if (threadIdx.x == 0) p.lse[row] = -INFINITY;
+        for (int c = threadIdx.x; c < HD; c += 32 * kCombineWarps) dst[c] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    // normaliser
+    float total = 0.f;
+    for (int i = threadIdx.x; i < n; i += 32 * kCombineWarps) total += expf(__ldg(lse_s + i) - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    __syncthreads();  // every warp has read red[] above
+    if (lane == 0) red[warp] = total;
+    __syncthreads();
+    total = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineWarps; ++w) total += red[w];
+    const float lse_tot = mx + logf(total);
+    // this warp's chunks, weighted
     float acc[V];
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[c] = 0.f;
-    __nv_bfloat16* dst = p.out + ((static_cast<size_t>(b) * p.nq + qi) * p.Hq + hq) * HD + lane * V;
-    if (mx == -INFINITY) {  // no keys: O = 0, lse = -inf
-        if (lane == 0) p.lse[row] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < V; ++c) dst[c] = __float2bfloat16_rn(0.f);
-        return;
-    }
-    float total = 0.f;
-    for (int i = lane; i < n; i += 32) total += expf(__ldg(lse_s + i) - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
-    const float lse_tot = mx + logf(total);
     const float* po = p.part_o + static_cast<size_t>(row) * p.max_chunks * HD + lane * V;
-    for (int c0 = 0; c0 < n; c0 += 32) {
-        const int m = min(32, n - c0);
-        const float li = lane < m ? __ldg(lse_s + c0 + lane) : -INFINITY;
+    // rounds of 32 * kCombineWarps chunks: warp w takes chunks c0 + w + kCombineWarps * k,
+    // lane k holding that chunk's weight
+    for (int c0 = 0; c0 < n; c0 += 32 * kCombineWarps) {
+        const int mine = c0 + warp + kCombineWarps * lane;
+        const float li = mine < n ? __ldg(lse_s + mine) : -INFINITY;
         const float wl = li == -INFINITY ? 0.f : expf(li - lse_tot);
-#pragma unroll 4
+        const int m = min(32, (n - c0 - warp + kCombineWarps - 1) / kCombineWarps);  // this warp's chunks
+#pragma unroll 8
         for (int k = 0; k < m; ++k) {
             const float w = __shfl_sync(0xffffffffu, wl, k);
-            const Vec x = __ldg(reinterpret_cast<const Vec*>(po + static_cast<size_t>(c0 + k) * HD));
+            const int ch = c0 + warp + kCombineWarps * k;
+            const Vec x = __ldg(reinterpret_cast<const Vec*>(po + static_cast<size_t>(ch) * HD));
             const float* xs = reinterpret_cast<const float*>(&x);
 #pragma unroll
             for (int c = 0; c < V; ++c) acc[c] = fmaf(w, xs[c], acc[c]);
         }
     }
-    if (lane == 0) p.lse[row] = lse_tot;
-    if (V == 4) {
-        uint2 w2;
-        w2.x = pack_bf16x2(acc[0], acc[1]);
-        w2.y = pack_bf16x2(acc[2 % V], acc[3 % V]);
-        *reinterpret_cast<uint2*>(dst) = w2;
-    } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0], acc[1 % V]);
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc_s[warp][lane * V + c] = acc[c];
+    __syncthreads();
+    for (int c = threadIdx.x; c < HD; c += 32 * kCombineWarps) {
+        float s = acc_s[0][c];
+#pragma unroll
+        for (int w = 1; w < kCombineWarps; ++w) s += acc_s[w][c];
+        dst[c] = __float2bfloat16_rn(s);
     }
+    if (threadIdx.x == 0) p.lse[row] = lse_tot;
 }
 
 // In-place cache append: new row i of sequence b goes to position
@@ -571,7 +595,7 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     c.pages_per_chunk = plan.pages_per_chunk;
     c.max_chunks = plan.max_chunks;
     const int rows = a.B * a.Hq * a.nq;
-    attn_decode_combine_kernel<HD><<<(rows + 7) / 8, 256, 0, stream>>>(c);
+    attn_decode_combine_kernel<HD><<<rows, 32 * kCombineWarps, 0, stream>>>(c);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error_message("attn_decode_combine launch: %s", cudaGetErrorString(e));
