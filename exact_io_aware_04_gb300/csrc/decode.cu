@@ -630,10 +630,13 @@ bool make_decode_plan(int B, int nq, int Hq, int Hkv, int d, int page_size, int 
     if (num_splits > 0) {
         ppc = (max_pages + num_splits - 1) / num_splits;
     } else {
-        // about 2432 chunks if every sequence were at its longest (16 per SM of a
-        // 152-SM part); a power of two in [4, 256] pages
+        // about 1216 chunks if every sequence were at its longest (8 per SM of a
+        // 152-SM part), a power of two in [4, 256] pages.  Several queries per
+        // sequence multiply the partials each chunk writes, so they get fewer,
+        // longer chunks: 608 for Nq = 2, 304 from Nq = 4 on (measured best on the
+        // 64-sequence 4K-32K-token workloads).
         const long long pages = static_cast<long long>(B > 0 ? B : 1) * plan->head_groups * max_pages;
-        long long target = pages / 2432;
+        long long target = pages / (2432 / (2 * nq < 8 ? 2 * nq : 8));
         ppc = 4;
         while (ppc < 256 && 2LL * ppc <= target) ppc *= 2;
     }
