@@ -210,8 +210,19 @@ __device__ __forceinline__ void issue_tn(uint32_t tmem_d, uint32_t tmem_a, uint6
                       b_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc, (!first || kk > 0) ? 1u : 0u);
 }
 
-// Stores 64 bf16 values (a row segment) from fp32 registers, times `mul`.
+// Stores 64 bf16 values (a row segment) from fp32 registers, times `mul`:
+// 32-byte stores (whole sectors) when dst is 32-byte aligned, else 16-byte.
 __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, const float* x, float mul) {
+    if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(x[c + 2 * i] * mul, x[c + 2 * i + 1] * mul);
+            st_global_v8(dst + c, w);
+        }
+        return;
+    }
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int c = 0; c < 64; c += 8) {

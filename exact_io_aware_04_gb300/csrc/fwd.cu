@@ -613,6 +613,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
         // ---- epilogue: O / l -> bf16, lse
         const size_t out_row = static_cast<size_t>(it.s.q_base + q_local) * p.Hq + it.h;
         __nv_bfloat16* dst = p.out + out_row * HD;
+        const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;  // rows are 128 or 256 bytes
         if (nt > 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_o_final, ocnt & 1, p.err));
             ++ocnt;
@@ -624,7 +625,15 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                 float o[32];
                 tmem_ld_32cols_f(t_o + cc, o);
                 tmem_ld_wait_f(o);
-                if (row_valid) {
+                if (row_valid && out32) {  // whole 32-byte sectors
+#pragma unroll
+                    for (int c = 0; c < 32; c += 16) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(o[c + 2 * i] * inv_l, o[c + 2 * i + 1] * inv_l);
+                        st_global_v8(dst + cc + c, w);
+                    }
+                } else if (row_valid) {
                     uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
                     for (int c = 0; c < 32; c += 8) {
