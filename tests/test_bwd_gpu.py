@@ -160,3 +160,17 @@ def test_deterministic(la):
 def test_full_size_mha_sampled_heads(la):
     p = workloads.mha_causal()
     check(la, p, pairs=[(0, 0), (3, 15), (1, 7)])
+
+
+def test_varlen_many_sequences(la):
+    """The packed-mode tile lookup scans cu_seqlens 32 sequences at a time:
+    100 sequences take several rounds."""
+    g = torch.Generator().manual_seed(91)
+    ql = torch.randint(0, 300, (100,), generator=g).tolist()
+    kl = [q + int(x) for q, x in zip(ql, torch.randint(0, 200, (100,), generator=g).tolist())]
+    check(la, workloads.make_varlen(ql, kl, 2, 1, 64, causal=True, seed=92))
+
+
+def test_varlen_window(la):
+    check(la, workloads.make_varlen([200, 5, 300], [700, 5, 300], 4, 2, 128, causal=False, seed=93,
+                                    window=(90, 40)))

@@ -125,3 +125,20 @@ def test_full_size_sampled_rows(la, name):
     go, gl = gather_prefill(p, out, lse, rows.numpy())
     stats = assert_close(p.name, go, gl, ref_o, ref_lse)
     print(p.name, stats)
+
+
+def test_varlen_many_sequences_natural_order(la):
+    """More (sequence, pair) entries than the in-kernel sort takes (1024): the
+    items run in their natural order.  1200 sequences of 0..599 rows."""
+    g = torch.Generator().manual_seed(81)
+    ql = torch.randint(0, 600, (1200,), generator=g).tolist()
+    kl = [q + int(x) for q, x in zip(ql, torch.randint(0, 300, (1200,), generator=g).tolist())]
+    p = workloads.make_varlen(ql, kl, 2, 1, 64, causal=True, seed=82)
+    n_pairs = sum((q + 255) // 256 for q in ql)
+    assert n_pairs > 1024
+    out, lse = run_prefill(la, p)
+    torch.cuda.synchronize()
+    rows = workloads.sample_rows(None, ql, p.Hq, 4, seed=83)
+    ref_o, ref_lse = oracle.prefill(p, rows.numpy())
+    go, gl = gather_prefill(p, out, lse, rows.numpy())
+    assert_close(p.name, go, gl, ref_o, ref_lse)
