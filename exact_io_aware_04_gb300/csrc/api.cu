@@ -24,7 +24,6 @@ namespace {
 thread_local char t_message[512] = "";
 std::atomic<int> g_validation{0};
 
-constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 bool g_dev_ready[kMaxDevices] = {};
 DeviceInfo g_dev[kMaxDevices];

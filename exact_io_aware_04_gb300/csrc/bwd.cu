@@ -32,6 +32,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -914,8 +916,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
 
 // ============================================================================ host
 template <typename K>
-attn_status prepare_kernel(K kernel, int smem_bytes, bool& done) {
-    if (done) return ATTN_OK;
+attn_status prepare_kernel(K kernel, int smem_bytes, std::atomic<bool>* done) {
+    if (done != nullptr && done->load(std::memory_order_acquire)) return ATTN_OK;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) {
         set_error_message("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -932,7 +934,7 @@ attn_status prepare_kernel(K kernel, int smem_bytes, bool& done) {
                           fa.numRegs, kLaunchRegs);
         return ATTN_ERR_UNSUPPORTED;
     }
-    done = true;
+    if (done != nullptr) done->store(true, std::memory_order_release);
     return ATTN_OK;
 }
 
@@ -996,9 +998,12 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
             return ATTN_ERR_CUDA;
         }
     }
-    static bool ready_kv[2] = {false, false}, ready_q[2] = {false, false};
-    attn_status st = prepare_kernel(attn_bwd_dkdv_kernel<HD>, KvCfg<HD>::kSmemBytes, ready_kv[HD == 128]);
-    if (st == ATTN_OK) st = prepare_kernel(attn_bwd_dq_kernel<HD>, QCfg<HD>::kSmemBytes, ready_q[HD == 128]);
+    static std::atomic<bool> ready_kv[kMaxDevices], ready_q[kMaxDevices];  // per instantiation and device
+    const bool cached = dev.device >= 0 && dev.device < kMaxDevices;
+    attn_status st = prepare_kernel(attn_bwd_dkdv_kernel<HD>, KvCfg<HD>::kSmemBytes,
+                                    cached ? &ready_kv[dev.device] : nullptr);
+    if (st == ATTN_OK)
+        st = prepare_kernel(attn_bwd_dq_kernel<HD>, QCfg<HD>::kSmemBytes, cached ? &ready_q[dev.device] : nullptr);
     if (st != ATTN_OK) return st;
     // grids: dense = (tiles x B, heads); packed = an upper bound on the
     // (sequence, tile) entries, the surplus CTAs return at once

@@ -564,15 +564,16 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     const int stage_bytes = 2 * kPage * HG * HD * 2;
     const int n_stages = std::min(8, kStageBudget / stage_bytes);
     const int smem = n_stages * stage_bytes + 1024;
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[HD == 128]) {
+    static std::atomic<bool> attr_set[kMaxDevices];  // per instantiation and device
+    const bool cached = dev.device >= 0 && dev.device < kMaxDevices;
+    if (!cached || !attr_set[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(attn_decode_split_kernel<HD>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kStageBudget + 1024);
         if (e != cudaSuccess) {
             set_error_message("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
         }
-        attr_set[HD == 128] = true;
+        if (cached) attr_set[dev.device].store(true, std::memory_order_release);
     }
     const int threads = 32 * (1 + HG * p.m_tiles);
     dim3 grid(plan.max_chunks, a.B * plan.head_groups);

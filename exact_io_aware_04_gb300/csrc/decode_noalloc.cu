@@ -28,7 +28,6 @@ constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 

@@ -784,8 +784,9 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         check_cu_seqlens_kernel<<<1, 256, 0, stream>>>(a.cu_q, a.B, a.Nq, dev.err_word);
         check_cu_seqlens_kernel<<<1, 256, 0, stream>>>(a.cu_k, a.B, a.Nk, dev.err_word);
     }
-    static bool attr_set[2] = {false, false};  // per instantiation, all devices
-    if (!attr_set[HD == 128]) {
+    static std::atomic<bool> attr_set[kMaxDevices];  // per instantiation and device
+    const bool cached = dev.device >= 0 && dev.device < kMaxDevices;
+    if (!cached || !attr_set[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) {
@@ -804,7 +805,7 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
                               fa.numRegs, kLaunchRegs);
             return ATTN_ERR_UNSUPPORTED;
         }
-        attr_set[HD == 128] = true;
+        if (cached) attr_set[dev.device].store(true, std::memory_order_release);
     }
     attn_fwd_kernel<HD><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
     cudaError_t e = cudaGetLastError();

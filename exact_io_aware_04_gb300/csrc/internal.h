@@ -6,9 +6,15 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "status.h"
 
 namespace attn {
+
+// Launch attributes (dynamic shared memory) are per device: the launchers
+// remember having set them for devices below this index.
+constexpr int kMaxDevices = 64;
 
 // Per-device facts the launchers need; cached after the first query.
 struct DeviceInfo {
