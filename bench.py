@@ -384,7 +384,10 @@ def run_reference(args, world, rank):
     # the headline of the hot-path step is the prefill metric; the CPU arm
     # times that part (the decode pool would not fit a bounded CPU sample)
     name = "mha_causal" if args.workload == "hot_path" else args.workload
+    # each step is a bounded sample: about 4 s, but the whole --steps/--warmup run stays near
+    # 150 s of oracle work however many steps are asked for
     per_step = float(os.environ.get("ATTN_REFERENCE_STEP_SECONDS", "4.0"))
+    per_step = max(0.02, min(per_step, 150.0 / max(1, args.steps + args.warmup)))
     if name in BWD_WORKLOADS:
         prefill = getattr(workloads, BWD_WORKLOADS[name])()
         decode = None
@@ -416,7 +419,7 @@ def run_reference(args, world, rank):
         wname += "_backward"
         metric = BWD_METRIC
     sample = (f"each step: seeded rows of the {wname} workload, "
-              f"about {per_step:.0f} s of fp64 oracle work, rate = work/seconds")
+              f"about {per_step:.2f} s of fp64 oracle work, rate = work/seconds")
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
