@@ -62,10 +62,12 @@ struct Tile {
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 2-D [rows, heads*d] bf16, box 64 x 128, 128B swizzle
     const float* lse;                      // dense [B, Hq, Nq]; packed [Hq, T_q]
-    // workspace: lse * log2 e and D, each [Hq][ws_row] fp32; sequence b's
-    // rows start at ws_offset(b), so every 128-row tile starts 16-byte aligned
-    const float* lse2;
-    const float* dvec;
+    // workspace: -lse * log2 e and -D, each [Hq][ws_row] fp32 (negated so
+    // that the softmax threads use them in packed fma / add directly);
+    // sequence b's rows start at ws_offset(b), so every 128-row tile starts
+    // 16-byte aligned
+    const float* nlse2;
+    const float* ndvec;
     long long ws_row;
     __nv_bfloat16 *dq, *dk, *dv;
     const int *cu_q, *cu_k;
@@ -186,6 +188,48 @@ __device__ __forceinline__ void lds_64(uint32_t saddr, float* r) {
                      : "r"(saddr + 16u * i));
 }
 
+// P of 64 columns: p[c] = 2^(x[c] * sc + b[c]), with sc = scale * log2 e and
+// b = -lse * log2 e (per column in the K/V pass, one value per row in the dQ
+// pass); the argument in packed fp32x2 fma, one ex2 per element.
+__device__ __forceinline__ void exp2_scaled_64(const float* x, uint64_t sc2, float* b_then_p) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, f2_pack(b_then_p[c], b_then_p[c + 1])), a0, a1);
+        b_then_p[c] = fast_exp2(a0);
+        b_then_p[c + 1] = fast_exp2(a1);
+    }
+}
+__device__ __forceinline__ void exp2_scaled_64(const float* x, uint64_t sc2, uint64_t b2, float* p) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(x[c], x[c + 1]), sc2, b2), a0, a1);
+        p[c] = fast_exp2(a0);
+        p[c + 1] = fast_exp2(a1);
+    }
+}
+
+// dS of 64 columns as bf16 pairs: ds[c] = p[c] * (dp[c] - D), given nd = -D
+// (per column, or one value per row), in packed fp32x2 add and mul.
+__device__ __forceinline__ void ds_pack_64(const float* pr, const float* dp, const float* nd, uint32_t* pk) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+        float a0, a1;
+        f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), f2_pack(nd[c], nd[c + 1])), f2_pack(pr[c], pr[c + 1])),
+                  a0, a1);
+        pk[c >> 1] = pack_bf16x2(a0, a1);
+    }
+}
+__device__ __forceinline__ void ds_pack_64(const float* pr, const float* dp, uint64_t nd2, uint32_t* pk) {
+#pragma unroll
+    for (int c = 0; c < 64; c += 2) {
+        float a0, a1;
+        f2_unpack(f2_mul(f2_add(f2_pack(dp[c], dp[c + 1]), nd2), f2_pack(pr[c], pr[c + 1])), a0, a1);
+        pk[c >> 1] = pack_bf16x2(a0, a1);
+    }
+}
+
 // S-type product: D[128 x 128] = A[128 x d] B[128 x d]^T, both K-major tiles.
 template <int HD>
 __device__ __forceinline__ void issue_nt(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc) {
@@ -286,7 +330,7 @@ __device__ __forceinline__ void drain_half(uint32_t taddr_row, int half, __nv_bf
 // both into the padded workspace layout the K/V pass copies tile by tile.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const BwdParams p, const __nv_bfloat16* o,
-                                                           const __nv_bfloat16* g, float* lse2, float* dvec,
+                                                           const __nv_bfloat16* g, float* nlse2, float* ndvec,
                                                            long long rows) {
     constexpr int kTpr = HD / 8;              // threads per row
     constexpr int kRowsPerBlock = 256 / kTpr;
@@ -323,8 +367,8 @@ __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const BwdParams p, co
         const Seq s = seq_of(p, b);
         const int i = t - s.q_base;
         const long long w = static_cast<long long>(h) * p.ws_row + ws_offset(b, s.q_base) + i;
-        lse2[w] = __ldg(p.lse + lse_index(p, b, h, s, i)) * kLog2e;
-        dvec[w] = acc;
+        nlse2[w] = -__ldg(p.lse + lse_index(p, b, h, s, i)) * kLog2e;
+        ndvec[w] = -acc;
     }
 }
 
@@ -426,8 +470,8 @@ __device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, u
             // lse * log2 e and D of the tile's rows (rows past the sequence
             // hold other values: every use of them is masked by a select)
             const long long w = static_cast<long long>(h) * p.ws_row + ws_offset(it.b, it.s.q_base) + qt * kBM;
-            bulk_load(base + 2 * T::kBytes, p.lse2 + w, kBM * 4, full);
-            bulk_load(base + 2 * T::kBytes + kBM * 4, p.dvec + w, kBM * 4, full);
+            bulk_load(base + 2 * T::kBytes, p.nlse2 + w, kBM * 4, full);
+            bulk_load(base + 2 * T::kBytes + kBM * 4, p.ndvec + w, kBM * 4, full);
         }
     }
     // drain: every copy issued has landed before the CTA may exit
@@ -512,13 +556,13 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
     // the query rows that see this key (none for rows past the sequence)
     const int qmin = key_valid ? row_first(key, it.s.nq, it.s.nk, p.win_right) : 1;
     const int qmax = key_valid ? row_last(key, it.s.nq, it.s.nk, p.win_left) : 0;
-    const float sl2 = p.scale_log2;
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int s = 0; s < it.steps && ok; ++s) {
         const int st = s % C::kStages;
         const int qt = it.qt_lo + s % it.nqt;
         const int c0 = qt * kBM + half * 64;  // first query of this thread's columns
-        const uint32_t vec = stage0 + st * C::kStageBytes + 2 * T::kBytes;  // lse*log2e [128], then D [128]
+        const uint32_t vec = stage0 + st * C::kStageBytes + 2 * T::kBytes;  // -lse*log2e [128], then -D [128]
         // acquire the stage's vectors (written by the producer lanes before
         // they arrived on its full barrier; the stage is not refilled before
         // this step's dK product has read it), then S^T(s)
@@ -533,16 +577,11 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
         tmem_ld_wait_f(x + 32);
         const int lo = qmin - c0, hi = qmax - c0;  // allowed columns [lo, hi]
         float pr[64];
-        lds_64(vec + half * 64 * 4, pr);  // lse*log2e of this thread's 64 query columns
-        if (lo <= 0 && hi >= 63) {        // every column allowed (the common case)
+        lds_64(vec + half * 64 * 4, pr);  // -lse*log2e of this thread's 64 query columns
+        exp2_scaled_64(x, sc2, pr);       // pr = 2^(s * scale * log2 e - lse * log2 e)
+        if (!(lo <= 0 && hi >= 63)) {     // masked columns (the common case has none)
 #pragma unroll
-            for (int c = 0; c < 64; ++c) pr[c] = fast_exp2(fmaf(x[c], sl2, -pr[c]));
-        } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float e = fast_exp2(fmaf(x[c], sl2, -pr[c]));
-                pr[c] = (c < lo || c > hi) ? 0.f : e;
-            }
+            for (int c = 0; c < 64; ++c) pr[c] = (c < lo || c > hi) ? 0.f : pr[c];
         }
         {
             uint32_t pk[32];
@@ -563,16 +602,14 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
         tmem_ld_wait_f(x);
         tmem_ld_wait_f(x + 32);
         {
-            float dd[64];
-            lds_64(vec + (kBM + half * 64) * 4, dd);  // D of this thread's 64 query columns
-            if (!(lo <= 0 && hi >= 63)) {  // masked columns: D may be any bits there
+            float nd[64];
+            lds_64(vec + (kBM + half * 64) * 4, nd);  // -D of this thread's 64 query columns
+            if (!(lo <= 0 && hi >= 63)) {  // masked columns: -D may be any bits there, dP - D := 0
 #pragma unroll
-                for (int c = 0; c < 64; ++c) dd[c] = (c < lo || c > hi) ? x[c] : dd[c];
+                for (int c = 0; c < 64; ++c) nd[c] = (c < lo || c > hi) ? -x[c] : nd[c];
             }
             uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 64; c += 2)
-                pk[c >> 1] = pack_bf16x2(pr[c] * (x[c] - dd[c]), pr[c + 1] * (x[c + 1] - dd[c + 1]));
+            ds_pack_64(pr, x, nd, pk);
             tmem_st_32cols(t_dp + half * 64, pk);  // over this warpgroup's own dP^T columns
             tmem_st_wait();
         }
@@ -651,17 +688,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
 }
 
 // ============================================================================ dQ
+// K_j and V_j stream through rings of their own.  V_j is read by one product
+// (dP), K_j by two (S, then dQ a step later), so K gets the deeper ring: the
+// load of K_{u+1} is issued about one and a half steps before S(u+1) needs it.
 template <int HD>
 struct QCfg {
-    static constexpr int kStages = HD == 128 ? 2 : 4;
-    static constexpr int kStageBytes = 2 * Tile<HD>::kBytes;  // K_j, V_j
-    static constexpr int kNeed = 2 * Tile<HD>::kBytes + kStages * kStageBytes + 1024;
+    static constexpr int kKStages = HD == 128 ? 3 : 4;
+    static constexpr int kVStages = HD == 128 ? 2 : 4;
+    static constexpr int kMaxStages = 4;
+    // [Q_i][G_i][K ring][V ring]
+    static constexpr int kNeed = (2 + kKStages + kVStages) * Tile<HD>::kBytes + 1024;
     static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;  // one CTA per SM
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+    static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages, "ring barriers");
+    static_assert(kNeed <= 227 * 1024 - 256, "shared memory of the dQ pass");
 };
 
-enum : int { Q_FULL = 0, Q_STAGE_FULL = 1, Q_STAGE_EMPTY = 5, Q_S_FULL = 9, Q_DP_FULL, Q_S_FREE, Q_DS_READY,
-             Q_ACC_FULL, Q_COUNT };
+enum : int { Q_FULL = 0, Q_K_FULL = 1, Q_K_EMPTY = 5, Q_V_FULL = 9, Q_V_EMPTY = 13, Q_S_FULL = 17, Q_DP_FULL,
+             Q_S_FREE, Q_DS_READY, Q_ACC_FULL, Q_COUNT };
 
 struct QItem {
     int b, h, i;
@@ -702,7 +746,8 @@ template <int HD>
 __device__ __noinline__ void q_producer(const BwdParams& p, const QItem& it, uint32_t smem0, uint32_t bar0) {
     using T = Tile<HD>;
     using C = QCfg<HD>;
-    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    const uint32_t kring = smem0 + 2 * T::kBytes;
+    const uint32_t vring = kring + C::kKStages * T::kBytes;
     const int g = it.h / p.group;
     bool ok = true;
     mbar_arrive_expect_tx(bar_at(bar0, Q_FULL), 2 * T::kBytes);
@@ -714,22 +759,30 @@ __device__ __noinline__ void q_producer(const BwdParams& p, const QItem& it, uin
                     it.s.q_base + it.q0);
     }
     for (int u = 0; u < it.n && ok; ++u) {
-        const int st = u % C::kStages;
-        if (u >= C::kStages) ok = mbar_wait(bar_at(bar0, Q_STAGE_EMPTY + st), ((u / C::kStages) - 1) & 1, p.err);
-        if (!ok) break;
-        const uint32_t base = stage0 + st * C::kStageBytes;
-        const uint32_t full = bar_at(bar0, Q_STAGE_FULL + st);
-        mbar_arrive_expect_tx(full, 2 * T::kBytes);
         const int y = it.s.k_base + (it.lo + u) * kBM;
+        const int ks = u % C::kKStages, vs = u % C::kVStages;
+        if (u >= C::kKStages) ok = mbar_wait(bar_at(bar0, Q_K_EMPTY + ks), ((u / C::kKStages) - 1) & 1, p.err);
+        if (!ok) break;
+        const uint32_t kfull = bar_at(bar0, Q_K_FULL + ks);
+        mbar_arrive_expect_tx(kfull, T::kBytes);
 #pragma unroll
-        for (int pn = 0; pn < T::kPanels; ++pn) {
-            tma_load_2d(base + pn * T::kPanelBytes, &p.tm_k, full, g * HD + pn * 64, y);
-            tma_load_2d(base + T::kBytes + pn * T::kPanelBytes, &p.tm_v, full, g * HD + pn * 64, y);
-        }
+        for (int pn = 0; pn < T::kPanels; ++pn)
+            tma_load_2d(kring + ks * T::kBytes + pn * T::kPanelBytes, &p.tm_k, kfull, g * HD + pn * 64, y);
+        if (u >= C::kVStages) ok = mbar_wait(bar_at(bar0, Q_V_EMPTY + vs), ((u / C::kVStages) - 1) & 1, p.err);
+        if (!ok) break;
+        const uint32_t vfull = bar_at(bar0, Q_V_FULL + vs);
+        mbar_arrive_expect_tx(vfull, T::kBytes);
+#pragma unroll
+        for (int pn = 0; pn < T::kPanels; ++pn)
+            tma_load_2d(vring + vs * T::kBytes + pn * T::kPanelBytes, &p.tm_v, vfull, g * HD + pn * 64, y);
     }
+    // drain: every copy issued has landed before the CTA may exit (a load
+    // left unissued after an error has no transaction to wait for)
     mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
-    for (int u = (it.n > C::kStages ? it.n - C::kStages : 0); u < it.n; ++u)
-        mbar_wait(bar_at(bar0, Q_STAGE_FULL + u % C::kStages), (u / C::kStages) & 1, p.err);
+    for (int u = (it.n > C::kKStages ? it.n - C::kKStages : 0); u < it.n; ++u)
+        mbar_wait(bar_at(bar0, Q_K_FULL + u % C::kKStages), (u / C::kKStages) & 1, p.err);
+    for (int u = (it.n > C::kVStages ? it.n - C::kVStages : 0); u < it.n; ++u)
+        mbar_wait(bar_at(bar0, Q_V_FULL + u % C::kVStages), (u / C::kVStages) & 1, p.err);
 }
 
 template <int HD>
@@ -737,46 +790,56 @@ __device__ __noinline__ void q_mma(const BwdParams& p, const QItem& it, uint32_t
                                    uint32_t tmem) {
     using T = Tile<HD>;
     using C = QCfg<HD>;
-    const uint32_t stage0 = smem0 + 2 * T::kBytes;
+    const uint32_t kring = smem0 + 2 * T::kBytes;
+    const uint32_t vring = kring + C::kKStages * T::kBytes;
     const uint64_t d_q = smem_desc_sw128(smem0, 16, 1024);               // Q_i, K-major
     const uint64_t d_g = smem_desc_sw128(smem0 + T::kBytes, 16, 1024);   // G_i, K-major
-    constexpr uint64_t kStageDesc = C::kStageBytes >> 4;
-    const uint64_t d_k0 = smem_desc_sw128(stage0, 16, 1024);                       // K_j as the B of S
-    const uint64_t d_v0 = smem_desc_sw128(stage0 + T::kBytes, 16, 1024);           // V_j as the B of dP
-    const uint64_t d_kmn0 = smem_desc_sw128(stage0, T::kPanelBytes, 1024);         // K_j row-major B
+    constexpr uint64_t kSlotDesc = T::kBytes >> 4;                        // descriptor step between ring slots
+    const uint64_t d_k0 = smem_desc_sw128(kring, 16, 1024);               // K_j as the B of S
+    const uint64_t d_kmn0 = smem_desc_sw128(kring, T::kPanelBytes, 1024); // K_j row-major B
+    const uint64_t d_v0 = smem_desc_sw128(vring, 16, 1024);               // V_j as the B of dP
     const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP, t_dq = tmem + C::kColDQ;
     const int n = it.n;
     bool ok = mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
     if (ok && n > 0) {
-        ok = mbar_wait(bar_at(bar0, Q_STAGE_FULL + 0), 0, p.err);
+        ok = mbar_wait(bar_at(bar0, Q_K_FULL + 0), 0, p.err);
         if (ok) {
             tc_fence_after_sync();
             issue_nt<HD>(t_s, d_q, d_k0);
             tc_commit(bar_at(bar0, Q_S_FULL));
+            ok = mbar_wait(bar_at(bar0, Q_V_FULL + 0), 0, p.err);
+        }
+        if (ok) {
+            tc_fence_after_sync();
             issue_nt<HD>(t_dp, d_g, d_v0);
             tc_commit(bar_at(bar0, Q_DP_FULL));
+            tc_commit(bar_at(bar0, Q_V_EMPTY + 0));  // V_j has no other reader
         }
     }
     for (int u = 0; u < n && ok; ++u) {
-        const int st = u % C::kStages;
+        const int ks = u % C::kKStages;
         const bool more = u + 1 < n;
-        const int st1 = (u + 1) % C::kStages;
+        const int ks1 = (u + 1) % C::kKStages, vs1 = (u + 1) % C::kVStages;
         if (more) {
             ok = mbar_wait(bar_at(bar0, Q_S_FREE), u & 1, p.err) &&
-                 mbar_wait(bar_at(bar0, Q_STAGE_FULL + st1), ((u + 1) / C::kStages) & 1, p.err);
+                 mbar_wait(bar_at(bar0, Q_K_FULL + ks1), ((u + 1) / C::kKStages) & 1, p.err);
             if (!ok) break;
             tc_fence_after_sync();
-            issue_nt<HD>(t_s, d_q, d_k0 + st1 * kStageDesc);  // S(u+1)
+            issue_nt<HD>(t_s, d_q, d_k0 + ks1 * kSlotDesc);  // S(u+1)
             tc_commit(bar_at(bar0, Q_S_FULL));
         }
         ok = mbar_wait(bar_at(bar0, Q_DS_READY), u & 1, p.err);
         if (!ok) break;
         tc_fence_after_sync();
-        issue_tn<HD>(t_dq, t_dp, d_kmn0 + st * kStageDesc, u == 0);  // dQ += dS K_j
-        tc_commit(bar_at(bar0, Q_STAGE_EMPTY + st));
+        issue_tn<HD>(t_dq, t_dp, d_kmn0 + ks * kSlotDesc, u == 0);  // dQ += dS K_j
+        tc_commit(bar_at(bar0, Q_K_EMPTY + ks));
         if (more) {
-            issue_nt<HD>(t_dp, d_g, d_v0 + st1 * kStageDesc);  // dP(u+1)
+            ok = mbar_wait(bar_at(bar0, Q_V_FULL + vs1), ((u + 1) / C::kVStages) & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_nt<HD>(t_dp, d_g, d_v0 + vs1 * kSlotDesc);  // dP(u+1)
             tc_commit(bar_at(bar0, Q_DP_FULL));
+            tc_commit(bar_at(bar0, Q_V_EMPTY + vs1));
         }
     }
     tc_commit(bar_at(bar0, Q_ACC_FULL));
@@ -796,13 +859,13 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
     const int nq = it.s.nq, nk = it.s.nk;
     const int kmin = row_valid ? key_first(i, nq, nk, p.win_left) : 1;
     const int kmax = row_valid ? key_last(i, nq, nk, p.win_right) : 0;
-    float l2 = 0.f, dd = 0.f;
+    float nl2 = 0.f, nd = 0.f;  // -lse * log2 e and -D of this row
     if (row_valid) {
         const long long w = static_cast<long long>(it.h) * p.ws_row + ws_offset(it.b, it.s.q_base) + i;
-        l2 = __ldg(p.lse2 + w);
-        dd = __ldg(p.dvec + w);
+        nl2 = __ldg(p.nlse2 + w);
+        nd = __ldg(p.ndvec + w);
     }
-    const float sl2 = p.scale_log2;
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int u = 0; u < it.n && ok; ++u) {
         const int k0 = (it.lo + u) * kBM + half * 64;
@@ -819,15 +882,10 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
         if (lane == 0) mbar_arrive(bar_at(bar0, Q_S_FREE));  // S may be overwritten
         const int lo = kmin - k0, hi = kmax - k0;
         float pr[64];
-        if (lo <= 0 && hi >= 63) {  // every column allowed (the common case)
+        exp2_scaled_64(x, sc2, f2_pack(nl2, nl2), pr);  // pr = 2^(s * scale * log2 e - lse * log2 e)
+        if (!(lo <= 0 && hi >= 63)) {                    // masked columns (the common case has none)
 #pragma unroll
-            for (int c = 0; c < 64; ++c) pr[c] = fast_exp2(fmaf(x[c], sl2, -l2));
-        } else {
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float e = fast_exp2(fmaf(x[c], sl2, -l2));
-                pr[c] = (c < lo || c > hi) ? 0.f : e;
-            }
+            for (int c = 0; c < 64; ++c) pr[c] = (c < lo || c > hi) ? 0.f : pr[c];
         }
         ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_DP_FULL), u & 1, p.err));
         if (!ok) break;
@@ -838,8 +896,7 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
         tmem_ld_wait_f(x + 32);
         {
             uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) pk[c >> 1] = pack_bf16x2(pr[c] * (x[c] - dd), pr[c + 1] * (x[c + 1] - dd));
+            ds_pack_64(pr, x, f2_pack(nd, nd), pk);
             tmem_st_32cols(t_dp + half * 64, pk);  // over this warpgroup's own dP columns
             tmem_st_wait();
         }
@@ -874,9 +931,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     const uint32_t bar0 = smem_addr(bars);
     if (threadIdx.x == 0) {
         mbar_init(bar_at(bar0, Q_FULL), 1);
-        for (int s = 0; s < QCfg<HD>::kStages; ++s) {
-            mbar_init(bar_at(bar0, Q_STAGE_FULL + s), 1);
-            mbar_init(bar_at(bar0, Q_STAGE_EMPTY + s), 1);
+        for (int s = 0; s < QCfg<HD>::kMaxStages; ++s) {
+            mbar_init(bar_at(bar0, Q_K_FULL + s), 1);
+            mbar_init(bar_at(bar0, Q_K_EMPTY + s), 1);
+            mbar_init(bar_at(bar0, Q_V_FULL + s), 1);
+            mbar_init(bar_at(bar0, Q_V_EMPTY + s), 1);
         }
         mbar_init(bar_at(bar0, Q_S_FULL), 1);
         mbar_init(bar_at(bar0, Q_DP_FULL), 1);
@@ -964,8 +1023,8 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     }
     p.lse = a.lse;
     p.ws_row = bwd_ws_row(a.B, varlen ? a.Nq : static_cast<long long>(a.B) * a.Nq);
-    p.lse2 = static_cast<float*>(a.workspace);
-    p.dvec = static_cast<float*>(a.workspace) + p.ws_row * a.Hq;
+    p.nlse2 = static_cast<float*>(a.workspace);
+    p.ndvec = static_cast<float*>(a.workspace) + p.ws_row * a.Hq;
     p.dq = static_cast<__nv_bfloat16*>(a.dq);
     p.dk = static_cast<__nv_bfloat16*>(a.dk);
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
@@ -990,8 +1049,8 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         constexpr int kRowsPerBlock = 256 / (HD / 8);
         attn_bwd_dot_kernel<HD><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0,
                                   stream>>>(p, static_cast<const __nv_bfloat16*>(a.out),
-                                            static_cast<const __nv_bfloat16*>(a.dout), const_cast<float*>(p.lse2),
-                                            const_cast<float*>(p.dvec), rows);
+                                            static_cast<const __nv_bfloat16*>(a.dout), const_cast<float*>(p.nlse2),
+                                            const_cast<float*>(p.ndvec), rows);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error_message("attn_bwd_dot launch: %s", cudaGetErrorString(e));
