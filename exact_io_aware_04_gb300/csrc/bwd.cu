@@ -699,13 +699,19 @@ struct QCfg {
     // [Q_i][G_i][K ring][V ring]
     static constexpr int kNeed = (2 + kKStages + kVStages) * Tile<HD>::kBytes + 1024;
     static constexpr int kSmemBytes = kNeed > 120 * 1024 ? kNeed : 120 * 1024;  // one CTA per SM
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+    // tensor memory: S, dQ, and dP in two buffers (dP(u+1) is computed while
+    // dQ(u) still waits for dS(u), which the softmax writes over dP(u))
+    static constexpr uint32_t kColS = 0, kColDQ = 256;
+    __device__ static constexpr uint32_t col_dp(int u) { return (u & 1) ? 384u : 128u; }
     static_assert(kKStages <= kMaxStages && kVStages <= kMaxStages, "ring barriers");
     static_assert(kNeed <= 227 * 1024 - 256, "shared memory of the dQ pass");
 };
 
-enum : int { Q_FULL = 0, Q_K_FULL = 1, Q_K_EMPTY = 5, Q_V_FULL = 9, Q_V_EMPTY = 13, Q_S_FULL = 17, Q_DP_FULL,
-             Q_S_FREE, Q_DS_READY, Q_ACC_FULL, Q_COUNT };
+// DP_FULL, DS_READY and DQ_DONE come in pairs, one per dP buffer: a barrier
+// of one buffer completes its next phase only after every waiter has passed
+// the current one (no phase can be skipped).
+enum : int { Q_FULL = 0, Q_K_FULL = 1, Q_K_EMPTY = 5, Q_V_FULL = 9, Q_V_EMPTY = 13, Q_S_FULL = 17, Q_DP_FULL = 18,
+             Q_S_FREE = 20, Q_DS_READY = 21, Q_DQ_DONE = 23, Q_ACC_FULL = 25, Q_S_DP_DONE = 26, Q_COUNT };
 
 struct QItem {
     int b, h, i;
@@ -785,64 +791,65 @@ __device__ __noinline__ void q_producer(const BwdParams& p, const QItem& it, uin
         mbar_wait(bar_at(bar0, Q_V_FULL + u % C::kVStages), (u / C::kVStages) & 1, p.err);
 }
 
+// Two issuing threads.  Thread 0 computes the products that do not need
+// dS: S(u+1) and dP(u+1); thread 1 computes dQ(u) = dS(u) K_u once the
+// softmax has written dS(u).  Each thread's barrier waits then overlap the
+// other thread's products (a thread's issue is close to synchronous with the
+// tensor pipe).  Cross-thread reuse of tensor memory waits for completion:
+// dP(u+1) overwrites the buffer that held dS(u-1) only after dQ(u-1) has
+// completed (DQ_DONE).
 template <int HD>
 __device__ __noinline__ void q_mma(const BwdParams& p, const QItem& it, uint32_t smem0, uint32_t bar0,
-                                   uint32_t tmem) {
+                                   uint32_t tmem, int role) {
     using T = Tile<HD>;
     using C = QCfg<HD>;
     const uint32_t kring = smem0 + 2 * T::kBytes;
     const uint32_t vring = kring + C::kKStages * T::kBytes;
-    const uint64_t d_q = smem_desc_sw128(smem0, 16, 1024);               // Q_i, K-major
-    const uint64_t d_g = smem_desc_sw128(smem0 + T::kBytes, 16, 1024);   // G_i, K-major
-    constexpr uint64_t kSlotDesc = T::kBytes >> 4;                        // descriptor step between ring slots
-    const uint64_t d_k0 = smem_desc_sw128(kring, 16, 1024);               // K_j as the B of S
-    const uint64_t d_kmn0 = smem_desc_sw128(kring, T::kPanelBytes, 1024); // K_j row-major B
-    const uint64_t d_v0 = smem_desc_sw128(vring, 16, 1024);               // V_j as the B of dP
-    const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP, t_dq = tmem + C::kColDQ;
+    constexpr uint64_t kSlotDesc = T::kBytes >> 4;  // descriptor step between ring slots
     const int n = it.n;
-    bool ok = mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
-    if (ok && n > 0) {
-        ok = mbar_wait(bar_at(bar0, Q_K_FULL + 0), 0, p.err);
-        if (ok) {
-            tc_fence_after_sync();
-            issue_nt<HD>(t_s, d_q, d_k0);
-            tc_commit(bar_at(bar0, Q_S_FULL));
-            ok = mbar_wait(bar_at(bar0, Q_V_FULL + 0), 0, p.err);
-        }
-        if (ok) {
-            tc_fence_after_sync();
-            issue_nt<HD>(t_dp, d_g, d_v0);
-            tc_commit(bar_at(bar0, Q_DP_FULL));
-            tc_commit(bar_at(bar0, Q_V_EMPTY + 0));  // V_j has no other reader
-        }
-    }
-    for (int u = 0; u < n && ok; ++u) {
-        const int ks = u % C::kKStages;
-        const bool more = u + 1 < n;
-        const int ks1 = (u + 1) % C::kKStages, vs1 = (u + 1) % C::kVStages;
-        if (more) {
-            ok = mbar_wait(bar_at(bar0, Q_S_FREE), u & 1, p.err) &&
-                 mbar_wait(bar_at(bar0, Q_K_FULL + ks1), ((u + 1) / C::kKStages) & 1, p.err);
+    bool ok = true;
+    if (role == 0) {
+        const uint64_t d_q = smem_desc_sw128(smem0, 16, 1024);              // Q_i, K-major
+        const uint64_t d_g = smem_desc_sw128(smem0 + T::kBytes, 16, 1024);  // G_i, K-major
+        const uint64_t d_k0 = smem_desc_sw128(kring, 16, 1024);             // K_j as the B of S
+        const uint64_t d_v0 = smem_desc_sw128(vring, 16, 1024);             // V_j as the B of dP
+        const uint32_t t_s = tmem + C::kColS;
+        ok = mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
+        for (int u = 0; u < n && ok; ++u) {  // S(u) and dP(u)
+            const int ks = u % C::kKStages, vs = u % C::kVStages;
+            ok = (u == 0 || mbar_wait(bar_at(bar0, Q_S_FREE), (u - 1) & 1, p.err)) &&
+                 mbar_wait(bar_at(bar0, Q_K_FULL + ks), (u / C::kKStages) & 1, p.err);
             if (!ok) break;
             tc_fence_after_sync();
-            issue_nt<HD>(t_s, d_q, d_k0 + ks1 * kSlotDesc);  // S(u+1)
+            issue_nt<HD>(t_s, d_q, d_k0 + ks * kSlotDesc);  // S(u)
             tc_commit(bar_at(bar0, Q_S_FULL));
-        }
-        ok = mbar_wait(bar_at(bar0, Q_DS_READY), u & 1, p.err);
-        if (!ok) break;
-        tc_fence_after_sync();
-        issue_tn<HD>(t_dq, t_dp, d_kmn0 + ks * kSlotDesc, u == 0);  // dQ += dS K_j
-        tc_commit(bar_at(bar0, Q_K_EMPTY + ks));
-        if (more) {
-            ok = mbar_wait(bar_at(bar0, Q_V_FULL + vs1), ((u + 1) / C::kVStages) & 1, p.err);
+            // the dP buffer of step u last held dS(u-2)
+            ok = (u < 2 || mbar_wait(bar_at(bar0, Q_DQ_DONE + (u & 1)), ((u - 2) >> 1) & 1, p.err)) &&
+                 mbar_wait(bar_at(bar0, Q_V_FULL + vs), (u / C::kVStages) & 1, p.err);
             if (!ok) break;
             tc_fence_after_sync();
-            issue_nt<HD>(t_dp, d_g, d_v0 + vs1 * kSlotDesc);  // dP(u+1)
-            tc_commit(bar_at(bar0, Q_DP_FULL));
-            tc_commit(bar_at(bar0, Q_V_EMPTY + vs1));
+            issue_nt<HD>(tmem + C::col_dp(u), d_g, d_v0 + vs * kSlotDesc);  // dP(u)
+            tc_commit(bar_at(bar0, Q_DP_FULL + (u & 1)));
+            tc_commit(bar_at(bar0, Q_V_EMPTY + vs));  // V_j has no other reader
         }
+        // drain: this thread's products (and their barrier arrivals) are done before it leaves
+        tc_commit(bar_at(bar0, Q_S_DP_DONE));
+        mbar_wait(bar_at(bar0, Q_S_DP_DONE), 0, p.err);
+    } else {
+        const uint64_t d_kmn0 = smem_desc_sw128(kring, T::kPanelBytes, 1024);  // K_j row-major B
+        const uint32_t t_dq = tmem + C::kColDQ;
+        for (int u = 0; u < n && ok; ++u) {  // dQ(u)
+            const int ks = u % C::kKStages;
+            ok = mbar_wait(bar_at(bar0, Q_DS_READY + (u & 1)), (u >> 1) & 1, p.err) &&
+                 mbar_wait(bar_at(bar0, Q_K_FULL + ks), (u / C::kKStages) & 1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_tn<HD>(t_dq, tmem + C::col_dp(u), d_kmn0 + ks * kSlotDesc, u == 0);  // dQ += dS K_j
+            tc_commit(bar_at(bar0, Q_K_EMPTY + ks));
+            tc_commit(bar_at(bar0, Q_DQ_DONE + (u & 1)));
+        }
+        tc_commit(bar_at(bar0, Q_ACC_FULL));
     }
-    tc_commit(bar_at(bar0, Q_ACC_FULL));
 }
 
 template <int HD>
@@ -853,7 +860,7 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
     const int half = warp >> 2;                // key columns [64 half, 64 half + 64)
     const int r = (warp & 3) * 32 + lane;      // query row == tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const uint32_t t_s = tmem + lane_off + C::kColS;
     const int i = it.q0 + r;
     const bool row_valid = r < it.rows;
     const int nq = it.s.nq, nk = it.s.nk;
@@ -887,9 +894,10 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
 #pragma unroll
             for (int c = 0; c < 64; ++c) pr[c] = (c < lo || c > hi) ? 0.f : pr[c];
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_DP_FULL), u & 1, p.err));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_DP_FULL + (u & 1)), (u >> 1) & 1, p.err));
         if (!ok) break;
         tc_fence_after_sync();
+        const uint32_t t_dp = tmem + lane_off + C::col_dp(u);
         tmem_ld_32cols_f(t_dp + half * 64, x);
         tmem_ld_32cols_f(t_dp + half * 64 + 32, x + 32);
         tmem_ld_wait_f(x);
@@ -902,7 +910,7 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(bar0, Q_DS_READY));
+        if (lane == 0) mbar_arrive(bar_at(bar0, Q_DS_READY + (u & 1)));
     }
     __nv_bfloat16* dq_row = p.dq + (static_cast<size_t>(it.s.q_base + i) * p.Hq + it.h) * HD;
     if (it.n == 0) {  // no key: zero gradient
@@ -938,10 +946,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
             mbar_init(bar_at(bar0, Q_V_EMPTY + s), 1);
         }
         mbar_init(bar_at(bar0, Q_S_FULL), 1);
-        mbar_init(bar_at(bar0, Q_DP_FULL), 1);
+        mbar_init(bar_at(bar0, Q_DP_FULL + 0), 1);
+        mbar_init(bar_at(bar0, Q_DP_FULL + 1), 1);
         mbar_init(bar_at(bar0, Q_S_FREE), kSoftmaxWarps);
-        mbar_init(bar_at(bar0, Q_DS_READY), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, Q_DS_READY + 0), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, Q_DS_READY + 1), kSoftmaxWarps);
+        mbar_init(bar_at(bar0, Q_DQ_DONE + 0), 1);
+        mbar_init(bar_at(bar0, Q_DQ_DONE + 1), 1);
         mbar_init(bar_at(bar0, Q_ACC_FULL), 1);
+        mbar_init(bar_at(bar0, Q_S_DP_DONE), 1);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -961,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
     if (warp >= 8) {
         regs_decrease<kControlRegs>();
         if (warp == kProducerWarp && lane == 0) q_producer<HD>(p, it, smem0, bar0);
-        if (warp == kMmaWarp && lane == 0) q_mma<HD>(p, it, smem0, bar0, tmem);
+        if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0) q_mma<HD>(p, it, smem0, bar0, tmem, warp - kMmaWarp);
         __syncwarp();
     } else {
         regs_increase<kSoftmaxRegs>();
