@@ -385,9 +385,11 @@ struct KvCfg {
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + HD;
 };
 
-// barriers of the K/V pass
-enum : int { KV_FULL = 0, KV_STAGE_FULL = 1, KV_STAGE_EMPTY = 3, KV_S_FULL = 5, KV_DP_FULL, KV_P_READY, KV_DS_READY,
-             KV_ACC_FULL, KV_COUNT };
+// barriers of the K/V pass.  A stage's Q_i (with the two vectors) and G_i
+// have barriers of their own: S^T(s+1) needs only Q_{s+1}, and G_i is
+// released as soon as dV has read it.
+enum : int { KV_FULL = 0, KV_Q_FULL = 1, KV_Q_EMPTY = 3, KV_G_FULL = 5, KV_G_EMPTY = 7, KV_S_FULL = 9, KV_DP_FULL,
+             KV_P_READY, KV_DS_READY, KV_ACC_FULL, KV_COUNT };
 
 struct KvItem {
     int b, g, j;
@@ -450,35 +452,43 @@ __device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, u
         const int h = it.g * p.group + s / it.nqt;
         const int qt = it.qt_lo + s % it.nqt;
         const uint32_t base = stage0 + st * C::kStageBytes;
+        const uint32_t par = ((s / C::kStages) - 1) & 1;
+        // Q_i with -lse*log2e and -D of the tile's rows (rows past the
+        // sequence hold other values: every use of them is masked by a select)
         if (s >= C::kStages)
-            ok = __shfl_sync(0xffffffffu,
-                             lane == 0 ? mbar_wait(bar_at(bar0, KV_STAGE_EMPTY + st), ((s / C::kStages) - 1) & 1,
-                                                   p.err)
-                                       : true,
-                             0);
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_at(bar0, KV_Q_EMPTY + st), par, p.err) : true, 0);
         if (!ok) break;
-        const uint32_t full = bar_at(bar0, KV_STAGE_FULL + st);
         if (lane == 0) {
-            mbar_arrive_expect_tx(full, 2 * T::kBytes + 2 * kBM * 4);
+            const uint32_t full = bar_at(bar0, KV_Q_FULL + st);
+            mbar_arrive_expect_tx(full, T::kBytes + 2 * kBM * 4);
 #pragma unroll
-            for (int pn = 0; pn < T::kPanels; ++pn) {
-                tma_load_2d(base + pn * T::kPanelBytes, &p.tm_q, full, h * HD + pn * 64,
-                            it.s.q_base + qt * kBM);
-                tma_load_2d(base + T::kBytes + pn * T::kPanelBytes, &p.tm_do, full, h * HD + pn * 64,
-                            it.s.q_base + qt * kBM);
-            }
-            // lse * log2 e and D of the tile's rows (rows past the sequence
-            // hold other values: every use of them is masked by a select)
+            for (int pn = 0; pn < T::kPanels; ++pn)
+                tma_load_2d(base + pn * T::kPanelBytes, &p.tm_q, full, h * HD + pn * 64, it.s.q_base + qt * kBM);
             const long long w = static_cast<long long>(h) * p.ws_row + ws_offset(it.b, it.s.q_base) + qt * kBM;
             bulk_load(base + 2 * T::kBytes, p.nlse2 + w, kBM * 4, full);
             bulk_load(base + 2 * T::kBytes + kBM * 4, p.ndvec + w, kBM * 4, full);
         }
+        // G_i
+        if (s >= C::kStages)
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar_at(bar0, KV_G_EMPTY + st), par, p.err) : true, 0);
+        if (!ok) break;
+        if (lane == 0) {
+            const uint32_t full = bar_at(bar0, KV_G_FULL + st);
+            mbar_arrive_expect_tx(full, T::kBytes);
+#pragma unroll
+            for (int pn = 0; pn < T::kPanels; ++pn)
+                tma_load_2d(base + T::kBytes + pn * T::kPanelBytes, &p.tm_do, full, h * HD + pn * 64,
+                            it.s.q_base + qt * kBM);
+        }
     }
-    // drain: every copy issued has landed before the CTA may exit
+    // drain: every copy issued has landed before the CTA may exit (a copy
+    // left unissued after an error has no transaction to wait for)
     if (lane == 0) {
         mbar_wait(bar_at(bar0, KV_FULL), 0, p.err);
-        for (int s = (it.steps > C::kStages ? it.steps - C::kStages : 0); s < it.steps; ++s)
-            mbar_wait(bar_at(bar0, KV_STAGE_FULL + s % C::kStages), (s / C::kStages) & 1, p.err);
+        for (int s = (it.steps > C::kStages ? it.steps - C::kStages : 0); s < it.steps; ++s) {
+            mbar_wait(bar_at(bar0, KV_Q_FULL + s % C::kStages), (s / C::kStages) & 1, p.err);
+            mbar_wait(bar_at(bar0, KV_G_FULL + s % C::kStages), (s / C::kStages) & 1, p.err);
+        }
     }
     __syncwarp();
 }
@@ -501,11 +511,15 @@ __device__ __noinline__ void kv_mma(const BwdParams& p, const KvItem& it, uint32
     bool ok = mbar_wait(bar_at(bar0, KV_FULL), 0, p.err);
     const int n = it.steps;
     if (ok && n > 0) {
-        ok = mbar_wait(bar_at(bar0, KV_STAGE_FULL + 0), 0, p.err);
+        ok = mbar_wait(bar_at(bar0, KV_Q_FULL + 0), 0, p.err);
         if (ok) {
             tc_fence_after_sync();
             issue_nt<HD>(t_s, dk_desc, dq_k0);
             tc_commit(bar_at(bar0, KV_S_FULL));
+            ok = mbar_wait(bar_at(bar0, KV_G_FULL + 0), 0, p.err);
+        }
+        if (ok) {
+            tc_fence_after_sync();
             issue_nt<HD>(t_dp, dv_desc, dg_k0);
             tc_commit(bar_at(bar0, KV_DP_FULL));
         }
@@ -516,10 +530,12 @@ __device__ __noinline__ void kv_mma(const BwdParams& p, const KvItem& it, uint32
         if (!ok) break;
         tc_fence_after_sync();
         issue_tn<HD>(t_dv, t_s, dg_mn0 + st * kStageDesc, s == 0);  // dV += P^T G_i
+        tc_commit(bar_at(bar0, KV_G_EMPTY + st));                     // G_i has no later reader
         const bool more = s + 1 < n;
         const int st1 = (s + 1) % C::kStages;
+        const uint32_t par1 = ((s + 1) / C::kStages) & 1;
         if (more) {
-            ok = mbar_wait(bar_at(bar0, KV_STAGE_FULL + st1), ((s + 1) / C::kStages) & 1, p.err);
+            ok = mbar_wait(bar_at(bar0, KV_Q_FULL + st1), par1, p.err);
             if (!ok) break;
             tc_fence_after_sync();
             issue_nt<HD>(t_s, dk_desc, dq_k0 + st1 * kStageDesc);  // S^T(s+1)
@@ -529,8 +545,11 @@ __device__ __noinline__ void kv_mma(const BwdParams& p, const KvItem& it, uint32
         if (!ok) break;
         tc_fence_after_sync();
         issue_tn<HD>(t_dk, t_dp, dq_mn0 + st * kStageDesc, s == 0);  // dK += dS^T Q_i
-        tc_commit(bar_at(bar0, KV_STAGE_EMPTY + st));
+        tc_commit(bar_at(bar0, KV_Q_EMPTY + st));  // Q_i and the stage's vectors
         if (more) {
+            ok = mbar_wait(bar_at(bar0, KV_G_FULL + st1), par1, p.err);
+            if (!ok) break;
+            tc_fence_after_sync();
             issue_nt<HD>(t_dp, dv_desc, dg_k0 + st1 * kStageDesc);  // dP^T(s+1)
             tc_commit(bar_at(bar0, KV_DP_FULL));
         }
@@ -563,10 +582,9 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
         const int qt = it.qt_lo + s % it.nqt;
         const int c0 = qt * kBM + half * 64;  // first query of this thread's columns
         const uint32_t vec = stage0 + st * C::kStageBytes + 2 * T::kBytes;  // -lse*log2e [128], then -D [128]
-        // acquire the stage's vectors (written by the producer lanes before
-        // they arrived on its full barrier; the stage is not refilled before
-        // this step's dK product has read it), then S^T(s)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, KV_STAGE_FULL + st), (s / C::kStages) & 1, p.err) &&
+        // acquire the stage's vectors (copied with Q_i; the Q part of the
+        // stage is not refilled before this step's dK product), then S^T(s)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, KV_Q_FULL + st), (s / C::kStages) & 1, p.err) &&
                                          mbar_wait(bar_at(bar0, KV_S_FULL), s & 1, p.err));
         if (!ok) break;
         tc_fence_after_sync();
@@ -650,8 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     if (threadIdx.x == 0) {
         mbar_init(bar_at(bar0, KV_FULL), 1);
         for (int s = 0; s < KvCfg<HD>::kStages; ++s) {
-            mbar_init(bar_at(bar0, KV_STAGE_FULL + s), 1);
-            mbar_init(bar_at(bar0, KV_STAGE_EMPTY + s), 1);
+            mbar_init(bar_at(bar0, KV_Q_FULL + s), 1);
+            mbar_init(bar_at(bar0, KV_Q_EMPTY + s), 1);
+            mbar_init(bar_at(bar0, KV_G_FULL + s), 1);
+            mbar_init(bar_at(bar0, KV_G_EMPTY + s), 1);
         }
         mbar_init(bar_at(bar0, KV_S_FULL), 1);
         mbar_init(bar_at(bar0, KV_DP_FULL), 1);
