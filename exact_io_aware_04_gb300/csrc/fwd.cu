@@ -541,67 +541,85 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                 for (int c = 0; c < 128; ++c)
                     if (c > hi_lim) x[c] = -INFINITY;
             }
-            // row max: 3-input max over 8 independent chains
-            float mc[8];
+            // row max of the tile in log2 units: 3-input max over 8 independent chains
+            auto row_max2 = [&]() {
+                float mc[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) mc[c] = fmaxf(x[c], x[c + 8]);
+                for (int c = 0; c < 8; ++c) mc[c] = fmaxf(x[c], x[c + 8]);
 #pragma unroll
-            for (int c = 16; c < 128; c += 16) {
+                for (int c = 16; c < 128; c += 16) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], x[c + k], x[c + 8 + k]);
-            }
-            const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-            const float mx2 = mx * sl2;
-            if (j == jlo) {
-                m_ref = mx2;
-            } else {
-                const bool need = mx2 > m_ref + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = fmaxf(m_ref, mx2);
-                    const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_ref - m_new);
-                    l *= alpha;
-                    m_ref = m_new;
-                    const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-                    for (int cc = 0; cc < HD; cc += 32) {
-                        float o[32];
-                        tmem_ld_32cols_f(t_o + cc, o);
-                        tmem_ld_wait_f(o);
+                    for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], x[c + k], x[c + 8 + k]);
+                }
+                const float mx =
+                    fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+                return mx * sl2;
+            };
+            // p = 2^(s*scale*log2e - m) into tensor memory (bf16): packed FMA
+            // for the argument, one ex2 per element, four independent packed
+            // partial sums; returns the row sum of p (fp32)
+            auto exp_pass = [&](float m) {
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const uint64_t nm2 = f2_pack(-m_use, -m_use);
+                uint64_t ls[4] = {0, 0, 0, 0};
 #pragma unroll
-                        for (int c = 0; c < 32; c += 2) {
-                            const uint64_t v = f2_mul(f2_pack(o[c], o[c + 1]), a2);
-                            f2_unpack(v, o[c], o[c + 1]);
-                        }
-                        tmem_st_32cols(t_o + cc, reinterpret_cast<const uint32_t(&)[32]>(o));
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        float a, b;
+                        f2_unpack(f2_fma(f2_pack(x[h * 64 + c], x[h * 64 + c + 1]), sc2, nm2), a, b);
+                        a = fast_exp2(a);
+                        b = fast_exp2(b);
+                        ls[(c >> 1) & 3] = f2_add(ls[(c >> 1) & 3], f2_pack(a, b));
+                        pk[c >> 1] = pack_bf16x2(a, b);
                     }
+                    tmem_st_32cols(t_s + h * 32, pk);
                 }
-            }
-            // p = 2^(s*scale*log2e - m): packed FMA for the argument, one
-            // ex2 per element, four independent packed partial sums
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            const uint64_t sc2 = f2_pack(sl2, sl2);
-            const uint64_t nm2 = f2_pack(-m_use, -m_use);
-            uint64_t ls[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float a, b;
-                    f2_unpack(f2_fma(f2_pack(x[h * 64 + c], x[h * 64 + c + 1]), sc2, nm2), a, b);
-                    a = fast_exp2(a);
-                    b = fast_exp2(b);
-                    ls[(c >> 1) & 3] = f2_add(ls[(c >> 1) & 3], f2_pack(a, b));
-                    pk[c >> 1] = pack_bf16x2(a, b);
-                }
-                tmem_st_32cols(t_s + h * 32, pk);
-            }
-            float lsum;
-            {
                 const uint64_t s01 = f2_add(ls[0], ls[1]), s23 = f2_add(ls[2], ls[3]);
                 float lo, hi;
                 f2_unpack(f2_add(s01, s23), lo, hi);
-                lsum = lo + hi;
+                return lo + hi;
+            };
+            float lsum;
+            if (j == jlo) {
+                m_ref = row_max2();
+                lsum = exp_pass(m_ref);
+            } else {
+                // Fast path: the reference max is kept unless the tile max
+                // exceeds it by more than the threshold, i.e. unless some
+                // p > 2^8.  p >= 0 and a rounded sum of non-negative terms is
+                // at least each term, so a row sum <= 2^8 proves every p of
+                // the row within the bound and the max is never needed.  A
+                // row with no key yet (reference -inf: every earlier key
+                // masked) always looks at the max.
+                lsum = exp_pass(m_ref);
+                if (__any_sync(0xffffffffu, !(lsum <= 256.f) || m_ref == -INFINITY)) {
+                    const float mx2 = row_max2();
+                    const bool need = mx2 > m_ref + kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, need)) {
+                        const float m_new = fmaxf(m_ref, mx2);
+                        const float alpha = (m_new == -INFINITY) ? 1.f : fast_exp2(m_ref - m_new);
+                        l *= alpha;
+                        m_ref = m_new;
+                        const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+                        for (int cc = 0; cc < HD; cc += 32) {
+                            float o[32];
+                            tmem_ld_32cols_f(t_o + cc, o);
+                            tmem_ld_wait_f(o);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 2) {
+                                const uint64_t v = f2_mul(f2_pack(o[c], o[c + 1]), a2);
+                                f2_unpack(v, o[c], o[c + 1]);
+                            }
+                            tmem_st_32cols(t_o + cc, reinterpret_cast<const uint32_t(&)[32]>(o));
+                        }
+                        tmem_st_wait();  // the first pass's P stores land before they are overwritten
+                        lsum = exp_pass(m_ref);
+                    }
+                }
             }
             l += lsum;
             tmem_st_wait();

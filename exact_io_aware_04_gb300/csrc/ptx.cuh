@@ -61,14 +61,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// try_wait with a suspend-time hint: the warp may sleep (up to `hint_ns`)
+// until the phase completes instead of returning at once, so a waiting warp
+// takes no issue slots from the warps that share its sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait until the barrier's phase with the given parity has completed.
 // Returns false (and records ATTN_ERR_TIMEOUT) after kWaitTimeoutNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u && global_timer_ns() - t0 > kWaitTimeoutNs) {
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 1000000u)) return true;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
             record_error(err, ATTN_ERR_TIMEOUT);
             return false;
         }

@@ -55,6 +55,23 @@ def test_small_problems_all_rows(la, cfg):
     check_all_rows(la, p)
 
 
+# Score ladders: the running max of a row holds, rises by less than the
+# rescale threshold over a whole block (row sums of p far above 2^8), jumps
+# far above it, and falls, tile after tile (workloads.score_ladder).
+LADDER = [
+    (1, 4, 2, 300, 1100, 128, False),
+    (1, 4, 2, 300, 1100, 128, True),
+    (2, 4, 4, 260, 700, 64, False),
+]
+
+
+@pytest.mark.parametrize("cfg", LADDER, ids=lambda c: "B{}_Hq{}_Hkv{}_Nq{}_Nk{}_d{}_{}".format(*c[:6], "c" if c[6] else "n"))
+def test_score_ladder_all_rows(la, cfg):
+    B, Hq, Hkv, Nq, Nk, d, causal = cfg
+    p = workloads.make_prefill(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=31 + Nk + d)
+    check_all_rows(la, workloads.score_ladder(p))
+
+
 VARLEN = [
     ([5, 300, 0, 129, 1000, 1], [5, 300, 17, 700, 1000, 1], 128, True),
     ([256, 3, 600], [100, 3, 2000], 128, True),     # a sequence with Nq > Nk

@@ -398,3 +398,24 @@ def one_hot_values(p: Prefill, base: int) -> Prefill:
                 for g in range(p.Hkv):
                     v[ck[b] + j, g, c] = float(g + 1)
     return dataclasses.replace(p, q=q, v=v)
+
+
+def score_ladder(p: Prefill, levels=(0, 4, 4, 13, 13, 2, 20, 0), block: int = 128) -> Prefill:
+    """Scores that step by key block: channel 0 of every query row is +8 (even
+    query heads) or -8 (odd query heads), channel 0 of key j is
+    levels[(j // block) % len(levels)], and the other channels are N(0, 1)/4
+    noise from the problem's own draws.  With scale 1/sqrt(128) a level step
+    of 1 moves the score by about one unit of log2, so the even heads see the
+    running maximum hold, rise a little (many keys of one block above the
+    first block's maximum) and jump (far above it); the odd heads see it
+    fall.  All values are exact in bf16."""
+    q = (p.q.float() * 0.25).to(torch.bfloat16)
+    k = (p.k.float() * 0.25).to(torch.bfloat16)
+    sign = torch.tensor([8.0 if h % 2 == 0 else -8.0 for h in range(p.Hq)])
+    q[:, :, 0] = sign.to(torch.bfloat16)
+    lens = p.seq_lens()
+    ck = [0] + list(_cumsum([nk for _, nk in lens]))
+    for b, (_, nk) in enumerate(lens):
+        lv = torch.tensor([float(levels[(j // block) % len(levels)]) for j in range(nk)])
+        k[ck[b]:ck[b] + nk, :, 0] = lv[:, None].to(torch.bfloat16)
+    return dataclasses.replace(p, q=q, k=k)
