@@ -132,3 +132,21 @@ def test_window_full_size_sampled_rows(la):
     go, gl = gather_prefill(p, out, lse, rows.numpy())
     stats = assert_close(p.name, go, gl, ref_o, ref_lse)
     print(p.name, stats)
+
+
+def test_tensors_past_4gib(la):
+    """q and out hold 2^31 elements (4 GiB) each, so the last rows sit past
+    every 32-bit element and byte offset.  A causal band of 128 keys keeps
+    the work small.  The rows checked sit at both ends of the tensors:
+    first rows that a wrapped offset would overwrite, and last rows that
+    only 64-bit arithmetic reaches."""
+    B, Hq, Hkv, N, d = 1, 64, 8, 262144, 128
+    p = workloads.make_prefill(B, Hq, Hkv, N, N, d, causal=True, seed=1237, window=(127, 0))
+    assert p.q.numel() == 1 << 31
+    out, lse = run_prefill(la, p)
+    torch.cuda.synchronize()
+    toks = [0, 1, 127, 128, 131071, 200003, N - 129, N - 128, N - 2, N - 1]
+    rows = np.array([(0, h, t) for h in (0, 37, Hq - 1) for t in toks], dtype=np.int32)
+    ref_o, ref_lse = oracle.prefill(p, rows)
+    go, gl = gather_prefill(p, out, lse, rows)
+    assert_close("past 4 GiB", go, gl, ref_o, ref_lse)
