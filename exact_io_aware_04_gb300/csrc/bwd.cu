@@ -323,21 +323,26 @@ __device__ __forceinline__ void drain_half(uint32_t taddr_row, int half, __nv_bf
 }
 
 // ============================================================================ D = rowsum(G o O)
-// d/8 threads per row, each with one 16-byte load of O and of G; the rows of
-// a warp are consecutive, so a warp reads contiguous memory.  Every lane of a
-// warp runs the same iterations (rows past the end contribute nothing), so
-// the shuffle reduction always has the full warp.  Also writes lse * log2 e,
-// both into the padded workspace layout the K/V pass copies tile by tile.
+// Block (x, h) takes kRows consecutive tokens of query head h, d/8 threads
+// per token, each with one 16-byte load of O and of G (a token's row of one
+// head is contiguous).  Consecutive tokens of one head are consecutive in the
+// lse and in the workspace, so those reads and writes are contiguous too.
+// Every lane of a warp runs the same iterations (tokens past the end
+// contribute nothing), so the shuffle reduction always has the full warp.
+// Also writes lse * log2 e, both into the padded workspace layout the K/V
+// pass copies tile by tile.
 template <int HD>
 __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const BwdParams p, const __nv_bfloat16* o,
                                                            const __nv_bfloat16* g, float* nlse2, float* ndvec,
-                                                           long long rows) {
-    constexpr int kTpr = HD / 8;              // threads per row
-    constexpr int kRowsPerBlock = 256 / kTpr;
+                                                           long long t_q) {
+    constexpr int kTpr = HD / 8;              // threads per token
+    constexpr int kRows = 256 / kTpr;         // tokens per block
     const int sub = threadIdx.x % kTpr;
-    const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kTpr;
+    const int h = blockIdx.y;
+    const long long t = static_cast<long long>(blockIdx.x) * kRows + threadIdx.x / kTpr;
     float acc = 0.f;
-    if (row < rows) {
+    if (t < t_q) {
+        const long long row = t * p.Hq + h;
         const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * HD) + sub);
         const uint4 b = __ldg(reinterpret_cast<const uint4*>(g + row * HD) + sub);
         const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
@@ -350,22 +355,21 @@ __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const BwdParams p, co
     }
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && sub == 0) {
-        const int t = static_cast<int>(row / p.Hq);   // token
-        const int h = static_cast<int>(row - static_cast<long long>(t) * p.Hq);
+    if (t < t_q && sub == 0) {
+        const int ti = static_cast<int>(t);
         int b;
         if (!p.varlen) {
-            b = t / p.Nq;
+            b = ti / p.Nq;
         } else {  // the sequence holding token t: last b with cu_q[b] <= t
             int lo = 0, hi = p.B;
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (__ldg(p.cu_q + mid) <= t) lo = mid; else hi = mid;
+                if (__ldg(p.cu_q + mid) <= ti) lo = mid; else hi = mid;
             }
             b = lo;
         }
         const Seq s = seq_of(p, b);
-        const int i = t - s.q_base;
+        const int i = ti - s.q_base;
         const long long w = static_cast<long long>(h) * p.ws_row + ws_offset(b, s.q_base) + i;
         nlse2[w] = -__ldg(p.lse + lse_index(p, b, h, s, i)) * kLog2e;
         ndvec[w] = -acc;
@@ -1077,13 +1081,13 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     p.err = dev.err_word;
 
     // D = rowsum(G o O)
-    const long long rows = static_cast<long long>(t_q) * a.Hq;
-    if (rows > 0) {
+    if (t_q > 0) {
         constexpr int kRowsPerBlock = 256 / (HD / 8);
-        attn_bwd_dot_kernel<HD><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 256, 0,
-                                  stream>>>(p, static_cast<const __nv_bfloat16*>(a.out),
-                                            static_cast<const __nv_bfloat16*>(a.dout), const_cast<float*>(p.nlse2),
-                                            const_cast<float*>(p.ndvec), rows);
+        const dim3 grid(static_cast<unsigned>((t_q + kRowsPerBlock - 1) / kRowsPerBlock), static_cast<unsigned>(a.Hq));
+        attn_bwd_dot_kernel<HD><<<grid, 256, 0, stream>>>(p, static_cast<const __nv_bfloat16*>(a.out),
+                                                          static_cast<const __nv_bfloat16*>(a.dout),
+                                                          const_cast<float*>(p.nlse2), const_cast<float*>(p.ndvec),
+                                                          static_cast<long long>(t_q));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error_message("attn_bwd_dot launch: %s", cudaGetErrorString(e));
