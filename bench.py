@@ -680,31 +680,20 @@ def run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind):
     # end to end: q, k, v, out, lse, dO from pinned host memory, dq/dk/dv back
     src = [q, k, v, out, lse, g]
     host_in = [t.cpu().pin_memory() for t in src]
-    dev_in = [torch.empty_like(t) for t in src]
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    bkw = {x: y for x, y in kw.items() if x not in ("dq", "dk", "dv")}
+    out_shapes = [(tuple(t.shape), t.dtype) for t in (dq, dk, dv)]
 
-    def one():
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        la.attn_bwd(*dev_in[:5], dev_in[5], **kw)
-        for h, d in zip(host_out, (dq, dk, dv)):
-            h.copy_(d, non_blocking=True)
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    barrier(world)
+    def compute(b, dev_in, dev_out):
+        la.attn_bwd(*dev_in[:5], dev_in[5], dq=dev_out[0], dk=dev_out[1], dv=dev_out[2], **bkw)
     n_e2e = min(args.steps, 20)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n_e2e):
-        one()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e_max, e_units = reduce_max_sum(world, e0.elapsed_time(e1), flops * n_e2e, dev)
+    barrier(world)
+    ms_e2e, host_out = run_streamed(host_in, compute, out_shapes, n_e2e, stream, dev)
+    e_max, e_units = reduce_max_sum(world, ms_e2e, flops * n_e2e, dev)
     line["e2e"] = {"value": e_units / (e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
                    "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
                    "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out), "steps": n_e2e,
-                   "note": "q, k, v, out, lse and dO copied from pinned host memory each step"}
+                   "note": "q, k, v, out, lse and dO copied from pinned host memory and dq, dk, dv copied back "
+                           "every step (transfers overlap neighbouring steps)"}
     if rank == 0 and world == 1 and args.cpu_baseline_seconds > 0:
         try:
             rate, what, dt, threads = oracle_bwd_rate(p, g_host, args.cpu_baseline_seconds, seed=4242)
@@ -722,64 +711,92 @@ def run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind):
     return 0
 
 
+def run_streamed(host_in, compute, out_shapes, steps, stream, dev, depth=2):
+    """End-to-end steps with the transfers of neighbouring steps overlapped,
+    as a streaming caller would run them: step i+1's inputs upload on one
+    copy stream while step i computes on `stream` and step i-1's results
+    download on another.  Every step still moves all of its inputs host ->
+    device and all of its results device -> host inside the timed region.
+    Device buffers are `depth`-deep; `compute(b, dev_in, dev_out)` runs step
+    buffer b.  Returns the elapsed ms between an event on `stream` before the
+    first upload and one after the last download (after 3 untimed steps)."""
+    dev_in = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in host_in] for _ in range(depth)]
+    dev_out = [[torch.empty(sh, dtype=dt, device=dev) for sh, dt in out_shapes] for _ in range(depth)]
+    host_out = [torch.empty(sh, dtype=dt).pin_memory() for sh, dt in out_shapes]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready = [ev() for _ in range(depth)]
+    comp_done = [ev() for _ in range(depth)]
+    out_done = [ev() for _ in range(depth)]
+
+    def run(n):
+        start = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        up.wait_event(start)
+        down.wait_event(start)
+        for i in range(n):
+            b = i % depth
+            with torch.cuda.stream(up):
+                if i >= depth:
+                    up.wait_event(comp_done[b])   # step i-depth has read these inputs
+                for h, d in zip(host_in, dev_in[b]):
+                    d.copy_(h, non_blocking=True)
+                in_ready[b].record(up)
+            stream.wait_event(in_ready[b])
+            if i >= depth:
+                stream.wait_event(out_done[b])    # step i-depth's results have left
+            compute(b, dev_in[b], dev_out[b])
+            comp_done[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(comp_done[b])
+                for h, d in zip(host_out, dev_out[b]):
+                    h.copy_(d, non_blocking=True)
+                out_done[b].record(down)
+        stream.wait_event(out_done[(n - 1) % depth])
+        end = torch.cuda.Event(enable_timing=True)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    run(3)
+    return run(steps), host_out
+
+
 def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev, steps, d_fn=None):
     """The headline metric through the public API with the step's inputs in
     pinned host memory: H2D copies, the call, and a D2H read of the result,
-    all inside the timed region."""
+    all inside the timed region (transfers of neighbouring steps overlap,
+    see run_streamed)."""
     if prefill is not None:
         host_in = [t.cpu().pin_memory() for t in fargs]
-        dev_in = [torch.empty_like(t) for t in fargs]
-        host_out = torch.empty(fkw["out"].shape, dtype=fkw["out"].dtype).pin_memory()
-        host_lse = torch.empty(fkw["lse"].shape, dtype=fkw["lse"].dtype).pin_memory()
-        kw = dict(fkw)
-        flops = prefill_flops(prefill)
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+        kw = {k: v for k, v in fkw.items() if k not in ("out", "lse")}
+        out_shapes = [(tuple(fkw["out"].shape), fkw["out"].dtype), (tuple(fkw["lse"].shape), fkw["lse"].dtype)]
 
-        def one():
-            for h, d in zip(host_in, dev_in):
-                d.copy_(h, non_blocking=True)
-            la.attn_fwd(*dev_in, **kw)
-            host_out.copy_(kw["out"], non_blocking=True)
-            host_lse.copy_(kw["lse"], non_blocking=True)
-        units, unit, scale = flops, "TFLOP/s", 1e-12
+        def compute(b, dev_in, dev_out):
+            la.attn_fwd(*dev_in, out=dev_out[0], lse=dev_out[1], **kw)
+        units, unit, scale = prefill_flops(prefill), "TFLOP/s", 1e-12
+        note = "prefill q, k, v copied from pinned host memory and out, lse copied back every step"
     else:
         # the step's inputs: the queries (and the new tokens' K/V when appending)
         names = ["q"] + [k for k in ("k_new", "v_new") if dkw.get(k) is not None]
         src = {"q": dargs[0], **{k: dkw[k] for k in names[1:]}}
-        host_in = {k: src[k].cpu().pin_memory() for k in names}
-        dev_in = {k: torch.empty_like(src[k]) for k in names}
-        host_out = torch.empty(dkw["out"].shape, dtype=dkw["out"].dtype).pin_memory()
-        host_lse = torch.empty(dkw["lse"].shape, dtype=dkw["lse"].dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
-        kw = dict(dkw)
-        kw.update({k: dev_in[k] for k in names[1:]})
+        host_in = [src[k].cpu().pin_memory() for k in names]
+        kw = {k: v for k, v in dkw.items() if k not in ("out", "lse", "k_new", "v_new")}
+        out_shapes = [(tuple(dkw["out"].shape), dkw["out"].dtype), (tuple(dkw["lse"].shape), dkw["lse"].dtype)]
 
-        def one():
-            for k in names:
-                dev_in[k].copy_(host_in[k], non_blocking=True)
-            d_fn(dev_in["q"], *dargs[1:], **kw)
-            host_out.copy_(dkw["out"], non_blocking=True)
-            host_lse.copy_(dkw["lse"], non_blocking=True)
+        def compute(b, dev_in, dev_out):
+            extra = dict(zip(names[1:], dev_in[1:]))
+            d_fn(dev_in[0], *dargs[1:], out=dev_out[0], lse=dev_out[1], **extra, **kw)
         units = kvcache_bytes(decode) if is_kvcache(decode) else decode_bytes(decode)
         unit, scale = "GB/s", 1e-9
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
+        note = "decode queries (and new K/V rows) copied each step; the paged cache stays resident"
     barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms, host_out = run_streamed(host_in, compute, out_shapes, steps, stream, dev)
     t_max, tot_units = reduce_max_sum(world, ms, units * steps, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
     return {"value": tot_units / (t_max * 1e-3) * scale, "unit": unit, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps,
-            "note": "prefill inputs copied from pinned host memory each step" if prefill is not None else
-                    "decode queries (and new K/V rows) copied each step; the paged cache stays resident"}
+            "d2h_bytes_per_step": d2h, "steps": steps, "note": note + " (transfers overlap neighbouring steps)"}
 
 
 def cpu_baseline(prefill, decode, seconds):
