@@ -52,6 +52,28 @@ constexpr int kMmaWarp = 9;
 constexpr int kSoftmaxWarps = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Tiled TMA store shared -> global of one box (bulk-group completion).  The
+// writer threads make their shared-memory writes visible to the async proxy
+// (fence_proxy_async_shared) and hand over through an mbarrier before one
+// thread issues it.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 template <int HD>
 struct Tile {
     static constexpr int kPanels = HD / 64;
@@ -61,6 +83,8 @@ struct Tile {
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;  // 2-D [rows, heads*d] bf16, box 64 x 128, 128B swizzle
+    CUtensorMap tm_dq, tm_dk, tm_dv;      // the same layout over the outputs (tiled stores)
+    int tma_store;                        // 1 when every output is 16-byte aligned
     const float* lse;                      // dense [B, Hq, Nq]; packed [Hq, T_q]
     // workspace: -lse * log2 e and -D, each [Hq][ws_row] fp32 (negated so
     // that the softmax threads use them in packed fma / add directly);
@@ -322,6 +346,52 @@ __device__ __forceinline__ void drain_half(uint32_t taddr_row, int half, __nv_bf
     else drain_row32(taddr_row + half * 32, dst_row + half * 32, mul, store);
 }
 
+// Rounds this thread's HD/2 accumulator columns (times mul) to bf16 and
+// writes them into a 128-row tile staged in shared memory in the layout of
+// the 128-byte-swizzled TMA maps: 64-column panels of 128 rows x 128 bytes,
+// the 16-byte chunk c of row r at chunk c ^ (r & 7) of its row.
+template <int HD>
+__device__ __forceinline__ void stage_half(uint32_t taddr_row, int half, uint32_t tile_smem, int r, float mul) {
+    constexpr int kCols = HD / 2;
+    float x[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; c += 32) tmem_ld_32cols_f(taddr_row + half * kCols + c, x + c);
+#pragma unroll
+    for (int c = 0; c < kCols; c += 32) tmem_ld_wait_f(x + c);
+#pragma unroll
+    for (int cc = 0; cc < kCols / 8; ++cc) {
+        const int col = half * kCols + cc * 8;
+        const uint32_t addr = tile_smem + (col >> 6) * Tile<HD>::kPanelBytes + r * 128 +
+                              ((((col & 63) >> 3) ^ (r & 7)) << 4);
+        const float* v = x + cc * 8;
+        sts_v4(addr, pack_bf16x2(v[0] * mul, v[1] * mul), pack_bf16x2(v[2] * mul, v[3] * mul),
+               pack_bf16x2(v[4] * mul, v[5] * mul), pack_bf16x2(v[6] * mul, v[7] * mul));
+    }
+}
+
+// The eight softmax warps have staged whole 128-row tiles: each warp makes
+// its writes visible to the async proxy and arrives on `staged` (one phase,
+// kSoftmaxWarps arrivals); thread 0 waits for all of them (a bounded wait:
+// a warp that left on an error leaves the tiles unstored and the error
+// recorded), stores the tiles with TMA panel by panel and waits until the
+// copies have read shared memory.
+template <int HD>
+__device__ __forceinline__ void store_staged(const CUtensorMap* m0, uint32_t src0, const CUtensorMap* m1,
+                                             uint32_t src1, int x, int y, uint32_t staged, int* err) {
+    fence_proxy_async_shared();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(staged);
+    if (threadIdx.x == 0 && mbar_wait(staged, 0, err)) {
+#pragma unroll
+        for (int pn = 0; pn < Tile<HD>::kPanels; ++pn) {
+            tma_store_2d(m0, src0 + pn * Tile<HD>::kPanelBytes, x + pn * 64, y);
+            if (m1 != nullptr) tma_store_2d(m1, src1 + pn * Tile<HD>::kPanelBytes, x + pn * 64, y);
+        }
+        bulk_commit_group();
+        bulk_wait_group_read0();
+    }
+}
+
 // ============================================================================ D = rowsum(G o O)
 // Block (x, h) takes kRows consecutive tokens of query head h, d/8 threads
 // per token, each with one 16-byte load of O and of G (a token's row of one
@@ -393,7 +463,7 @@ struct KvCfg {
 // have barriers of their own: S^T(s+1) needs only Q_{s+1}, and G_i is
 // released as soon as dV has read it.
 enum : int { KV_FULL = 0, KV_Q_FULL = 1, KV_Q_EMPTY = 3, KV_G_FULL = 5, KV_G_EMPTY = 7, KV_S_FULL = 9, KV_DP_FULL,
-             KV_P_READY, KV_DS_READY, KV_ACC_FULL, KV_COUNT };
+             KV_P_READY, KV_DS_READY, KV_ACC_FULL, KV_STAGED, KV_COUNT };
 
 struct KvItem {
     int b, g, j;
@@ -653,6 +723,15 @@ __device__ __noinline__ void kv_softmax(const BwdParams& p, const KvItem& it, ui
     ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, KV_ACC_FULL), 0, p.err)) && ok;
     if (!ok) return;
     tc_fence_after_sync();
+    if (p.tma_store && it.keys == kBM) {
+        // every product has completed, so K_j and V_j are no longer read:
+        // dV is staged over K_j and dK over V_j, then stored with TMA
+        stage_half<HD>(tmem + lane_off + C::kColDV, half, smem0, r, 1.f);
+        stage_half<HD>(tmem + lane_off + C::kColDK, half, smem0 + T::kBytes, r, p.scale);
+        store_staged<HD>(&p.tm_dv, smem0, &p.tm_dk, smem0 + T::kBytes, it.g * HD, it.s.k_base + it.k0,
+                         bar_at(bar0, KV_STAGED), p.err);
+        return;
+    }
     drain_half<HD>(tmem + lane_off + C::kColDV, half, dv_row, 1.f, key_valid);
     drain_half<HD>(tmem + lane_off + C::kColDK, half, dk_row, p.scale, key_valid);
 }
@@ -682,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
         mbar_init(bar_at(bar0, KV_P_READY), kSoftmaxWarps);
         mbar_init(bar_at(bar0, KV_DS_READY), kSoftmaxWarps);
         mbar_init(bar_at(bar0, KV_ACC_FULL), 1);
+        mbar_init(bar_at(bar0, KV_STAGED), kSoftmaxWarps);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -735,7 +815,8 @@ struct QCfg {
 // of one buffer completes its next phase only after every waiter has passed
 // the current one (no phase can be skipped).
 enum : int { Q_FULL = 0, Q_K_FULL = 1, Q_K_EMPTY = 5, Q_V_FULL = 9, Q_V_EMPTY = 13, Q_S_FULL = 17, Q_DP_FULL = 18,
-             Q_S_FREE = 20, Q_DS_READY = 21, Q_DQ_DONE = 23, Q_ACC_FULL = 25, Q_S_DP_DONE = 26, Q_COUNT };
+             Q_S_FREE = 20, Q_DS_READY = 21, Q_DQ_DONE = 23, Q_ACC_FULL = 25, Q_S_DP_DONE = 26, Q_STAGED = 27,
+             Q_COUNT };
 
 struct QItem {
     int b, h, i;
@@ -877,7 +958,8 @@ __device__ __noinline__ void q_mma(const BwdParams& p, const QItem& it, uint32_t
 }
 
 template <int HD>
-__device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint32_t bar0, uint32_t tmem) {
+__device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint32_t smem0, uint32_t bar0,
+                                       uint32_t tmem) {
     using C = QCfg<HD>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -947,6 +1029,14 @@ __device__ __noinline__ void q_softmax(const BwdParams& p, const QItem& it, uint
     ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, Q_ACC_FULL), 0, p.err)) && ok;
     if (!ok) return;
     tc_fence_after_sync();
+    if (p.tma_store && it.rows == kBM) {
+        // every product has completed, so Q_i is no longer read: dQ is
+        // staged over it and stored with TMA
+        stage_half<HD>(tmem + lane_off + C::kColDQ, half, smem0, r, p.scale);
+        store_staged<HD>(&p.tm_dq, smem0, nullptr, 0, it.h * HD, it.s.q_base + it.q0, bar_at(bar0, Q_STAGED),
+                         p.err);
+        return;
+    }
     drain_half<HD>(tmem + lane_off + C::kColDQ, half, dq_row, p.scale, row_valid);
 }
 
@@ -979,6 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         mbar_init(bar_at(bar0, Q_DQ_DONE + 1), 1);
         mbar_init(bar_at(bar0, Q_ACC_FULL), 1);
         mbar_init(bar_at(bar0, Q_S_DP_DONE), 1);
+        mbar_init(bar_at(bar0, Q_STAGED), kSoftmaxWarps);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) {
@@ -1002,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dq_kernel(const __grid_c
         __syncwarp();
     } else {
         regs_increase<kSoftmaxRegs>();
-        q_softmax<HD>(p, it, bar0, tmem);
+        q_softmax<HD>(p, it, smem0, bar0, tmem);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1057,6 +1148,22 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         attn_status st = encode_tma_bf16(&p.tm_k, no_keys ? a.q : a.k, 2, dims, strides, box, true);
         if (st == ATTN_OK) st = encode_tma_bf16(&p.tm_v, no_keys ? a.q : a.v, 2, dims, strides, box, true);
         if (st != ATTN_OK) return st;
+    }
+    // the outputs as TMA store targets of full tiles (outputs that are not
+    // 16-byte aligned keep the per-row stores); with no keys at all the
+    // K/V pass has no tile and dQ is all zeros, so nothing is stored by TMA
+    const auto aligned16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+    const bool any_keys = (varlen ? static_cast<uint64_t>(a.Nk) : static_cast<uint64_t>(a.B) * a.Nk) > 0;
+    if (any_keys && t_q > 0 && aligned16(a.dq) && aligned16(a.dk) && aligned16(a.dv)) {
+        const uint64_t dq_dims[2] = {static_cast<uint64_t>(a.Hq) * HD, t_q};
+        const uint64_t dq_strides[1] = {static_cast<uint64_t>(a.Hq) * HD * 2};
+        const uint64_t dk_dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, t_k};
+        const uint64_t dk_strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
+        attn_status st = encode_tma_bf16(&p.tm_dq, a.dq, 2, dq_dims, dq_strides, box, true);
+        if (st == ATTN_OK) st = encode_tma_bf16(&p.tm_dk, a.dk, 2, dk_dims, dk_strides, box, true);
+        if (st == ATTN_OK) st = encode_tma_bf16(&p.tm_dv, a.dv, 2, dk_dims, dk_strides, box, true);
+        if (st != ATTN_OK) return st;
+        p.tma_store = 1;
     }
     p.lse = a.lse;
     p.ws_row = bwd_ws_row(a.B, varlen ? a.Nq : static_cast<long long>(a.B) * a.Nq);
