@@ -174,3 +174,47 @@ def test_varlen_many_sequences(la):
 def test_varlen_window(la):
     check(la, workloads.make_varlen([200, 5, 300], [700, 5, 300], 4, 2, 128, causal=False, seed=93,
                                     window=(90, 40)))
+
+
+def test_tensors_past_4gib(la):
+    """q, dO, out and dQ hold 2^31 elements (4 GiB) each, so the last rows
+    sit past every 32-bit element and byte offset.  With a causal band of
+    128 keys each gradient depends only on nearby rows and keys, and the
+    tiles of the last 1024 tokens line up with those of a run on those
+    tokens alone: the big run's tail must equal that run bit for bit (the
+    kernels are deterministic), and the small run is checked against the
+    oracle.  The big tensors repeat a seeded 2^24-element block, which keeps
+    their generation quick."""
+    N, Hq, Hkv, d, W, T = 262144, 64, 8, 128, 127, 1024
+    scale = 1.0 / np.sqrt(d)
+    rep = lambda seed: workloads.randn_bf16((1 << 24,), seed=seed).repeat((N * Hq * d) >> 24)
+    q = rep(1301).view(1, N, Hq, d).cuda()
+    g = rep(1302).view(1, N, Hq, d).cuda()
+    k = workloads.randn_bf16((1, N, Hkv, d), seed=1303).cuda()
+    v = workloads.randn_bf16((1, N, Hkv, d), seed=1304).cuda()
+    assert q.numel() == 1 << 31
+    kw = dict(causal=True, scale=scale, window=(W, 0))
+    out, lse = la.attn_fwd(q, k, v, **kw)
+    dq, dk, dv = la.attn_bwd(q, k, v, out, lse, g, **kw)
+    torch.cuda.synchronize()
+    t0 = N - T
+    tail = lambda x: x[:, t0:].contiguous()
+    qs, ks, vs, gs = tail(q), tail(k), tail(v), tail(g)
+    out_s, lse_s = la.attn_fwd(qs, ks, vs, **kw)
+    dq_s, dk_s, dv_s = la.attn_bwd(qs, ks, vs, out_s, lse_s, gs, **kw)
+    torch.cuda.synchronize()
+    # rows from W on see the same keys in both runs; keys W .. T-W-2 are seen
+    # by the same rows, all of them from W on
+    assert torch.equal(out[:, t0 + W:], out_s[:, W:])
+    assert torch.equal(lse[:, :, t0 + W:], lse_s[:, :, W:])
+    assert torch.equal(dq[:, t0 + W:], dq_s[:, W:])
+    assert torch.equal(dk[:, t0 + W:N - W - 1], dk_s[:, W:T - W - 1])
+    assert torch.equal(dv[:, t0 + W:N - W - 1], dv_s[:, W:T - W - 1])
+    p = workloads.Prefill("tail_1024", qs.view(T, Hq, d).cpu(), ks.view(T, Hkv, d).cpu(), vs.view(T, Hkv, d).cpu(),
+                          1, Hq, Hkv, T, T, d, scale, True, seed=1301, window=(W, 0))
+    rq, rk, rv = oracle.backward(p, gs.view(T, Hq, d).cpu())
+    f = lambda t, like: t.float().cpu().double().numpy().reshape(like.shape)
+    for name, got, ref in (("dq", f(dq_s, rq), rq), ("dk", f(dk_s, rk), rk), ("dv", f(dv_s, rv), rv)):
+        rel, mx, sc = grad_stats(name, got, ref)
+        assert rel <= REL_RMS, f"tail {name}: relative RMS error {rel:.3e}"
+        assert mx <= MAX_REL * sc + ABS_FLOOR, f"tail {name}: max abs error {mx:.3e} (max |ref| {sc:.3e})"
