@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
     extern __shared__ __align__(1024) uint8_t smem_dyn[];
     __shared__ __align__(8) uint64_t bar_full[8], bar_empty[8];
 
+    // the combine kernel (a programmatic dependent launch) may be placed as
+    // soon as every CTA here has started; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int chunk = blockIdx.x;
     const int b = blockIdx.y / p.head_groups;
     const int hg = blockIdx.y - b * p.head_groups;
@@ -394,6 +397,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps) attn_decode_combine_kernel
     using Vec = typename std::conditional<V == 4, float4, float2>::type;
     __shared__ float red[kCombineWarps];
     __shared__ float acc_s[kCombineWarps][HD];
+    // launched as a programmatic dependent of the split kernel: wait until
+    // that grid has completed and its partials are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = row / (p.Hq * p.nq);
@@ -596,8 +602,17 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     c.pages_per_chunk = plan.pages_per_chunk;
     c.max_chunks = plan.max_chunks;
     const int rows = a.B * a.Hq * a.nq;
-    attn_decode_combine_kernel<HD><<<rows, 32 * kCombineWarps, 0, stream>>>(c);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows));
+    cfg.blockDim = dim3(32 * kCombineWarps);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel<HD>, c);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error_message("attn_decode_combine launch: %s", cudaGetErrorString(e));
         return ATTN_ERR_CUDA;
