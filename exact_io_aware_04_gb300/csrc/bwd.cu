@@ -407,6 +407,10 @@ __global__ void __launch_bounds__(256) attn_bwd_dot_kernel(const BwdParams p, co
                                                            long long t_q) {
     constexpr int kTpr = HD / 8;              // threads per token
     constexpr int kRows = 256 / kTpr;         // tokens per block
+    // the dK/dV pass is a programmatic dependent of this kernel: its CTAs may
+    // be placed once every block here has started (they wait for completion
+    // before reading the workspace)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int sub = threadIdx.x % kTpr;
     const int h = blockIdx.y;
     const long long t = static_cast<long long>(blockIdx.x) * kRows + threadIdx.x / kTpr;
@@ -521,6 +525,10 @@ __device__ __noinline__ void kv_producer(const BwdParams& p, const KvItem& it, u
                         it.g * HD + pn * 64, it.s.k_base + it.k0);
         }
     }
+    // this pass may start before the D kernel has finished (programmatic
+    // dependent launch): the workspace it writes is read from here on
+    if (lane == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    __syncwarp();
     for (int s = 0; s < it.steps && ok; ++s) {
         const int st = s % C::kStages;
         const int h = it.g * p.group + s / it.nqt;
@@ -745,7 +753,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     const int lane = threadIdx.x & 31;
     KvItem it;
     const bool live = kv_item(p, it);  // uniform over the CTA
-    if (!live) return;
+    // every CTA (not only those that read the workspace) ends after the D
+    // kernel has: work queued behind this pass then sees that kernel done
+    if (!live) {
+        if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     const uint32_t smem0 = (smem_addr(smem_dyn) + 1023u) & ~1023u;
     const uint32_t bar0 = smem_addr(bars);
     if (threadIdx.x == 0) {
@@ -789,6 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_dkdv_kernel(const __grid
     __syncthreads();
     tc_fence_after_sync();
     if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ============================================================================ dQ
@@ -1219,9 +1233,18 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         return ATTN_ERR_UNSUPPORTED;
     }
     if (kv_x > 0) {
-        attn_bwd_dkdv_kernel<HD><<<dim3(static_cast<unsigned>(kv_x), a.Hkv), kThreads, KvCfg<HD>::kSmemBytes,
-                                   stream>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(kv_x), static_cast<unsigned>(a.Hkv));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = KvCfg<HD>::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = t_q > 0 ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, attn_bwd_dkdv_kernel<HD>, p);
+        if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) {
             set_error_message("attn_bwd_dkdv launch: %s", cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
