@@ -526,6 +526,57 @@ def test_decode_multi_equals_prefill_on_gathered_keys():
             assert np.array_equal(out[r], o[0]) and (lse[r] == l[0] or (np.isneginf(lse[r]) and np.isneginf(l[0])))
 
 
+def test_append_kv_gathered_sequence_ends_with_the_new_rows():
+    """Independent of the oracle's position arithmetic: after the append, each
+    sequence read back with the paged gather of the paged-attention page
+    (concatenate the listed pages, keep the first `length` tokens) is its old
+    first L - Nq tokens followed by the Nq new rows, L being the length after
+    the append.  Sequences whose new positions would start below zero keep
+    only the rows that land at positions >= 0."""
+    lens = [40, 2, 17, 0, 16, 33]
+    nq = 3
+    p = workloads.make_decode(lens, 4, 2, 16, num_pages=14, seed=12, max_pages=4)
+    g = torch.Generator().manual_seed(6)
+    k_new = bf16(torch.randn(p.B, nq, p.Hkv, p.d, generator=g))
+    v_new = bf16(torch.randn(p.B, nq, p.Hkv, p.d, generator=g))
+    kc, vc = oracle.append_kv(p.k_cache, p.v_cache, p.block_table, p.seq_lens, k_new, v_new)
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        table = p.block_table[b, :-(-L // p.page_size)].tolist()
+        for after, before, new in ((kc, p.k_cache, k_new), (vc, p.v_cache, v_new)):
+            seq = paged_gather(after, table, L)
+            old = paged_gather(before, table, L)
+            kept = max(L - nq, 0)
+            assert torch.equal(seq[:kept], old[:kept])
+            assert torch.equal(seq[kept:], new[b, nq - (L - kept):])
+
+
+def test_decode_after_append_equals_prefill_over_old_keys_then_new_keys():
+    """The appended tokens are the newest keys: Nq-query decode over the
+    appended cache equals the prefill oracle (bottom-right causal corner)
+    over the old gathered keys followed by the new rows."""
+    lens = [40, 5, 17, 33]
+    nq = 4
+    p = workloads.make_decode(lens, 4, 2, 16, num_pages=12, seed=13, max_pages=3)
+    g = torch.Generator().manual_seed(7)
+    k_new = bf16(torch.randn(p.B, nq, p.Hkv, p.d, generator=g))
+    v_new = bf16(torch.randn(p.B, nq, p.Hkv, p.d, generator=g))
+    q = bf16(torch.randn(p.B, nq, p.Hq, p.d, generator=g))
+    kc, vc = oracle.append_kv(p.k_cache, p.v_cache, p.block_table, p.seq_lens, k_new, v_new)
+    rows = np.asarray([(b, h, i) for b in range(p.B) for h in range(p.Hq) for i in range(nq)], dtype=np.int32)
+    out, lse = oracle.decode_multi_rows(q, kc, vc, p.block_table, p.seq_lens, scale=p.scale, causal=True,
+                                        rows=rows)
+    for r, (b, h, i) in enumerate(rows):
+        L = lens[b]
+        table = p.block_table[b, :-(-L // p.page_size)].tolist()
+        kk = torch.cat([paged_gather(p.k_cache, table, L)[:L - nq], k_new[b]])
+        vv = torch.cat([paged_gather(p.v_cache, table, L)[:L - nq], v_new[b]])
+        o, l = oracle.prefill_rows(q[b], kk, vv, B=1, Hq=p.Hq, Hkv=p.Hkv, Nq=nq, Nk=L, scale=p.scale,
+                                   causal=True, rows=[[0, h, i]])
+        assert np.array_equal(out[r], o[0]) and lse[r] == l[0]
+
+
 def test_append_kv_writes_exactly_the_new_positions():
     """Brute force: after the append, position L - Nq + i of sequence b, looked
     up through the block table, holds new row i; every other slot keeps its

@@ -1,8 +1,9 @@
 """The oracle's pins must fail when a plausible mistake is planted in it.
 
 Each case copies the oracle package to a temporary directory, applies one
-textual mistake to oracle.c, and runs tests/test_oracle.py against the
-mutated copy in a child process: the run has to fail.
+textual mistake to oracle.c (or to the package's Python half), and runs
+tests/test_oracle.py against the mutated copy in a child process: the run has
+to fail.
 """
 import os
 import shutil
@@ -37,18 +38,23 @@ MUTATIONS = {
     "backward dV from dP": ("dv_row[c] += p[j] * bf16_value(g_row[c]);", "dv_row[c] += dp[j] * bf16_value(g_row[c]);"),
     "backward dQ from values": ("dq_row[c] += jb->scale * ds * bf16_value(k_row[c]);",
                                 "dq_row[c] += jb->scale * ds * bf16_value(jb->v[((k_first + j) * jb->Hkv + g) * (long)d + c]);"),
+    # the in-place append lives in the Python half of the oracle
+    "append position off by one": ("pos = lens[b] - Nq + i\n", "pos = lens[b] - Nq + i + 1\n", "__init__.py"),
+    "append reads seq_lens as the length before the append": ("pos = lens[b] - Nq + i\n", "pos = lens[b] + i\n",
+                                                              "__init__.py"),
 }
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name, tmp_path):
-    old, new = MUTATIONS[name]
+    old, new, *where = MUTATIONS[name]
+    fname = where[0] if where else "oracle.c"
     dst = tmp_path / "oracle"
     shutil.copytree(os.path.join(ROOT, "oracle"), dst,
                     ignore=shutil.ignore_patterns("*.so", "__pycache__", "*.tmp*"))
-    src = (dst / "oracle.c").read_text()
+    src = (dst / fname).read_text()
     assert old in src, f"mutation anchor not found: {old!r}"
-    (dst / "oracle.c").write_text(src.replace(old, new, 1))
+    (dst / fname).write_text(src.replace(old, new, 1))
     env = dict(os.environ)
     env["PYTHONPATH"] = os.pathsep.join([str(tmp_path), ROOT])
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
