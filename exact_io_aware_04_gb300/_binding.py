@@ -340,7 +340,9 @@ def attn_decode_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     """attn_decode_paged without a workspace: for callers that cannot
     allocate device memory at call time, the library keeps the per-chunk
     partials in its own fixed 32 MiB device array (shared by all calls, so
-    calls must not overlap on the GPU).  Returns (out, lse)."""
+    calls must not overlap on the GPU).  The call runs with q's device
+    current, because the array's address is taken in the current device's
+    context.  Returns (out, lse)."""
     L = lib()
     f = L.attn_decode_paged_noalloc
     if f.argtypes is None:
@@ -360,11 +362,16 @@ def attn_decode_paged_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
         raise ValueError("block_table [B, max_pages] and seq_lens [B] required")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (block_table, "block_table"),
+                 (seq_lens, "seq_lens")):
+        if t.device != q.device:
+            raise ValueError(f"{n} is on {t.device}, q on {q.device}")
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
-    _check(f(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
-             _ptr(out), _ptr(lse), B, Hq, Hkv, d, page, num_pages, float(scale), int(num_splits),
-             _stream_handle(stream)))
+    with torch.cuda.device(q.device):
+        _check(f(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), int(block_table.shape[1]),
+                 _ptr(seq_lens), _ptr(out), _ptr(lse), B, Hq, Hkv, d, page, num_pages, float(scale),
+                 int(num_splits), _stream_handle(stream)))
     return out, lse

@@ -112,6 +112,35 @@ attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const 
     return ATTN_OK;
 }
 
+// Every check of the paged-decode entry points except those on the
+// workspace; fills the chunk plan on success.
+attn_status decode_check(const char* fn, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                         const void* v_cache, const int* block_table, int max_pages_per_seq, const int* seq_lens,
+                         const void* out, const float* lse, int B, int Nq, int Hq, int Hkv, int d, int page_size,
+                         int num_pages, float scale, int causal, int num_splits, DecodePlan* plan) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if ((k_new == nullptr) != (v_new == nullptr)) return fail(ATTN_ERR_INVALID_ARG, "%s: give both k_new and v_new or neither", fn);
+    if (B < 0 || Nq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: bad size", fn);
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "%s: Hq %% Hkv != 0 (%d, %d)", fn, Hq, Hkv);
+    if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", fn);
+    if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse) ||
+        (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "%s: head_dim %d (built: 64, 128)", fn, d);
+    if (page_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "%s: page_size %d (built: 16)", fn, page_size);
+    if (static_cast<long long>(max_pages_per_seq) * page_size > INT32_MAX)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: sequences longer than 2^31 tokens", fn);
+    if (static_cast<long long>(Hq / Hkv) * Nq > 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: (Hq/Hkv) * Nq = %lld query rows per K/V head (built: up to 128)", fn,
+                    static_cast<long long>(Hq / Hkv) * Nq);
+    if (!make_decode_plan(B, Nq, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, plan))
+        return fail(ATTN_ERR_UNSUPPORTED, "%s: no plan for Hq/Hkv = %d, Nq = %d", fn, Hq / Hkv, Nq);
+    return ATTN_OK;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -255,27 +284,13 @@ attn_status decode_call(const char* fn, const void* q, const void* k_new, const 
                         void* v_cache, const int* block_table, int max_pages_per_seq, const int* seq_lens, void* out,
                         float* lse, int B, int Nq, int Hq, int Hkv, int d, int page_size, int num_pages, float scale,
                         int causal, int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse || !workspace)
-        return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", fn);
-    if ((k_new == nullptr) != (v_new == nullptr)) return fail(ATTN_ERR_INVALID_ARG, "%s: give both k_new and v_new or neither", fn);
-    if (B < 0 || Nq <= 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pages_per_seq <= 0 || num_splits < 0)
-        return fail(ATTN_ERR_INVALID_ARG, "%s: bad size", fn);
-    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "%s: Hq %% Hkv != 0 (%d, %d)", fn, Hq, Hkv);
-    if (!isfinite(scale) || !(scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "%s: scale must be finite and > 0", fn);
-    if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(lse) ||
-        (k_new && (!aligned16(k_new) || !aligned16(v_new))) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
-    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "%s: head_dim %d (built: 64, 128)", fn, d);
-    if (page_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "%s: page_size %d (built: 16)", fn, page_size);
-    if (static_cast<long long>(max_pages_per_seq) * page_size > INT32_MAX)
-        return fail(ATTN_ERR_UNSUPPORTED, "%s: sequences longer than 2^31 tokens", fn);
-    if (static_cast<long long>(Hq / Hkv) * Nq > 128)
-        return fail(ATTN_ERR_UNSUPPORTED, "%s: (Hq/Hkv) * Nq = %lld query rows per K/V head (built: up to 128)", fn,
-                    static_cast<long long>(Hq / Hkv) * Nq);
     DecodePlan plan;
-    if (!make_decode_plan(B, Nq, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan))
-        return fail(ATTN_ERR_UNSUPPORTED, "%s: no plan for Hq/Hkv = %d, Nq = %d", fn, Hq / Hkv, Nq);
+    attn_status st = decode_check(fn, q, k_new, v_new, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens,
+                                  out, lse, B, Nq, Hq, Hkv, d, page_size, num_pages, scale, causal, num_splits, &plan);
+    if (st != ATTN_OK) return st;
+    if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "%s: NULL pointer", fn);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "%s: misaligned pointer", fn);
     if (workspace_bytes < plan.total_bytes)
         return fail(ATTN_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", fn, workspace_bytes,
                     plan.total_bytes);

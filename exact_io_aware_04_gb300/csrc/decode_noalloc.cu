@@ -14,8 +14,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "internal.h"
 
 namespace attn {
@@ -28,33 +26,19 @@ constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (the first call on a device does it).
+// Device address of the scratch array in the current device's context.  It is
+// looked up on every call (a table lookup once the module is loaded), so a
+// context that was torn down and rebuilt -- cudaDeviceReset, or recovery from
+// a sticky error, which reloads the module -- never sees a stale address.  The
+// first call on a device may load the module.
 attn_status scratch_on_current_device(void** out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        set_error_message("cudaGetDevice: %s", cudaGetErrorString(e));
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        set_error_message("cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
         return ATTN_ERR_CUDA;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        set_error_message("device index %d out of range", dev);
-        return ATTN_ERR_CUDA;
-    }
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            set_error_message("cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
-            return ATTN_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return ATTN_OK;
 }
 
@@ -68,26 +52,25 @@ extern "C" attn_status attn_decode_paged_noalloc(const void* q, const void* k_ca
                                                  void* out, float* lse, int B, int Hq, int Hkv, int d,
                                                  int page_size, int num_pages, float scale, int num_splits,
                                                  void* stream) {
-    // Same plan and checks as attn_decode_paged; the scratch must fit the array.
+    // attn_decode_paged's own argument checks come first, so a bad pointer or
+    // size gets the same error as there; then the scratch must fit the array.
     DecodePlan plan;
-    if (B >= 0 && Hq > 0 && Hkv > 0 && max_pages_per_seq > 0 && num_splits >= 0 &&
-        make_decode_plan(B, 1, Hq, Hkv, d, page_size, max_pages_per_seq, num_splits, &plan) &&
-        plan.total_bytes > kScratchBytes) {
+    attn_status st = decode_check("attn_decode_paged_noalloc", q, nullptr, nullptr, k_cache, v_cache, block_table,
+                                  max_pages_per_seq, seq_lens, out, lse, B, 1, Hq, Hkv, d, page_size, num_pages,
+                                  scale, 0, num_splits, &plan);
+    if (st != ATTN_OK) return st;
+    if (plan.total_bytes > kScratchBytes) {
         set_error_message(
             "attn_decode_paged_noalloc: these sizes need %zu bytes of scratch, more than the library's fixed "
-            "%zu; use attn_decode_paged with a caller workspace, or a larger num_splits page range",
+            "%zu; use attn_decode_paged with a caller workspace, or pass a smaller nonzero num_splits "
+            "(fewer, longer chunks)",
             plan.total_bytes, kScratchBytes);
         return ATTN_ERR_INVALID_ARG;
     }
+    if (B == 0) return ATTN_OK;
     void* scratch = nullptr;
-    // Argument errors are reported by attn_decode_paged before it touches the
-    // scratch; look the array up only for calls that can run.
-    if (q && k_cache && v_cache && block_table && seq_lens && out && lse && B > 0) {
-        attn_status st = scratch_on_current_device(&scratch);
-        if (st != ATTN_OK) return st;
-    } else {
-        scratch = reinterpret_cast<void*>(uintptr_t(256));  // never dereferenced: the checks reject first
-    }
+    st = scratch_on_current_device(&scratch);
+    if (st != ATTN_OK) return st;
     return attn_decode_paged(q, k_cache, v_cache, block_table, max_pages_per_seq, seq_lens, out, lse, B, Hq, Hkv, d,
                              page_size, num_pages, scale, num_splits, scratch, kScratchBytes, stream);
 }

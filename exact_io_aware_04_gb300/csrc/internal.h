@@ -96,4 +96,12 @@ bool make_decode_plan(int B, int nq, int Hq, int Hkv, int d, int page_size, int 
                       DecodePlan* plan);
 attn_status launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
+// Every argument check of the paged-decode entry points except those on the
+// workspace (pointers, sizes, alignment, head_dim, page size, plan); fills
+// `plan` on success.  `fn` names the entry point in the error message.
+attn_status decode_check(const char* fn, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                         const void* v_cache, const int* block_table, int max_pages_per_seq, const int* seq_lens,
+                         const void* out, const float* lse, int B, int Nq, int Hq, int Hkv, int d, int page_size,
+                         int num_pages, float scale, int causal, int num_splits, DecodePlan* plan);
+
 }  // namespace attn

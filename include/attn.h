@@ -243,11 +243,14 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int d, int page_size,
  *
  *  - Limit: the scratch that attn_decode_workspace_size reports for the same
  *    sizes must be at most 32 MiB (33554432 bytes); larger sizes return
- *    ATTN_ERR_INVALID_ARG with a message.  A larger num_splits page range
- *    (fewer chunks) shrinks the requirement.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress) and remembers it; make that first call before any
- *    stream capture begins.
+ *    ATTN_ERR_INVALID_ARG with a message.  A smaller nonzero num_splits
+ *    (fewer, longer chunks per sequence) shrinks the requirement.
+ *  - Argument errors are checked first and reported exactly as
+ *    attn_decode_paged reports them; the size limit is checked after them.
+ *  - Every call looks up the array's device address in the current device's
+ *    context (cudaGetSymbolAddress); the first call on a device may load the
+ *    library's device code there, so make that first call before any stream
+ *    capture begins.
  *  - All calls share the one array and it keeps the last call's contents
  *    (nothing in it needs to start at zero).  Calls that overlap on the GPU
  *    -- on different streams, or from different threads -- race on it: order

@@ -98,6 +98,32 @@ def test_decode_host_rejections(lib):
     assert dec(lib, B=0) == 0
 
 
+def noalloc(lib, q=FAKE, out=FAKE, B=64, Hq=32, Hkv=8, d=128, max_pages=2048, splits=64, scale=0.1):
+    f = lib.attn_decode_paged_noalloc
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.argtypes = [P, P, P, P, I, P, P, P, I, I, I, I, I, I, F, I, P]
+    f.restype = I
+    return f(q, FAKE, FAKE, FAKE, max_pages, FAKE, out, FAKE, B, Hq, Hkv, d, 16, 10, scale, splits, None)
+
+
+def test_decode_noalloc_host_rejections(lib):
+    """Argument errors come first, worded as attn_decode_paged words them; the
+    fixed-array limit (32 MiB of partials) is checked only after them."""
+    assert noalloc(lib, q=None) == -1
+    assert b"NULL pointer" in lib.attn_last_error_message()
+    assert noalloc(lib, out=ctypes.c_void_p(0x10008)) == -1
+    assert b"misaligned" in lib.attn_last_error_message()
+    assert noalloc(lib, Hq=30) == -1
+    assert b"Hq % Hkv" in lib.attn_last_error_message()
+    assert noalloc(lib, d=96) == -2
+    # valid arguments whose partials need about 64.5 MiB: rejected by the limit
+    assert lib.attn_decode_workspace_size(64, 32, 8, 128, 16, 2048, 64) > (64 << 20)
+    assert noalloc(lib) == -1
+    assert b"scratch" in lib.attn_last_error_message()
+    assert b"smaller nonzero num_splits" in lib.attn_last_error_message()
+    assert noalloc(lib, B=0, splits=16) == 0       # fits, nothing to do
+
+
 def bwd(lib, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, causal=1, wl=-1, wr=-1, ws=ctypes.c_void_p(0x100000),
         ws_bytes=1 << 20, dout=FAKE):
     return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, dout, FAKE, FAKE, FAKE, FAKE, B, Hq, Hkv, Nq, Nk, d, 0.1, causal,

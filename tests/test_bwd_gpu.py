@@ -5,9 +5,12 @@ output and lse come from attn_fwd; dO is seeded.
 Tolerance (the accuracy contract states none for gradients): the kernels
 round P, dS and the three outputs to bf16 (relative 2^-9 each) and build D
 from the bf16 forward output, so every gradient element carries a few bf16
-roundings of terms of its own size: relative RMS <= 1e-2 per tensor, and
-max |err| <= 2e-2 * max |ref| (a single worst element may sit on several
-rounding errors of the same sign), plus an absolute floor of 1e-4 for the
+roundings of terms of its own size.  A single bf16 rounding of uniformly
+distributed relative position has an RMS of 2^-9/sqrt(3) = 1.1e-3; the
+measured relative RMS is 2.2-2.6e-3 on every case (two to three such
+roundings), bounded here at 5e-3 per tensor.  max |err| <= 1e-2 * max |ref|
+(measured at most 0.52%: a single worst element may sit on several rounding
+errors of the same sign), plus an absolute floor of 1e-4 for the
 fp32 residue of exact cancellations (a row with a single key has dS = 0 in
 exact arithmetic; dP and D = G.O are then two fp32 dot products of d terms
 that agree to ~1e-6)."""
@@ -23,8 +26,8 @@ from parity import run_prefill
 
 pytestmark = pytest.mark.gpu
 
-REL_RMS = 1e-2
-MAX_REL = 2e-2
+REL_RMS = 5e-3
+MAX_REL = 1e-2
 ABS_FLOOR = 1e-4
 
 

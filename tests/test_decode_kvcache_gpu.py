@@ -139,7 +139,8 @@ def test_append_with_bad_pages_writes_nothing_outside(la):
 
 
 def test_full_size_spec_decode(la):
-    p = workloads.spec_decode(device="cuda")
+    # NaN in every unused slot, and in the slots the append fills until it writes them
+    p = workloads.spec_decode(device="cuda", nan_fill_unused=True)
     host = p.to("cpu")   # the inputs, before the call writes the device cache
     out, lse = la.attn_decode_kvcache(p.q, p.k_cache, p.v_cache, p.block_table, p.seq_lens, k_new=p.k_new,
                                       v_new=p.v_new, causal=True, scale=p.scale)

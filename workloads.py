@@ -339,14 +339,14 @@ def make_kvcache_decode(seq_lens, Nq, Hq, Hkv, d, *, num_pages, seed, causal=Tru
                          B, Nq, Hq, Hkv, d, page_size, num_pages, base.scale, bool(causal), seed=seed)
 
 
-def spec_decode(device="cpu") -> KVCacheDecode:
+def spec_decode(device="cpu", nan_fill_unused=False) -> KVCacheDecode:
     """Speculative-decoding verify step: B=64, Nq=4 new tokens per sequence,
     Hq=32, Hkv=8, d=128, len ~ U[4096, 32768] after the append, causal, 16-token
     pages in a 200,000-page pool, block table [64, 2048]."""
     lens = decode_lengths(seed=SEED_BASE + 7)
     return make_kvcache_decode(lens, 4, 32, 8, 128, num_pages=200_000, seed=SEED_BASE + 7, causal=True,
-                               append=True, max_pages=2048, name="spec_decode_b64_nq4_hq32_hkv8_d128",
-                               device=device)
+                               append=True, max_pages=2048, nan_fill_unused=nan_fill_unused,
+                               name="spec_decode_b64_nq4_hq32_hkv8_d128", device=device)
 
 
 # --------------------------------------------------------------------------
