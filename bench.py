@@ -1,24 +1,33 @@
 """Benchmark of the exact-attention hot path on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-  * attn_fwd on the MHA causal prefill workload (B=4, Hq=Hkv=16, N=4096,
-    d=128, bottom-right causal), and
-  * attn_decode_paged on the paged split-KV decode workload (B=64, Hq=32,
-    Hkv=8, d=128, lengths U[4096, 32768], 16-token pages, 200k-page pool).
-`value` is the prefill throughput in TFLOP/s (exact attended query-key pairs
-x 4 x d, i.e. causal-adjusted); the decode bandwidth in GB/s (algorithmic
-bytes: every K/V row the sequences own, read once, plus q, out, lse and the
-block-table rows) is reported beside it.  Both are timed per call with CUDA
-events on the launching stream; L2 is flushed (a 256 MB write) between steps,
-outside the timed calls.
+attn_fwd on each single-GPU prefill configuration and attn_decode_paged on the
+paged decode configuration, all inputs resident in HBM:
+  * GQA causal prefill  B=2, Hq=32, Hkv=8, N=8192, d=128, one K channel x3
+    (the largest configuration: it carries the headline `value`),
+  * MHA causal prefill  B=4, Hq=Hkv=16, N=4096, d=128,
+  * varlen chunked prefill  16 sequences, Nk ~ U[1024, 16384], Nq = min(512, Nk),
+    Hq=32, Hkv=8, d=128, packed with cu_seqlens,
+  * paged split-KV decode  B=64, Hq=32, Hkv=8, d=128, lengths U[4096, 32768],
+    16-token pages in a 200k-page pool.
+Prefill throughput is TFLOP/s of exact attended query-key pairs x 4 x d
+(causal-adjusted); decode bandwidth is GB/s of algorithmic bytes (every K/V
+row the sequences own, read once, plus q, out, lse and the block-table rows).
+Every call is timed with CUDA events on the launching stream; L2 is flushed
+(a 256 MB write) at the start of each step, outside the timed calls.  Each
+configuration gets its own roofline record and, on rank 0 with one GPU, an
+accuracy record against the fp64 oracle on a seeded row sample (the CPU
+baseline leg).  After the step, the next rows (backward, local window,
+several queries with the in-place append) are timed on their own.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
                   [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|swa_causal|tiny|
                               paged_decode|paged_decode_small|spec_decode|mha_causal_bwd|gqa_causal_bwd]
+                  [--no-next]
 
 --impl reference times the fp64 CPU oracle on the host cores (bounded row
-samples of the same workload, same metric and unit).  Under torchrun each rank
-runs an independent replica on its own GPU (the path needs no exchange);
+samples of the headline workload, same metric and unit).  Under torchrun each
+rank runs an independent replica on its own GPU (the path needs no exchange);
 rank 0 prints one JSON line with the max time over ranks.
 """
 from __future__ import annotations
@@ -158,21 +167,24 @@ def load_peaks():
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every `period_ms`, each
+    sample stamped with the host clock when it arrives so that the samples of
+    a window (the timed region) can be summarised on their own."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.samples = []   # (host time, csv line)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -182,7 +194,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -193,10 +205,14 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and throttle reasons of the samples that
+        arrived in [t0, t1] (all samples when no window is given)."""
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.samples:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -212,6 +228,14 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+    def record(self, t0, t1):
+        """The timed window's summary, with the whole run (warm-up included,
+        sampler started before it) beside it."""
+        rec = self.summary(t0, t1)
+        rec["period_ms"] = self.period_ms
+        rec["whole_run"] = self.summary()
+        return rec
 
 
 # ---------------------------------------------------------------- distributed
@@ -363,27 +387,194 @@ def oracle_decode_rate(d, target_s: float, seed: int):
 
 
 # ---------------------------------------------------------------- main
+# The default step: the three single-GPU prefill configurations (the largest,
+# GQA causal N8192, first: it carries the headline value) and the paged decode.
+HOT_PREFILL = ("gqa_causal", "mha_causal", "varlen_chunked")
+DECODE_WORKLOADS = ("paged_decode", "paged_decode_small", "spec_decode")
+# Measured after the step on their own (backward, window, several queries with append).
+NEXT_ROWS = ("mha_causal_bwd", "gqa_causal_bwd", "swa_causal", "spec_decode")
+
+
 def make_workloads(name, device):
-    prefill = decode = None
-    if name in ("hot_path",) + PREFILL_WORKLOADS:
-        pname = "mha_causal" if name == "hot_path" else name
-        prefill = getattr(workloads, pname)() if pname != "tiny" else workloads.tiny(True)
-    if name in ("hot_path", "paged_decode"):
-        decode = workloads.paged_decode(device=device)
-    if name == "paged_decode_small":
-        decode = workloads.paged_decode_small(device=device)
-    if name == "spec_decode":
-        decode = workloads.spec_decode(device=device)
-    return prefill, decode
+    """(prefill problems on the host, decode problem on `device` or None)."""
+    if name == "hot_path":
+        return [getattr(workloads, n)() for n in HOT_PREFILL], workloads.paged_decode(device=device)
+    if name == "tiny":
+        return [workloads.tiny(True)], None
+    if name in PREFILL_WORKLOADS:
+        return [getattr(workloads, name)()], None
+    return [], getattr(workloads, name)(device=device)
+
+
+class PrefillCall:
+    """attn_fwd on one prefill problem with device-resident inputs and outputs."""
+    kind, kernel, unit, unit_scale, launches, bound = "prefill", "attn_fwd", "TFLOP/s", 1e-12, 1, "tensor"
+
+    def __init__(self, la, p, dev):
+        self.la, self.p, self.name = la, p, p.name
+        g = p.to(dev)
+        if p.varlen:
+            self.args = (g.q, g.k, g.v)
+            self.kw = dict(causal=p.causal, scale=p.scale, cu_seqlens_q=g.cu_q, cu_seqlens_k=g.cu_k)
+        else:
+            self.args = (g.q.view(p.B, p.Nq, p.Hq, p.d), g.k.view(p.B, p.Nk, p.Hkv, p.d),
+                         g.v.view(p.B, p.Nk, p.Hkv, p.d))
+            self.kw = dict(causal=p.causal, scale=p.scale)
+        if tuple(p.window) != (-1, -1):
+            self.kw["window"] = tuple(p.window)
+        self.out = torch.empty_like(self.args[0])
+        self.lse = torch.empty((p.Hq, g.q.shape[0]) if p.varlen else (p.B, p.Hq, p.Nq), dtype=torch.float32,
+                               device=dev)
+        self.units = prefill_flops(p)
+
+    def __call__(self):
+        self.la.attn_fwd(*self.args, out=self.out, lse=self.lse, **self.kw)
+
+    def describe(self):
+        p = self.p
+        return {"B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Nq": p.Nq, "Nk": p.Nk, "d": p.d, "causal": p.causal,
+                "varlen": p.varlen, "window": list(p.window)}
+
+    def roofline_extra(self):
+        return {"flops_per_launch": self.units, "flops_per_launch_literal_formula": prefill_flops_literal(self.p),
+                "compulsory_bytes": prefill_bytes(self.p)}
+
+    def e2e_parts(self):
+        """(host inputs, compute(dev_in, dev_out), output shapes, note)."""
+        host_in = [t.cpu().pin_memory() for t in self.args]
+        kw = dict(self.kw)
+
+        def compute(dev_in, dev_out):
+            self.la.attn_fwd(*dev_in, out=dev_out[0], lse=dev_out[1], **kw)
+        shapes = [(tuple(self.out.shape), self.out.dtype), (tuple(self.lse.shape), self.lse.dtype)]
+        return host_in, compute, shapes, "prefill q, k, v copied from pinned host memory and out, lse copied back every step"
+
+
+class DecodeCall:
+    """attn_decode_paged (one query) or attn_decode_kvcache (several, with the
+    append) on a decode problem whose paged cache stays resident."""
+    kind, unit, unit_scale, bound = "decode", "GB/s", 1e-9, "hbm"
+
+    def __init__(self, la, d, dev):
+        self.la, self.d, self.name = la, d, d.name
+        self.dargs = (d.q, d.k_cache, d.v_cache, d.block_table, d.seq_lens)
+        self.out = torch.empty_like(d.q)
+        if is_kvcache(d):
+            ws = la.attn_decode_kvcache_workspace_size(d.B, d.Nq, d.Hq, d.Hkv, d.d, d.page_size, d.max_pages, 0)
+            self.lse = torch.empty((d.B, d.Hq, d.Nq), dtype=torch.float32, device=dev)
+            self.dkw = dict(k_new=d.k_new, v_new=d.v_new, causal=d.causal, scale=d.scale)
+            self.fn, self.kernel = la.attn_decode_kvcache, "attn_decode_kvcache"
+            self.units, self.launches = kvcache_bytes(d), 2 + (d.k_new is not None)
+        else:
+            ws = la.attn_decode_workspace_size(d.B, d.Hq, d.Hkv, d.d, d.page_size, d.max_pages, 0)
+            self.lse = torch.empty((d.B, d.Hq), dtype=torch.float32, device=dev)
+            self.dkw = dict(scale=d.scale)
+            self.fn, self.kernel = la.attn_decode_paged, "attn_decode_paged"
+            self.units, self.launches = decode_bytes(d), 2
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.fn(*self.dargs, out=self.out, lse=self.lse, workspace=self.ws, **self.dkw)
+
+    def describe(self):
+        d = self.d
+        r = {"B": d.B, "Hq": d.Hq, "Hkv": d.Hkv, "d": d.d, "page_size": d.page_size, "num_pages": d.num_pages,
+             "tokens": int(d.seq_lens.sum())}
+        if is_kvcache(d):
+            r.update(Nq=d.Nq, causal=d.causal, append=d.k_new is not None)
+        return r
+
+    def roofline_extra(self):
+        return {"bytes_per_call": self.units, "launches_per_call": self.launches}
+
+    def e2e_parts(self):
+        names = ["q"] + [k for k in ("k_new", "v_new") if self.dkw.get(k) is not None]
+        src = {"q": self.dargs[0], **{k: self.dkw[k] for k in names[1:]}}
+        host_in = [src[k].cpu().pin_memory() for k in names]
+        kw = {k: v for k, v in self.dkw.items() if k not in ("k_new", "v_new")}
+
+        def compute(dev_in, dev_out):
+            extra = dict(zip(names[1:], dev_in[1:]))
+            self.fn(dev_in[0], *self.dargs[1:], out=dev_out[0], lse=dev_out[1], workspace=self.ws, **extra, **kw)
+        shapes = [(tuple(self.out.shape), self.out.dtype), (tuple(self.lse.shape), self.lse.dtype)]
+        return host_in, compute, shapes, "decode queries (and new K/V rows) copied each step; the paged cache stays resident"
+
+
+def time_calls(calls, steps, warmup, stream, flush, sampler=None):
+    """W untimed steps, then `steps` timed ones.  A step flushes L2 (a 256 MB
+    write) and runs every call once; each call is bracketed by CUDA events on
+    the launching stream.  Returns (ms per call per step, wall seconds and
+    host window of the timed region)."""
+    def step(ev=None):
+        flush.fill_(1)
+        for c, fn in enumerate(calls):
+            if ev is not None:
+                ev[c][0].record(stream)
+            fn()
+            if ev is not None:
+                ev[c][1].record(stream)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+              for _ in range(steps)]
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(events[i])
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    ms = [[events[i][c][0].elapsed_time(events[i][c][1]) for i in range(steps)] for c in range(len(calls))]
+    return ms, t1 - t0, (t0, t1)
+
+
+def call_roofline(call, ms, peaks, peaks_kind):
+    """Roofline record of one call from its per-step CUDA-event times."""
+    mean = sum(ms) / len(ms)
+    ach = call.units / (mean * 1e-3) * call.unit_scale
+    peak = peaks["bf16_tflops"] if call.bound == "tensor" else peaks["hbm_gbs"]
+    nominal = NOMINAL["bf16_tflops"] if call.bound == "tensor" else NOMINAL["hbm_gbs"]
+    rec = {"kernel": call.kernel, "bound": call.bound, "achieved": ach, "peak": peak, "unit": call.unit,
+           "frac": ach / peak, "frac_nominal": nominal and ach / nominal,
+           "traffic": measured_traffic(call.kernel, call.name),
+           "peak_source": f"{peaks_kind} " + ("bf16 burst" if call.bound == "tensor" else "copy bandwidth"),
+           "ms_mean": mean, "ms_median": statistics.median(ms), "ms_p95": sorted(ms)[int(0.95 * (len(ms) - 1))]}
+    rec.update(call.roofline_extra())
+    return rec
+
+
+def kernel_roofline(calls, ms, peaks, peaks_kind):
+    """The dominant kernel (most device time in the step) over all its
+    launches: achieved = algorithmic work per launch / average launch time,
+    i.e. the total work of its launches over their total time."""
+    by_kernel = {}
+    for c, call in enumerate(calls):
+        by_kernel.setdefault(call.kernel, []).append(c)
+    kern = max(by_kernel, key=lambda k: sum(sum(ms[c]) for c in by_kernel[k]))
+    idx = by_kernel[kern]
+    first = calls[idx[0]]
+    tot_ms = sum(sum(ms[c]) for c in idx)
+    steps = len(ms[idx[0]])
+    units = sum(calls[c].units for c in idx) * steps
+    ach = units / (tot_ms * 1e-3) * first.unit_scale
+    peak = peaks["bf16_tflops"] if first.bound == "tensor" else peaks["hbm_gbs"]
+    traffic = [measured_traffic(calls[c].kernel, calls[c].name) for c in idx]
+    n_launch = sum(calls[c].launches for c in idx)
+    return {"kernel": kern, "bound": first.bound, "achieved": ach, "peak": peak, "unit": first.unit,
+            "frac": ach / peak, "peak_source": f"{peaks_kind} " + ("bf16 burst" if first.bound == "tensor"
+                                                                 else "copy bandwidth"),
+            "traffic": (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None,
+            "launches_per_step": n_launch, "configs": [calls[c].name for c in idx],
+            "ms_per_launch_mean": tot_ms / (steps * len(idx))}
 
 
 def run_reference(args, world, rank):
     """fp64 CPU oracle on bounded samples of the same workload."""
     if rank != 0:
         return 0
-    # the headline of the hot-path step is the prefill metric; the CPU arm
-    # times that part (the decode pool would not fit a bounded CPU sample)
-    name = "mha_causal" if args.workload == "hot_path" else args.workload
+    # the headline of the default step is the largest prefill configuration;
+    # the CPU arm times that part (the decode pool would not fit a bounded CPU sample)
+    name = HOT_PREFILL[0] if args.workload == "hot_path" else args.workload
     # each step is a bounded sample: about 4 s, but the whole --steps/--warmup run stays near
     # 150 s of oracle work however many steps are asked for
     per_step = float(os.environ.get("ATTN_REFERENCE_STEP_SECONDS", "4.0"))
@@ -393,7 +584,8 @@ def run_reference(args, world, rank):
         decode = None
         grad = workloads.randn_bf16(tuple(prefill.q.shape), seed=prefill.seed + 900)
     else:
-        prefill, decode = make_workloads(name, "cpu")
+        prefills, decode = make_workloads(name, "cpu")
+        prefill = prefills[0] if prefills else None
     if name in BWD_WORKLOADS:
         rate_fn = lambda s: oracle_bwd_rate(prefill, grad, per_step, seed=s)[0]
         unit, metric_scale = "TFLOP/s", 1e-12
@@ -439,13 +631,13 @@ BWD_METRIC = "bwd TFLOP/s (5 recomputation products per attended pair) & % bf16 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libattn", "reference"], default="libattn")
     ap.add_argument("--workload", default="hot_path",
-                    choices=["hot_path", "paged_decode", "paged_decode_small", "spec_decode"]
-                    + list(PREFILL_WORKLOADS) + list(BWD_WORKLOADS))
+                    choices=["hot_path"] + list(DECODE_WORKLOADS) + list(PREFILL_WORKLOADS) + list(BWD_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
+    ap.add_argument("--no-next", action="store_true", help="skip the separately timed next rows")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -460,151 +652,64 @@ def main(argv=None):
     if args.workload in BWD_WORKLOADS:
         return run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind)
 
-    prefill, decode = make_workloads(args.workload, dev)
-    # ---- device-resident inputs
-    if prefill is not None:
-        pg = prefill.to(dev)
-        if prefill.varlen:
-            fargs = (pg.q, pg.k, pg.v)
-            fkw = dict(causal=pg.causal, scale=pg.scale, cu_seqlens_q=pg.cu_q, cu_seqlens_k=pg.cu_k)
-        else:
-            fargs = (pg.q.view(pg.B, pg.Nq, pg.Hq, pg.d), pg.k.view(pg.B, pg.Nk, pg.Hkv, pg.d),
-                     pg.v.view(pg.B, pg.Nk, pg.Hkv, pg.d))
-            fkw = dict(causal=pg.causal, scale=pg.scale)
-        if tuple(prefill.window) != (-1, -1):
-            fkw["window"] = tuple(prefill.window)
-        f_out = torch.empty_like(fargs[0])
-        f_lse = torch.empty((pg.Hq, pg.q.shape[0]) if prefill.varlen else (pg.B, pg.Hq, pg.Nq),
-                            dtype=torch.float32, device=dev)
-        fkw.update(out=f_out, lse=f_lse)
-        p_flops = prefill_flops(prefill)
-    d_kernel, d_fn, d_launches = None, None, 0
-    if decode is not None and is_kvcache(decode):
-        ws = torch.empty(la.attn_decode_kvcache_workspace_size(decode.B, decode.Nq, decode.Hq, decode.Hkv,
-                                                               decode.d, decode.page_size, decode.max_pages, 0),
-                         dtype=torch.uint8, device=dev)
-        d_out = torch.empty_like(decode.q)
-        d_lse = torch.empty((decode.B, decode.Hq, decode.Nq), dtype=torch.float32, device=dev)
-        dargs = (decode.q, decode.k_cache, decode.v_cache, decode.block_table, decode.seq_lens)
-        dkw = dict(k_new=decode.k_new, v_new=decode.v_new, causal=decode.causal, scale=decode.scale, out=d_out,
-                   lse=d_lse, workspace=ws)
-        d_bytes = kvcache_bytes(decode)
-        d_kernel, d_fn, d_launches = "attn_decode_kvcache", la.attn_decode_kvcache, 2 + (decode.k_new is not None)
-    elif decode is not None:
-        ws = torch.empty(la.attn_decode_workspace_size(decode.B, decode.Hq, decode.Hkv, decode.d,
-                                                       decode.page_size, decode.max_pages, 0),
-                         dtype=torch.uint8, device=dev)
-        d_out = torch.empty_like(decode.q)
-        d_lse = torch.empty((decode.B, decode.Hq), dtype=torch.float32, device=dev)
-        dargs = (decode.q, decode.k_cache, decode.v_cache, decode.block_table, decode.seq_lens)
-        dkw = dict(scale=decode.scale, out=d_out, lse=d_lse, workspace=ws)
-        d_bytes = decode_bytes(decode)
-        d_kernel, d_fn, d_launches = "attn_decode_paged", la.attn_decode_paged, 2
+    prefills, decode = make_workloads(args.workload, dev)
+    calls = [PrefillCall(la, p, dev) for p in prefills] + ([DecodeCall(la, decode, dev)] if decode else [])
+    head = calls[0]   # the headline: the largest prefill configuration (or the one workload asked for)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step(ev=None):
-        flush.fill_(1)
-        if ev is not None:
-            ev[0].record(stream)
-        if prefill is not None:
-            la.attn_fwd(*fargs, **fkw)
-        if ev is not None:
-            ev[1].record(stream)
-        if decode is not None:
-            d_fn(*dargs, **dkw)
-        if ev is not None:
-            ev[2].record(stream)
-
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    if la.attn_get_device_status() != 0:
-        raise RuntimeError("device error during warm-up")
-
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
-    with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            step(events[i])
-        torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
+    with ClockSampler(local) as clocks:   # started before the warm-up
+        ms, t_wall, window = time_calls(calls, args.steps, args.warmup, stream, flush)
     barrier(world)
     st = la.attn_get_device_status()
     if st != 0:
         raise RuntimeError(f"device status {la.attn_status_string(st)} after the timed region")
-    f_ms = [e[0].elapsed_time(e[1]) for e in events]
-    d_ms = [e[1].elapsed_time(e[2]) for e in events]
-    f_tot, d_tot = sum(f_ms), sum(d_ms)
-    step_ms = (f_tot + d_tot) / args.steps
 
     # whole-job figures (max time over ranks, units summed over ranks)
-    rooflines = {}
-    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+    h_max, h_units = reduce_max_sum(world, sum(ms[0]), head.units * args.steps, dev)
+    value = h_units / (h_max * 1e-3) * head.unit_scale
+    rooflines = {call.name: call_roofline(call, ms[c], peaks, peaks_kind) for c, call in enumerate(calls)}
+    line = {"metric": METRIC, "value": value, "unit": head.unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sum(sum(m) for m in ms) / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) rounded to bf16)"}
-    if prefill is not None:
-        f_max, f_units = reduce_max_sum(world, f_tot, p_flops * args.steps, dev)
-        value = f_units / (f_max * 1e-3) / 1e12
-        ach = p_flops / (f_tot / args.steps * 1e-3) / 1e12
-        rooflines["attn_fwd"] = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"],
-                                 "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
-                                 "frac_nominal": ach / NOMINAL["bf16_tflops"],
-                                 "traffic": measured_traffic("attn_fwd", prefill.name),
-                                 "compulsory_bytes": prefill_bytes(prefill),
-                                 "peak_source": f"{peaks_kind} bf16 burst",
-                                 "ms_per_launch_median": statistics.median(f_ms),
-                                 "ms_per_launch_p95": sorted(f_ms)[int(0.95 * (len(f_ms) - 1))],
-                                 "flops_per_launch": p_flops,
-                                 "flops_per_launch_literal_formula": prefill_flops_literal(prefill)}
-        line.update(value=value, unit="TFLOP/s")
-    if decode is not None:
-        d_max, d_units = reduce_max_sum(world, d_tot, d_bytes * args.steps, dev)
-        dval = d_units / (d_max * 1e-3) / 1e9
-        ach = d_bytes / (d_tot / args.steps * 1e-3) / 1e9
-        rooflines[d_kernel] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                               "frac": ach / peaks["hbm_gbs"], "frac_nominal": ach / NOMINAL["hbm_gbs"],
-                               "traffic": measured_traffic(d_kernel, decode.name),
-                               "peak_source": f"{peaks_kind} copy bandwidth",
-                               "ms_per_call_median": statistics.median(d_ms),
-                               "ms_per_call_p95": sorted(d_ms)[int(0.95 * (len(d_ms) - 1))],
-                               "bytes_per_call": d_bytes, "launches_per_call": d_launches}
-        line["decode"] = {"value": dval, "unit": "GB/s", "frac_of_measured_hbm": dval / world / peaks["hbm_gbs"],
-                          "frac_of_8TBs": dval / world / NOMINAL["hbm_gbs"]}
-        if prefill is None:
-            line.update(value=dval, unit="GB/s")
-    dominant = max(rooflines, key=lambda k: (f_tot if k == "attn_fwd" else d_tot))
-    line["roofline"] = dict(rooflines[dominant], kernel=dominant)
+    line["roofline"] = kernel_roofline(calls, ms, peaks, peaks_kind)
     line["rooflines"] = rooflines
-    line["ms_per_step"] = step_ms
-    line["gpu_launches"] = args.steps * ((1 if prefill is not None else 0) + d_launches)
-    cfg = {"workload": ("mha_causal_b4_h16_n4096_d128 + paged_decode_b64_hq32_hkv8_d128"
-                        if args.workload == "hot_path" else (prefill or decode).name),
-           "l2": "flushed between steps (256 MB write, outside the timed calls)",
-           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
-    if prefill is not None:
-        cfg.update(prefill={"B": prefill.B, "Hq": prefill.Hq, "Hkv": prefill.Hkv, "Nq": prefill.Nq,
-                            "Nk": prefill.Nk, "d": prefill.d, "causal": prefill.causal,
-                            "varlen": prefill.varlen})
-    if decode is not None:
-        cfg.update(decode={"B": decode.B, "Hq": decode.Hq, "Hkv": decode.Hkv, "d": decode.d,
-                           "page_size": decode.page_size, "num_pages": decode.num_pages,
-                           "tokens": int(decode.seq_lens.sum())})
-        if is_kvcache(decode):
-            cfg["decode"].update(Nq=decode.Nq, causal=decode.causal, append=decode.k_new is not None)
-    line["config"] = cfg
-    line["clocks"] = clocks.summary()
+    line["headline"] = {"config": head.name, "kernel": head.kernel, "value": value, "unit": head.unit,
+                        "frac_of_measured_peak": rooflines[head.name]["frac"]}
+    dcall = None
+    if decode is not None and head.kind != "decode":
+        dcall = calls[-1]
+        d_max, d_units = reduce_max_sum(world, sum(ms[-1]), dcall.units * args.steps, dev)
+        dval = d_units / (d_max * 1e-3) * 1e-9
+        line["decode"] = {"config": dcall.name, "value": dval, "unit": "GB/s",
+                          "frac_of_measured_hbm": dval / world / peaks["hbm_gbs"],
+                          "frac_of_8TBs": dval / world / NOMINAL["hbm_gbs"]}
+    line["gpu_launches"] = args.steps * sum(c.launches for c in calls)
+    line["config"] = {"workload": " + ".join(c.name for c in calls), "headline": head.name,
+                      "l2": "flushed between steps (256 MB write, outside the timed calls); every input is also "
+                            "larger than L2",
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                      "calls": {c.name: c.describe() for c in calls}}
+    line["clocks"] = clocks.record(*window)
     line["wall_s_timed_region"] = t_wall
 
-    # ---- end to end through the public API with pinned host buffers
-    line["e2e"] = measure_e2e(la, prefill, decode, fargs if prefill is not None else None,
-                              fkw if prefill is not None else None, dargs if decode is not None else None,
-                              dkw if decode is not None else None, stream, world, dev,
-                              steps=min(args.steps, 20), d_fn=d_fn)
+    # ---- end to end through the public API with pinned host buffers (the headline call)
+    line["e2e"] = measure_e2e(head, stream, world, dev, steps=min(args.steps, 20))
 
+    # ---- the CPU baseline leg (rank 0, one GPU): the oracle timed on the host
+    # cores, and each configuration's GPU output checked on a seeded row sample
     if rank == 0 and world == 1 and args.cpu_baseline_seconds > 0:
-        line["cpu_baseline"] = cpu_baseline(prefill, decode, args.cpu_baseline_seconds)
+        line["cpu_baseline"] = cpu_baseline(head, args.cpu_baseline_seconds)
+        line["accuracy"] = {c.name: accuracy(c) for c in calls}
+
+    # ---- the next rows, each timed on its own after the step
+    if world == 1 and not args.no_next and args.workload == "hot_path":
+        calls.clear()   # free the step's device buffers (the 13 GB decode pool among them)
+        head = decode = prefills = dcall = None
+        torch.cuda.empty_cache()
+        line["next_rows"] = measure_next_rows(la, dev, stream, flush, min(args.steps, 20), args.warmup,
+                                              peaks, peaks_kind)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -762,59 +867,167 @@ def run_streamed(host_in, compute, out_shapes, steps, stream, dev, depth=2):
     return run(steps), host_out
 
 
-def measure_e2e(la, prefill, decode, fargs, fkw, dargs, dkw, stream, world, dev, steps, d_fn=None):
-    """The headline metric through the public API with the step's inputs in
+def measure_e2e(call, stream, world, dev, steps):
+    """The call's metric through the public API with the step's inputs in
     pinned host memory: H2D copies, the call, and a D2H read of the result,
     all inside the timed region (transfers of neighbouring steps overlap,
     see run_streamed)."""
-    if prefill is not None:
-        host_in = [t.cpu().pin_memory() for t in fargs]
-        kw = {k: v for k, v in fkw.items() if k not in ("out", "lse")}
-        out_shapes = [(tuple(fkw["out"].shape), fkw["out"].dtype), (tuple(fkw["lse"].shape), fkw["lse"].dtype)]
-
-        def compute(b, dev_in, dev_out):
-            la.attn_fwd(*dev_in, out=dev_out[0], lse=dev_out[1], **kw)
-        units, unit, scale = prefill_flops(prefill), "TFLOP/s", 1e-12
-        note = "prefill q, k, v copied from pinned host memory and out, lse copied back every step"
-    else:
-        # the step's inputs: the queries (and the new tokens' K/V when appending)
-        names = ["q"] + [k for k in ("k_new", "v_new") if dkw.get(k) is not None]
-        src = {"q": dargs[0], **{k: dkw[k] for k in names[1:]}}
-        host_in = [src[k].cpu().pin_memory() for k in names]
-        kw = {k: v for k, v in dkw.items() if k not in ("out", "lse", "k_new", "v_new")}
-        out_shapes = [(tuple(dkw["out"].shape), dkw["out"].dtype), (tuple(dkw["lse"].shape), dkw["lse"].dtype)]
-
-        def compute(b, dev_in, dev_out):
-            extra = dict(zip(names[1:], dev_in[1:]))
-            d_fn(dev_in[0], *dargs[1:], out=dev_out[0], lse=dev_out[1], **extra, **kw)
-        units = kvcache_bytes(decode) if is_kvcache(decode) else decode_bytes(decode)
-        unit, scale = "GB/s", 1e-9
-        note = "decode queries (and new K/V rows) copied each step; the paged cache stays resident"
+    host_in, compute, out_shapes, note = call.e2e_parts()
     barrier(world)
-    ms, host_out = run_streamed(host_in, compute, out_shapes, steps, stream, dev)
-    t_max, tot_units = reduce_max_sum(world, ms, units * steps, dev)
+    ms, host_out = run_streamed(host_in, lambda b, dev_in, dev_out: compute(dev_in, dev_out), out_shapes, steps,
+                                stream, dev)
+    t_max, tot_units = reduce_max_sum(world, ms, call.units * steps, dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    return {"value": tot_units / (t_max * 1e-3) * scale, "unit": unit, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "note": note + " (transfers overlap neighbouring steps)"}
+    return {"value": tot_units / (t_max * 1e-3) * call.unit_scale, "unit": call.unit, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "config": call.name,
+            "note": note + " (transfers overlap neighbouring steps)"}
 
 
-def cpu_baseline(prefill, decode, seconds):
+class BwdCall:
+    """attn_bwd on the backward of a prefill problem: q, k, v, the forward's
+    out and lse, and a seeded dO resident on the device."""
+    kind, kernel, unit, unit_scale, launches, bound = "backward", "attn_bwd", "TFLOP/s", 1e-12, 3, "tensor"
+
+    def __init__(self, la, p, dev):
+        self.la, self.p, self.name = la, p, p.name + "_backward"
+        pg = p.to(dev)
+        self.q = pg.q.view(p.B, p.Nq, p.Hq, p.d)
+        self.k, self.v = pg.k.view(p.B, p.Nk, p.Hkv, p.d), pg.v.view(p.B, p.Nk, p.Hkv, p.d)
+        self.out, self.lse = la.attn_fwd(self.q, self.k, self.v, causal=p.causal, scale=p.scale)
+        self.g = workloads.randn_bf16(tuple(p.q.shape), seed=p.seed + 900).to(dev).view(self.q.shape)
+        ws = torch.empty(la.lib().attn_bwd_workspace_size(p.B, p.Hq, p.Nq, 0), dtype=torch.uint8, device=dev)
+        self.kw = dict(causal=p.causal, scale=p.scale, dq=torch.empty_like(self.q), dk=torch.empty_like(self.k),
+                       dv=torch.empty_like(self.v), workspace=ws)
+        self.units = backward_flops(p)
+
+    def __call__(self):
+        self.la.attn_bwd(self.q, self.k, self.v, self.out, self.lse, self.g, **self.kw)
+
+    def describe(self):
+        p = self.p
+        return {"B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Nq": p.Nq, "Nk": p.Nk, "d": p.d, "causal": p.causal}
+
+    def roofline_extra(self):
+        return {"flops_per_call": self.units, "flops_executed_per_call": 14.0 * self.p.d * attended_pairs(self.p),
+                "launches_per_call": 3}
+
+
+def measure_next_rows(la, dev, stream, flush, steps, warmup, peaks, peaks_kind):
+    """Each next row (backward, local window, several queries with the
+    append) timed on its own with CUDA events, after the step's buffers are
+    freed; a row that fails reports its error instead of a number."""
+    rows = {}
+    for name in NEXT_ROWS:
+        call = None
+        try:
+            if name in BWD_WORKLOADS:
+                call = BwdCall(la, getattr(workloads, BWD_WORKLOADS[name])(), dev)
+            elif name in PREFILL_WORKLOADS:
+                call = PrefillCall(la, getattr(workloads, name)(), dev)
+            else:
+                call = DecodeCall(la, getattr(workloads, name)(device=dev), dev)
+            ms, wall, _ = time_calls([call], steps, warmup, stream, flush)
+            st = la.attn_get_device_status()
+            if st != 0:
+                raise RuntimeError(f"device status {la.attn_status_string(st)}")
+            rec = call_roofline(call, ms[0], peaks, peaks_kind)
+            rec.update(value=rec["achieved"], steps=steps, gpu_launches=steps * call.launches,
+                       config=call.describe())
+            rows[call.name] = rec
+        except Exception as e:   # a next row never blocks the step's line
+            rows[name] = {"error": f"{type(e).__name__}: {e}"}
+        finally:
+            call = None
+            torch.cuda.empty_cache()
+    return rows
+
+
+def _gather_prefill(p, out, lse, rows):
+    """GPU results at rows (b, h, i) of a prefill problem (host arrays)."""
+    o = out.reshape(-1, p.Hq, p.d)
+    if p.varlen:
+        tok = p.cu_q.cpu().numpy().astype(np.int64)[rows[:, 0]] + rows[:, 2]
+        li = rows[:, 1].astype(np.int64) * o.shape[0] + tok
+    else:
+        tok = rows[:, 0].astype(np.int64) * p.Nq + rows[:, 2]
+        li = (rows[:, 0].astype(np.int64) * p.Hq + rows[:, 1]) * p.Nq + rows[:, 2]
+    go = o[torch.as_tensor(tok).to(out.device), torch.as_tensor(rows[:, 1].astype(np.int64)).to(out.device)]
+    gl = lse.reshape(-1)[torch.as_tensor(li).to(lse.device)]
+    return go.float().cpu().numpy().astype(np.float64), gl.float().cpu().numpy().astype(np.float64)
+
+
+TOL = {"o_max_abs": 1e-2, "o_rel_rms": 5e-3, "lse_abs": 1e-3}
+
+
+def _compare(got_o, got_lse, ref_o, ref_lse):
+    err = np.abs(got_o - ref_o)
+    denom = float(np.sqrt((ref_o ** 2).sum()))
+    fin = np.isfinite(ref_lse)
+    rec = {"o_max_abs": float(err.max(initial=0.0)),
+           "o_rel_rms": float(np.sqrt((err ** 2).sum()) / denom) if denom > 0 else float(np.sqrt((err ** 2).sum())),
+           "lse_abs": float(np.abs(got_lse[fin] - ref_lse[fin]).max(initial=0.0)),
+           "finite": bool(np.isfinite(got_o).all() and (np.isfinite(got_lse) == fin).all())}
+    rec["within_tolerance"] = rec["finite"] and all(rec[k] <= v for k, v in TOL.items())
+    rec["tolerance"] = TOL
+    return rec
+
+
+def accuracy(call):
+    """The call's GPU output from the timed run against the fp64 oracle:
+    prefill on a seeded row sample per (sequence, head) that always holds the
+    first, last and tile-boundary rows; decode on every (sequence, head) row."""
+    import oracle
+    t0 = time.perf_counter()
     try:
-        if prefill is not None:
-            host = prefill.to("cpu")
-            rate, n, dt, threads, fl = oracle_sample_rate(host, seconds, seed=4242)
+        if call.kind == "prefill":
+            p = call.p
+            per = 16 if p.varlen else 64
+            rows = workloads.sample_rows(None, [nq for nq, _ in p.seq_lens()], p.Hq, per,
+                                         seed=p.seed + 700).numpy()
+            ref_o, ref_lse = oracle.prefill(p, rows)
+            got_o, got_lse = _gather_prefill(p, call.out, call.lse, rows)
+            what = f"{len(rows)} seeded rows ({per} per sequence and head)"
+        elif is_kvcache(call.d):
+            host = appended_host_copy(call.d)
+            rows = np.asarray([(b, h, i) for b in range(host.B) for h in range(host.Hq) for i in range(host.Nq)],
+                              dtype=np.int32)
+            ref_o, ref_lse = oracle.decode_multi_rows(host.q, host.k_cache, host.v_cache, host.block_table,
+                                                      host.seq_lens, scale=host.scale, causal=host.causal, rows=rows)
+            got_o = call.out.float().cpu().numpy()[rows[:, 0], rows[:, 2], rows[:, 1]].astype(np.float64)
+            got_lse = call.lse.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]].astype(np.float64)
+            what = f"all {len(rows)} (sequence, head, query) rows"
+        else:
+            host = call.d.to("cpu")
+            ref_o, ref_lse = oracle.decode(host)
+            got_o = call.out.float().cpu().numpy().reshape(-1, host.d).astype(np.float64)
+            got_lse = call.lse.cpu().numpy().reshape(-1).astype(np.float64)
+            what = f"all {len(ref_lse)} (sequence, head) rows"
+        rec = _compare(got_o, got_lse, ref_o, ref_lse)
+        rec["sample"] = what
+        rec["seconds"] = time.perf_counter() - t0
+        return rec
+    except Exception as e:   # the accuracy record never blocks the GPU line
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
+def cpu_baseline(call, seconds):
+    """The oracle as it stands, timed on the host cores on a bounded sample of
+    the headline configuration."""
+    try:
+        if call.kind == "prefill":
+            rate, n, dt, threads, fl = oracle_sample_rate(call.p, seconds, seed=4242)
             return {"value": rate * 1e-12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                    "sample": f"{n} seeded query rows of {prefill.name} ({fl / 1e9:.1f} GFLOP fp64) in {dt:.1f} s"}
-        if is_kvcache(decode):
-            host = appended_host_copy(decode)
+                    "sample": f"{n} seeded query rows of {call.name} ({fl / 1e9:.1f} GFLOP fp64) in {dt:.1f} s"}
+        if is_kvcache(call.d):
+            host = appended_host_copy(call.d)
             rate, n, dt, threads = oracle_kvcache_rate(host, seconds, seed=4242)
             return {"value": rate * 1e-9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                    "sample": f"{n} seeded (sequence, head, query) rows of {decode.name} in {dt:.1f} s"}
-        host = decode.to("cpu")
+                    "sample": f"{n} seeded (sequence, head, query) rows of {call.name} in {dt:.1f} s"}
+        host = call.d.to("cpu")
         rate, n, dt, threads = oracle_decode_rate(host, seconds, seed=4242)
         return {"value": rate * 1e-9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                "sample": f"{n} seeded (sequence, head) rows of {decode.name} in {dt:.1f} s"}
+                "sample": f"{n} seeded (sequence, head) rows of {call.name} in {dt:.1f} s"}
     except Exception as e:  # the baseline never blocks the GPU line
         return {"value": None, "unit": None, "cores": None, "kind": "oracle", "sample": f"failed: {e}"}
 
