@@ -27,6 +27,17 @@ Parity status of each function (what pins it, see ``tests/test_oracle.py``):
                   gathered keys.
   append_kv    -- pinned: brute-force gather of the written positions through
                   the block table; untouched slots keep their bytes.
+  e4m3_value, e4m3_from_float -- pinned: torch's float8_e4m3fn casts (a
+                  library routine) on every code and on every finite bf16
+                  value below the saturation point; saturation at 448.
+  quantize_fp8 -- pinned: every tile's largest magnitude lands on the code
+                  448; the round trip is within half a step of the E4M3 grid
+                  at each value's own scale; tiles start at sequence starts
+                  and at multiples of 128 tokens inside a sequence (an
+                  outlier moves the codes of its own tile only); all-zero
+                  tiles give zero codes.
+  prefill_rows_f64 -- pinned: bit-identical to prefill_rows on inputs
+                  that bf16 holds exactly (the same code path).
   backward     -- pinned: torch autograd through SDPA's fp64 MATH backend with
                   an explicit keep mask; central finite differences of
                   <G, O> on inputs whose perturbations are exact in bf16;
@@ -82,6 +93,16 @@ def _load():
             lib.oracle_backward.restype = I
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = I
+            lib.oracle_prefill_rows_f64.argtypes = [P, P, P, I, I, I, I, I, I, D, I, I, I, P, P, P, L, P, P, I]
+            lib.oracle_prefill_rows_f64.restype = I
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = D
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_quantize_fp8.argtypes = [P, I, I, I, I, P, P, P, L]
+            lib.oracle_quantize_fp8.restype = I
+            lib.oracle_dequantize_fp8.argtypes = [P, P, L, I, I, I, I, P, P]
+            lib.oracle_dequantize_fp8.restype = I
             _lib = lib
     return _lib
 
@@ -262,3 +283,112 @@ def backward(p, g, pairs=None, threads: int = 0, row_stride: int = 1):
         raise ValueError(f"oracle_backward rejected its arguments (status {rc})")
     return dq, dk, dv
 
+
+
+# ---------------------------------------------------------------------------
+# 8-bit (E4M3) per-tile quantization and attention on the values it stands for
+# ---------------------------------------------------------------------------
+def fp8_scale_count(B: int, T: int) -> int:
+    """Scale entries per head for T tokens in B sequences (tiles of 128 tokens
+    counted from each sequence's first token; tile t of sequence b is entry
+    T_b // 128 + b + t, T_b the sequence's first token)."""
+    return T // 128 + B
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def e4m3_from_float(x: float) -> int:
+    return int(_load().oracle_e4m3_from_float(float(x)))
+
+
+def _seq_args(T, B, N, cu):
+    if cu is None:
+        if N is None or B * N != T:
+            raise ValueError("dense layout needs B * N == T")
+        return int(N), None
+    c = _i32(cu)
+    if c.shape[0] != B + 1 or int(c[-1]) != T:
+        raise ValueError("cu must have B + 1 entries ending at T")
+    return 0, c
+
+
+def quantize_fp8(x, *, B, N=None, cu=None):
+    """Per-tile E4M3 quantization of x [T, H, d] bf16 (see oracle.c).
+    Returns (codes uint8 [T, H, d], scales float32 [H, fp8_scale_count(B, T)]);
+    scale entries between sequences are 0."""
+    T, H, d = (int(v) for v in x.shape)
+    n, c = _seq_args(T, B, N, cu)
+    xb = _bits(x)
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    ns = fp8_scale_count(B, T)
+    scales = np.zeros((H, ns), dtype=np.float32)
+    rc = _load().oracle_quantize_fp8(_ptr(xb), B, H, n, d, _ptr(c), _ptr(codes), _ptr(scales), ns)
+    if rc != 0:
+        raise ValueError(f"oracle_quantize_fp8 rejected its arguments (status {rc})")
+    return codes, scales
+
+
+def dequantize_fp8(codes, scales, *, B, N=None, cu=None):
+    """The fp64 values E4M3 codes [T, H, d] with their per-tile scales stand for."""
+    codes = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    scales = np.ascontiguousarray(np.asarray(scales, dtype=np.float32))
+    T, H, d = codes.shape
+    n, c = _seq_args(T, B, N, cu)
+    out = np.zeros((T, H, d), dtype=np.float64)
+    rc = _load().oracle_dequantize_fp8(_ptr(codes), _ptr(scales), int(scales.shape[1]), B, H, n, d, _ptr(c),
+                                       _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_dequantize_fp8 rejected its arguments (status {rc})")
+    return out
+
+
+def prefill_rows_f64(q, k, v, *, B, Hq, Hkv, Nq, Nk, scale, causal, rows, cu_q=None, cu_k=None,
+                     window=(-1, -1), threads: int = 0):
+    """prefill_rows on fp64 inputs q [T_q, Hq, d], k/v [T_k, Hkv, d]."""
+    f = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    qd, kd, vd = f(q), f(k), f(v)
+    d = int(qd.shape[-1])
+    r = _i32(rows).reshape(-1, 3)
+    n = r.shape[0]
+    out = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    cq, ck = _i32(cu_q), _i32(cu_k)
+    left, right = (int(x) for x in window)
+    rc = _load().oracle_prefill_rows_f64(_ptr(qd), _ptr(kd), _ptr(vd), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                                         int(bool(causal)), left, right, _ptr(cq), _ptr(ck), _ptr(r), n,
+                                         _ptr(out), _ptr(lse), threads if threads > 0 else num_threads())
+    if rc != 0:
+        raise ValueError(f"oracle_prefill_rows_f64 rejected its arguments (status {rc})")
+    return out, lse
+
+
+def quantize_problem_fp8(p):
+    """Per-tile E4M3 codes and scales of a workloads.Prefill problem's q, k, v:
+    {"q": (codes, scales), "k": ..., "v": ...}."""
+    tq = sum(nq for nq, _ in p.seq_lens())
+    tk = sum(nk for _, nk in p.seq_lens())
+    if p.varlen:
+        return {"q": quantize_fp8(p.q, B=p.B, cu=p.cu_q), "k": quantize_fp8(p.k, B=p.B, cu=p.cu_k),
+                "v": quantize_fp8(p.v, B=p.B, cu=p.cu_k)}
+    return {"q": quantize_fp8(p.q, B=p.B, N=p.Nq), "k": quantize_fp8(p.k, B=p.B, N=p.Nk),
+            "v": quantize_fp8(p.v, B=p.B, N=p.Nk)}
+
+
+def prefill_fp8(p, rows=None, quantized=None, threads: int = 0):
+    """Attention of a workloads.Prefill problem on the values its per-tile
+    E4M3 quantization stands for: rows (b, h, i) of softmax(QK^T*scale +
+    mask) V over the dequantized q, k, v, fp64.  Returns (out, lse)."""
+    if quantized is None:
+        quantized = quantize_problem_fp8(p)
+    if rows is None:
+        rows = all_rows(p)
+    seq = dict(B=p.B, cu=p.cu_q) if p.varlen else dict(B=p.B, N=p.Nq)
+    seqk = dict(B=p.B, cu=p.cu_k) if p.varlen else dict(B=p.B, N=p.Nk)
+    q = dequantize_fp8(*quantized["q"], **seq)
+    k = dequantize_fp8(*quantized["k"], **seqk)
+    v = dequantize_fp8(*quantized["v"], **seqk)
+    return prefill_rows_f64(q, k, v, B=p.B, Hq=p.Hq, Hkv=p.Hkv, Nq=p.Nq, Nk=p.Nk, scale=p.scale, causal=p.causal,
+                            rows=rows, cu_q=p.cu_q, cu_k=p.cu_k, window=getattr(p, "window", (-1, -1)),
+                            threads=threads)

@@ -60,7 +60,13 @@
  *   dQ_i  = scale * sum_j dS_ij k_j      dK_j += scale * dS_ij q_i
  * with the K/V gradients of a grouped head summed over its query heads.
  *
- * Inputs are bf16 bit patterns (uint16); each is widened exactly to double.
+ * 8-bit inputs (oracle_quantize_fp8 / oracle_dequantize_fp8, at the end of
+ * this file): per-tile E4M3 codes and fp32 scales, and the values they stand
+ * for; attention on those values is the same definition on fp64 inputs
+ * (oracle_prefill_rows_f64).
+ *
+ * Inputs are bf16 bit patterns (uint16), each widened exactly to double, or
+ * doubles.
  * Threads: POSIX threads over output rows; each row is computed by one thread
  * in the order written above, so results do not depend on the thread count.
  */
@@ -96,9 +102,16 @@ static int key_allowed(long i, long j, long nq, long nk, int causal, long left, 
     return 1;
 }
 
+/* ---- one element of an input tensor: bf16 bits, or (f64 = 1) a double ---- */
+static double elem(const void *base, int f64, long idx)
+{
+    return f64 ? ((const double *)base)[idx] : bf16_value(((const uint16_t *)base)[idx]);
+}
+
 /* ---- where the key/value rows of one sequence live ---- */
 typedef struct {
-    const uint16_t *k, *v;    /* K and V base pointers */
+    const void *k, *v;        /* K and V base pointers */
+    int f64;                  /* element type of q, k, v: 0 bf16 bits, 1 double */
     long first_token;         /* contiguous: token row of key 0 */
     const int32_t *pages;     /* paged: this sequence's block-table row, else NULL */
     int page_size;
@@ -114,13 +127,14 @@ static long token_of_key(const key_store *ks, long j)
     return ks->first_token + j;
 }
 
-static const uint16_t *key_row(const key_store *ks, const uint16_t *base, long j, int g)
+/* element index of channel 0 of key j, K/V head g */
+static long key_row(const key_store *ks, long j, int g)
 {
-    return base + (token_of_key(ks, j) * ks->hkv + g) * (long)ks->d;
+    return (token_of_key(ks, j) * ks->hkv + g) * (long)ks->d;
 }
 
 /* ---- one output row, by the definition ---- */
-static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
+static void attend_row(const void *q, long q_row, const key_store *ks, int g,
                        long i, long nq, long nk, int causal, long left, long right, double scale,
                        double *s, double *out, double *lse)
 {
@@ -132,10 +146,10 @@ static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
     for (long j = 0; j < nk; ++j) {
         if (!key_allowed(i, j, nq, nk, causal, left, right))
             continue;
-        const uint16_t *k_row = key_row(ks, ks->k, j, g);
+        const long k_row = key_row(ks, j, g);
         double dot = 0.0;
         for (int c = 0; c < d; ++c)
-            dot += bf16_value(q_row[c]) * bf16_value(k_row[c]);
+            dot += elem(q, ks->f64, q_row + c) * elem(ks->k, ks->f64, k_row + c);
         s[j] = scale * dot;
         if (n_allowed == 0 || s[j] > m)
             m = s[j];
@@ -156,9 +170,9 @@ static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
             continue;
         double w = exp(s[j] - m);
         l += w;
-        const uint16_t *v_row = key_row(ks, ks->v, j, g);
+        const long v_row = key_row(ks, j, g);
         for (int c = 0; c < d; ++c)
-            out[c] += w * bf16_value(v_row[c]);
+            out[c] += w * elem(ks->v, ks->f64, v_row + c);
     }
     for (int c = 0; c < d; ++c)
         out[c] /= l;
@@ -168,7 +182,8 @@ static void attend_row(const uint16_t *q_row, const key_store *ks, int g,
 /* ---- row jobs ---- */
 typedef struct {
     /* shared inputs */
-    const uint16_t *q, *k, *v;
+    const void *q, *k, *v;
+    int f64;   /* element type of q, k, v: 0 bf16 bits, 1 double */
     int B, Hq, Hkv, Nq, Nk, d, causal, paged, page_size, max_pages;
     long win_left, win_right;
     double scale;
@@ -191,6 +206,7 @@ static void run_row(job *jb, long r, double *s)
     memset(&ks, 0, sizeof ks);
     ks.k = jb->k;
     ks.v = jb->v;
+    ks.f64 = jb->f64;
     ks.hkv = jb->Hkv;
     ks.d = jb->d;
 
@@ -208,18 +224,18 @@ static void run_row(job *jb, long r, double *s)
             ks.first_token = (long)b * jb->Nk;
             nk = jb->Nk;
         }
-        const uint16_t *q_row = jb->q + ((q_first + i) * jb->Hq + h) * (long)jb->d;
-        attend_row(q_row, &ks, h / group, i, nq, nk, jb->causal, jb->win_left, jb->win_right, jb->scale, s, out,
-                   lse);
+        const long q_row = ((q_first + i) * jb->Hq + h) * (long)jb->d;
+        attend_row(jb->q, q_row, &ks, h / group, i, nq, nk, jb->causal, jb->win_left, jb->win_right, jb->scale, s,
+                   out, lse);
     } else if (jb->paged == 1) {
         int b = jb->rows[2 * r], h = jb->rows[2 * r + 1];
         long len = jb->seq_lens[b];
         ks.pages = jb->block_table + (long)b * jb->max_pages;
         ks.page_size = jb->page_size;
-        const uint16_t *q_row = jb->q + ((long)b * jb->Hq + h) * (long)jb->d;
+        const long q_row = ((long)b * jb->Hq + h) * (long)jb->d;
         /* one query per sequence: it is the last position, so under the
          * bottom-right rule it sees every cached key (i = 0, nq = 1). */
-        attend_row(q_row, &ks, h / group, 0, 1, len, 0, -1, -1, jb->scale, s, out, lse);
+        attend_row(jb->q, q_row, &ks, h / group, 0, 1, len, 0, -1, -1, jb->scale, s, out, lse);
     } else {
         /* Nq queries per sequence over the paged cache: query i is position
          * len - Nq + i, so under the bottom-right rule (with causal) it sees
@@ -228,8 +244,8 @@ static void run_row(job *jb, long r, double *s)
         long len = jb->seq_lens[b];
         ks.pages = jb->block_table + (long)b * jb->max_pages;
         ks.page_size = jb->page_size;
-        const uint16_t *q_row = jb->q + (((long)b * jb->Nq + i) * jb->Hq + h) * (long)jb->d;
-        attend_row(q_row, &ks, h / group, i, jb->Nq, len, jb->causal, -1, -1, jb->scale, s, out, lse);
+        const long q_row = (((long)b * jb->Nq + i) * jb->Hq + h) * (long)jb->d;
+        attend_row(jb->q, q_row, &ks, h / group, i, jb->Nq, len, jb->causal, -1, -1, jb->scale, s, out, lse);
     }
 }
 
@@ -319,6 +335,13 @@ int oracle_prefill_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                       rows, n_rows, out, lse, n_threads);
 }
 
+static int prefill_rows(const void *q, const void *k, const void *v, int f64,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        double scale, int causal, int win_left, int win_right,
+                        const int32_t *cu_q, const int32_t *cu_k,
+                        const int32_t *rows, long n_rows,
+                        double *out, double *lse, int n_threads);
+
 /* As oracle_prefill_rows, with a local window (win_left, win_right); -1 on a
  * side leaves it unbounded. */
 int oracle_prefill_rows_window(const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -327,6 +350,31 @@ int oracle_prefill_rows_window(const uint16_t *q, const uint16_t *k, const uint1
                                const int32_t *cu_q, const int32_t *cu_k,
                                const int32_t *rows, long n_rows,
                                double *out, double *lse, int n_threads)
+{
+    return prefill_rows(q, k, v, 0, B, Hq, Hkv, Nq, Nk, d, scale, causal, win_left, win_right, cu_q, cu_k,
+                        rows, n_rows, out, lse, n_threads);
+}
+
+/* As oracle_prefill_rows_window on inputs given as doubles (used for the
+ * values an 8-bit encoding and its per-tile scales stand for, which bf16
+ * cannot hold). */
+int oracle_prefill_rows_f64(const double *q, const double *k, const double *v,
+                            int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                            double scale, int causal, int win_left, int win_right,
+                            const int32_t *cu_q, const int32_t *cu_k,
+                            const int32_t *rows, long n_rows,
+                            double *out, double *lse, int n_threads)
+{
+    return prefill_rows(q, k, v, 1, B, Hq, Hkv, Nq, Nk, d, scale, causal, win_left, win_right, cu_q, cu_k,
+                        rows, n_rows, out, lse, n_threads);
+}
+
+static int prefill_rows(const void *q, const void *k, const void *v, int f64,
+                        int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                        double scale, int causal, int win_left, int win_right,
+                        const int32_t *cu_q, const int32_t *cu_k,
+                        const int32_t *rows, long n_rows,
+                        double *out, double *lse, int n_threads)
 {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || n_rows < 0)
         return -1;
@@ -346,7 +394,7 @@ int oracle_prefill_rows_window(const uint16_t *q, const uint16_t *k, const uint1
     }
     job jb;
     memset(&jb, 0, sizeof jb);
-    jb.q = q; jb.k = k; jb.v = v;
+    jb.q = q; jb.k = k; jb.v = v; jb.f64 = f64;
     jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.Nq = Nq; jb.Nk = Nk; jb.d = d;
     jb.causal = causal; jb.scale = scale;
     jb.win_left = win_left < 0 ? -1 : win_left;
@@ -609,3 +657,139 @@ int oracle_backward(const uint16_t *q, const uint16_t *k, const uint16_t *v, con
     return jb.status;
 }
 
+
+/* ---- 8-bit floating point, E4M3 ----
+ *
+ * "FP8 Path and Quantization" ("Flash Attention: A Complete Architectural
+ * Autopsy", part 4) and "FlashAttention-3: asynchrony and low precision on
+ * Hopper" ("FlashAttention-3 and PagedAttention") name the E4M3 format and
+ * per-tile (block) quantization: a tile is scaled by a factor taken from its
+ * absolute maximum before it is cast to 8 bits, and the scores are turned
+ * back into fp32 before the softmax.
+ *
+ * E4M3 as this file reads it: 1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 holds the subnormals m * 2^-9; no
+ * infinities; the one pattern S.1111.111 is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_value(uint8_t code)
+{
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    /* (1 + m/8) * 2^(e-7) = (8 + m) * 2^(e-10) for e >= 1 */
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return sign ? -mag : mag;
+}
+
+/* x rounded to the nearest E4M3 value, ties to the even mantissa; magnitudes
+ * from 448 up give 448 (saturation), NaN gives NaN. */
+uint8_t oracle_e4m3_from_float(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x))
+        return (uint8_t)(sign | 0x7f);
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7e);
+    if (a == 0.0)
+        return sign;
+    /* spacing of the representable values around a: 2^(floor(log2 a) - 3) in
+     * the normal range, 2^-9 among the subnormals (below 2^-6) */
+    int e2;
+    frexp(a, &e2);
+    int ue = e2 - 1;   /* floor(log2 a) */
+    if (ue < -6)
+        ue = -6;
+    const double ulp = ldexp(1.0, ue - 3);
+    const double v = rint(a / ulp) * ulp;   /* a / ulp is exact; rint ties to even */
+    if (v < ldexp(1.0, -6))                 /* subnormal: the code is v / 2^-9 */
+        return (uint8_t)(sign | (int)(v / ldexp(1.0, -9)));
+    frexp(v, &e2);
+    const int ve = e2 - 1;                  /* rounding may have reached the next binade */
+    const int m = (int)((v / ldexp(1.0, ve) - 1.0) * 8.0);
+    return (uint8_t)(sign | ((ve + 7) << 3) | m);
+}
+
+/*
+ * Per-tile quantization of x [T, H, d] (bf16 bits) to E4M3 codes.
+ *
+ * A tile is 128 consecutive tokens of one sequence, counted from the
+ * sequence's first token (the last tile of a sequence may be shorter), for
+ * one head and all d channels.  Sequence b owns tokens [b*N, (b+1)*N) when cu
+ * is NULL (dense), else [cu[b], cu[b+1]).  For each tile, in fp32:
+ *   amax  = max |x| over the tile (exact: bf16 values are fp32 values)
+ *   scale = amax / 448,  inv = 448 / amax          (each rounded to fp32)
+ *   code  = E4M3(x * inv)  (the product rounded to fp32, then to E4M3)
+ * so the tile's largest magnitude lands on 448 and x is represented as
+ * E4M3(code) * scale.  A tile whose amax is below 2^-100 (all zero, or so
+ * small that 448 / amax would overflow) gets scale 1 and all-zero codes.
+ * scales [H, n_scale]: tile t of sequence b is entry floor(s_b / 128) + b + t,
+ * s_b the sequence's first token; n_scale = T / 128 + B covers every
+ * sequence (entries between sequences are left untouched).
+ * Returns 0, or -1 for invalid arguments.
+ */
+int oracle_quantize_fp8(const uint16_t *x, int B, int H, int N, int d, const int32_t *cu,
+                        uint8_t *codes, float *scales, long n_scale)
+{
+    if (B < 0 || H <= 0 || d <= 0 || (!cu && N < 0))
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        const long first = cu ? cu[b] : (long)b * N;
+        const long len = cu ? (long)cu[b + 1] - cu[b] : N;
+        if (first < 0 || len < 0)
+            return -1;
+        for (long t = 0; t * 128 < len; ++t) {
+            const long idx = first / 128 + b + t;
+            if (idx >= n_scale)
+                return -1;
+            const long r0 = first + 128 * t;
+            const long rows = len - 128 * t < 128 ? len - 128 * t : 128;
+            for (int h = 0; h < H; ++h) {
+                float amax = 0.0f;
+                for (long r = r0; r < r0 + rows; ++r)
+                    for (int c = 0; c < d; ++c) {
+                        const float a = (float)fabs(bf16_value(x[(r * H + h) * (long)d + c]));
+                        if (a > amax)
+                            amax = a;
+                    }
+                const int zero = !(amax >= 0x1p-100f);
+                const float scale = zero ? 1.0f : amax / 448.0f;
+                const float inv = zero ? 0.0f : 448.0f / amax;
+                for (long r = r0; r < r0 + rows; ++r)
+                    for (int c = 0; c < d; ++c) {
+                        const long at = (r * H + h) * (long)d + c;
+                        const float y = (float)bf16_value(x[at]) * inv;
+                        codes[at] = zero ? 0 : oracle_e4m3_from_float(y);
+                    }
+                scales[(long)h * n_scale + idx] = scale;
+            }
+        }
+    }
+    return 0;
+}
+
+/* The values quantized tiles stand for: out = E4M3(code) * scale of the
+ * code's tile, in fp64 (exact), with the tiles and the scale layout of
+ * oracle_quantize_fp8. */
+int oracle_dequantize_fp8(const uint8_t *codes, const float *scales, long n_scale, int B, int H, int N, int d,
+                          const int32_t *cu, double *out)
+{
+    if (B < 0 || H <= 0 || d <= 0 || (!cu && N < 0))
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        const long first = cu ? cu[b] : (long)b * N;
+        const long len = cu ? (long)cu[b + 1] - cu[b] : N;
+        for (long r = first; r < first + len; ++r) {
+            const long idx = first / 128 + b + (r - first) / 128;
+            if (idx >= n_scale)
+                return -1;
+            for (int h = 0; h < H; ++h)
+                for (int c = 0; c < d; ++c) {
+                    const long at = (r * H + h) * (long)d + c;
+                    out[at] = oracle_e4m3_value(codes[at]) * (double)scales[(long)h * n_scale + idx];
+                }
+        }
+    }
+    return 0;
+}

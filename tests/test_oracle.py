@@ -746,3 +746,125 @@ def test_backward_varlen_equals_per_sequence_dense():
         assert np.array_equal(sq, dq[cq[b]:cq[b + 1]])
         assert np.array_equal(sk, dk[ck[b]:ck[b + 1]]) and np.array_equal(sv, dv[ck[b]:ck[b + 1]])
 
+
+
+# ---------------------------------------------------------------------------
+# 8-bit (E4M3) per-tile quantization ("FP8 Path and Quantization"; "FlashAttention-3:
+# asynchrony and low precision on Hopper")
+# ---------------------------------------------------------------------------
+def test_e4m3_decoding_matches_torch_on_every_code():
+    """torch's float8_e4m3fn (a library routine) decodes all 256 codes."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).tolist()
+    for c in range(256):
+        got = oracle.e4m3_value(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(got), c
+        else:
+            assert got == ref[c] and math.copysign(1, got) == math.copysign(1, ref[c]), c
+    assert oracle.e4m3_value(0x7E) == 448.0 and math.isnan(oracle.e4m3_value(0x7F))
+
+
+def test_e4m3_rounding_matches_torch_on_every_bf16_value():
+    """Round to nearest, ties to even, on every finite bf16 value up to 464
+    (torch's cast turns larger ones into NaN; this encoding saturates them to
+    448 instead)."""
+    bits = torch.arange(-32768, 32768, dtype=torch.int32).to(torch.int16)
+    x = bits.view(torch.bfloat16).to(torch.float32)
+    keep = torch.isfinite(x) & (x.abs() <= 464)
+    xs = x[keep]
+    ref = xs.to(torch.float8_e4m3fn).view(torch.uint8).tolist()
+    got = [oracle.e4m3_from_float(v) for v in xs.tolist()]
+    assert got == ref
+    for v in (465.0, 480.0, 1e6, float("inf")):
+        assert oracle.e4m3_from_float(v) == 0x7E and oracle.e4m3_from_float(-v) == 0xFE
+
+
+def test_quantize_tile_maximum_lands_on_448_and_round_trip_within_half_step():
+    """Each tile's largest magnitude becomes the code for +-448, and every
+    value comes back within half a step of the E4M3 grid at its own scale:
+    |x - x~| <= 2^-4 |x| in the normal range, <= 2^-10 * scale below it."""
+    lens = [300, 1, 128, 129, 0, 77]
+    p = workloads.make_varlen(lens, lens, 3, 2, 64, causal=True, seed=21)
+    spread = torch.logspace(-3, 2, p.q.shape[0])[:, None, None]
+    x = (p.q.float() * spread).to(torch.bfloat16)
+    codes, scales = oracle.quantize_fp8(x, B=p.B, cu=p.cu_q)
+    deq = oracle.dequantize_fp8(codes, scales, B=p.B, cu=p.cu_q)
+    xd = x.double().numpy()
+    cq = p.cu_q.tolist()
+    for b, L in enumerate(lens):
+        for t in range(0, L, 128):
+            r0, r1 = cq[b] + t, cq[b] + min(L, t + 128)
+            tile_codes = codes[r0:r1]
+            for h in range(x.shape[1]):
+                mags = np.abs([oracle.e4m3_value(c) for c in tile_codes[:, h].reshape(-1)])
+                assert mags.max() == 448.0
+                sc = float(scales[h, cq[b] // 128 + b + t // 128])
+                err = np.abs(xd[r0:r1, h] - deq[r0:r1, h])
+                bound = np.maximum(2.0 ** -4 * np.abs(xd[r0:r1, h]), 2.0 ** -10 * sc) * (1 + 1e-6)
+                assert (err <= bound).all()
+
+
+def test_quantize_tiles_start_at_each_sequence_start():
+    """An outlier changes the codes of its own tile (128 tokens counted from
+    its sequence's first token, one head) and of no other."""
+    lens = [200, 70, 260]
+    p = workloads.make_varlen(lens, lens, 2, 2, 64, causal=False, seed=22)
+    base_codes, base_scales = oracle.quantize_fp8(p.q, B=p.B, cu=p.cu_q)
+    cq = p.cu_q.tolist()
+    for b, tok in ((0, 130), (1, 3), (2, 255)):
+        x = p.q.clone()
+        x[cq[b] + tok, 1, 5] = 64.0 * x.float().abs().max()
+        codes, scales = oracle.quantize_fp8(x, B=p.B, cu=p.cu_q)
+        t = tok // 128
+        r0, r1 = cq[b] + 128 * t, cq[b] + min(lens[b], 128 * (t + 1))
+        changed = np.argwhere((codes != base_codes).any(axis=2))
+        assert len(changed) > 0
+        assert ((changed[:, 0] >= r0) & (changed[:, 0] < r1) & (changed[:, 1] == 1)).all()
+        diff = np.argwhere(scales != base_scales)
+        assert diff.tolist() == [[1, cq[b] // 128 + b + t]]
+
+
+def test_quantize_zero_tile_and_dense_layout():
+    x = bf16(torch.randn(2 * 256, 2, 64, generator=torch.Generator().manual_seed(23)))
+    x[256 + 128:] = 0.0          # sequence 1, tile 1: all zero
+    codes, scales = oracle.quantize_fp8(x, B=2, N=256)
+    assert (codes[256 + 128:] == 0).all()
+    assert scales.shape == (2, 512 // 128 + 2)
+    # sequence 1 starts at token 256: its tiles are entries 2 + 1 and 2 + 1 + 1; entry 2 is a gap
+    assert (scales[:, 4] == 1.0).all() and (scales[:, 2] == 0).all()
+    assert (scales[:, [0, 1, 3]] > 0).all()
+
+
+def test_f64_attention_equals_bf16_attention_on_bf16_values():
+    p = workloads.make_varlen([33, 130, 0, 7], [40, 200, 5, 7], 4, 2, 64, causal=True, seed=24)
+    rows = oracle.all_rows(p)
+    o1, l1 = oracle.prefill(p, rows)
+    o2, l2 = oracle.prefill_rows_f64(p.q.double().numpy(), p.k.double().numpy(), p.v.double().numpy(), B=p.B,
+                                     Hq=p.Hq, Hkv=p.Hkv, Nq=p.Nq, Nk=p.Nk, scale=p.scale, causal=True, rows=rows,
+                                     cu_q=p.cu_q, cu_k=p.cu_k)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_fp8_attention_on_exactly_quantizable_inputs_equals_attention():
+    """Inputs that are E4M3 values times a power of two, with a +-448 * 2^k
+    element in every tile, quantize exactly (scale 2^k): attention on the
+    values they stand for is attention on the inputs themselves."""
+    g = torch.Generator().manual_seed(25)
+    p = workloads.make_prefill(2, 4, 2, 300, 300, 64, causal=True, seed=26)
+
+    def exact(t, k):
+        c = torch.randint(0, 256, t.shape, generator=g, dtype=torch.int32)
+        c[(c & 0x7F) == 0x7F] = 0          # no NaN codes
+        v = c.to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float32) * 2.0 ** k
+        rows = t.shape[0]
+        for r0 in range(0, rows, 300):       # one +-448 * 2^k element in every tile of every head
+            for tt in range(r0, min(rows, r0 + 300), 128):
+                v[tt, :, 0] = 448.0 * 2.0 ** k
+        return v.to(torch.bfloat16)
+    q, k, v = exact(p.q, -8), exact(p.k, -7), exact(p.v, -2)
+    p = workloads.Prefill(p.name, q, k, v, p.B, p.Hq, p.Hkv, p.Nq, p.Nk, p.d, p.scale, p.causal, seed=p.seed)
+    rows = oracle.all_rows(p)
+    o1, l1 = oracle.prefill(p, rows)
+    o2, l2 = oracle.prefill_fp8(p, rows)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)

@@ -30,14 +30,19 @@ MUTATIONS = {
     "window measured from the top-left": ("j < i + nk - nq - left)", "j < i - left)"),
     "multi-query decode reads query 0 for every row": ("(((long)b * jb->Nq + i) * jb->Hq + h)",
                                                         "(((long)b * jb->Nq) * jb->Hq + h)"),
-    "multi-query decode ignores causal": ("attend_row(q_row, &ks, h / group, i, jb->Nq, len, jb->causal,",
-                                          "attend_row(q_row, &ks, h / group, i, jb->Nq, len, 0,"),
+    "multi-query decode ignores causal": ("attend_row(jb->q, q_row, &ks, h / group, i, jb->Nq, len, jb->causal,",
+                                          "attend_row(jb->q, q_row, &ks, h / group, i, jb->Nq, len, 0,"),
     "backward drops the row term D": ("const double ds = p[j] * (dp[j] - D);", "const double ds = p[j] * dp[j];"),
     "backward dK without the scale": ("dk_row[c] += jb->scale * ds * bf16_value(q_row[c]);",
                                       "dk_row[c] += ds * bf16_value(q_row[c]);"),
     "backward dV from dP": ("dv_row[c] += p[j] * bf16_value(g_row[c]);", "dv_row[c] += dp[j] * bf16_value(g_row[c]);"),
     "backward dQ from values": ("dq_row[c] += jb->scale * ds * bf16_value(k_row[c]);",
                                 "dq_row[c] += jb->scale * ds * bf16_value(jb->v[((k_first + j) * jb->Hkv + g) * (long)d + c]);"),
+    "E4M3 rounding truncates": ("const double v = rint(a / ulp) * ulp;", "const double v = floor(a / ulp) * ulp;"),
+    "E4M3 subnormal spacing": ("if (ue < -6)\n        ue = -6;", "if (ue < -7)\n        ue = -7;"),
+    "E4M3 exponent bias off by one": ("ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 11)"),
+    "fp8 scale for another largest code": ("amax / 448.0f", "amax / 240.0f"),
+    "fp8 tiles ignore the sequence start": ("const long idx = first / 128 + b + t;", "const long idx = b + t;"),
     # the in-place append lives in the Python half of the oracle
     "append position off by one": ("pos = lens[b] - Nq + i\n", "pos = lens[b] - Nq + i + 1\n", "__init__.py"),
     "append reads seq_lens as the length before the append": ("pos = lens[b] - Nq + i\n", "pos = lens[b] + i\n",
