@@ -392,7 +392,9 @@ def oracle_decode_rate(d, target_s: float, seed: int):
 HOT_PREFILL = ("gqa_causal", "mha_causal", "varlen_chunked")
 DECODE_WORKLOADS = ("paged_decode", "paged_decode_small", "spec_decode")
 # Measured after the step on their own (backward, window, several queries with append).
-NEXT_ROWS = ("mha_causal_bwd", "gqa_causal_bwd", "swa_causal", "spec_decode")
+NEXT_ROWS = ("mha_causal_bwd", "gqa_causal_bwd", "swa_causal", "spec_decode", "gqa_causal_fp8", "mha_causal_fp8",
+             "gqa_causal_quantize_fp8")
+FP8_WORKLOADS = {"gqa_causal_fp8": "gqa_causal", "mha_causal_fp8": "mha_causal", "varlen_chunked_fp8": "varlen_chunked"}
 
 
 def make_workloads(name, device):
@@ -532,12 +534,14 @@ def call_roofline(call, ms, peaks, peaks_kind):
     """Roofline record of one call from its per-step CUDA-event times."""
     mean = sum(ms) / len(ms)
     ach = call.units / (mean * 1e-3) * call.unit_scale
-    peak = peaks["bf16_tflops"] if call.bound == "tensor" else peaks["hbm_gbs"]
-    nominal = NOMINAL["bf16_tflops"] if call.bound == "tensor" else NOMINAL["hbm_gbs"]
+    peak_scale = getattr(call, "peak_scale", 1.0)
+    peak = (peaks["bf16_tflops"] if call.bound == "tensor" else peaks["hbm_gbs"]) * peak_scale
+    nominal = (NOMINAL["bf16_tflops"] if call.bound == "tensor" else NOMINAL["hbm_gbs"]) * peak_scale
     rec = {"kernel": call.kernel, "bound": call.bound, "achieved": ach, "peak": peak, "unit": call.unit,
            "frac": ach / peak, "frac_nominal": nominal and ach / nominal,
            "traffic": measured_traffic(call.kernel, call.name),
-           "peak_source": f"{peaks_kind} " + ("bf16 burst" if call.bound == "tensor" else "copy bandwidth"),
+           "peak_source": getattr(call, "peak_note", None) or
+                          (f"{peaks_kind} " + ("bf16 burst" if call.bound == "tensor" else "copy bandwidth")),
            "ms_mean": mean, "ms_median": statistics.median(ms), "ms_p95": sorted(ms)[int(0.95 * (len(ms) - 1))]}
     rec.update(call.roofline_extra())
     return rec
@@ -913,6 +917,67 @@ class BwdCall:
                 "launches_per_call": 3}
 
 
+class Fp8Call(PrefillCall):
+    """attn_fwd_fp8 on the per-tile E4M3 quantization of a prefill problem
+    (quantized on the device by attn_quantize_fp8 before timing).  Work is
+    the same 4 d FLOP per attended pair; the S product runs at the 8-bit rate
+    and the PV product at the 16-bit rate, so the peak for this kernel is
+    4/3 of the bf16 peak (half the FLOPs at twice the rate)."""
+    kernel, peak_scale = "attn_fwd_fp8", 4.0 / 3.0
+
+    def __init__(self, la, p, dev, peaks_kind="measured"):
+        super().__init__(la, p, dev)
+        self.name = p.name + "_fp8"
+        q, k, v = self.args
+        kw = dict(cu_seqlens=self.kw["cu_seqlens_q"]) if p.varlen else {}
+        kwk = dict(cu_seqlens=self.kw["cu_seqlens_k"]) if p.varlen else {}
+        self.q8, self.qs = la.attn_quantize_fp8(q, **kw)
+        self.k8, self.ks = la.attn_quantize_fp8(k, **kwk)
+        self.v8, self.vs = la.attn_quantize_fp8(v, **kwk)
+        self.fkw = {x: y for x, y in self.kw.items() if x != "window"}
+        self.peak_note = (f"{peaks_kind} bf16 burst x 4/3 (S at the 8-bit rate, nominally 2x bf16; "
+                          "PV at the 16-bit rate)")
+
+    def __call__(self):
+        self.la.attn_fwd_fp8(self.q8, self.k8, self.v8, self.qs, self.ks, self.vs, out=self.out, lse=self.lse,
+                             **self.fkw)
+
+
+class QuantizeCall:
+    """attn_quantize_fp8 on q, k and v of a prefill problem (three launches):
+    every bf16 element read once, every code written once, plus the scales."""
+    kind, kernel, unit, unit_scale, launches, bound = "quantize", "attn_quantize_fp8", "GB/s", 1e-9, 3, "hbm"
+
+    def __init__(self, la, p, dev):
+        self.la, self.p, self.name = la, p, p.name + "_quantize_fp8"
+        g = p.to(dev)
+        self.xs = [g.q, g.k, g.v]
+        self.cu = [g.cu_q, g.cu_k, g.cu_k]
+        self.outs = []
+        for x, cu in zip(self.xs, self.cu):
+            T, H, d = x.shape
+            B = p.B
+            self.outs.append((torch.empty_like(x, dtype=torch.uint8),
+                              torch.zeros((H, la.attn_fp8_scale_count(B, T)), dtype=torch.float32, device=dev)))
+        self.units = float(sum(3 * x.numel() + 4 * o[1].numel() for x, o in zip(self.xs, self.outs)))
+
+    def __call__(self):
+        p = self.p
+        for x, cu, (o8, osc) in zip(self.xs, self.cu, self.outs):
+            if p.varlen:
+                self.la.attn_quantize_fp8(x, cu_seqlens=cu, out=o8, scale=osc)
+            else:
+                T, H, d = x.shape
+                self.la.attn_quantize_fp8(x.view(p.B, T // p.B, H, d), out=o8.view(p.B, T // p.B, H, d), scale=osc)
+
+    def describe(self):
+        return {"B": self.p.B, "tokens_q": int(self.xs[0].shape[0]), "tokens_k": int(self.xs[1].shape[0]),
+                "Hq": self.p.Hq, "Hkv": self.p.Hkv, "d": self.p.d}
+
+    def roofline_extra(self):
+        return {"bytes_per_call": self.units, "launches_per_call": 3}
+
+
 def measure_next_rows(la, dev, stream, flush, steps, warmup, peaks, peaks_kind):
     """Each next row (backward, local window, several queries with the
     append) timed on its own with CUDA events, after the step's buffers are
@@ -923,6 +988,10 @@ def measure_next_rows(la, dev, stream, flush, steps, warmup, peaks, peaks_kind):
         try:
             if name in BWD_WORKLOADS:
                 call = BwdCall(la, getattr(workloads, BWD_WORKLOADS[name])(), dev)
+            elif name in FP8_WORKLOADS:
+                call = Fp8Call(la, getattr(workloads, FP8_WORKLOADS[name])(), dev, peaks_kind)
+            elif name.endswith("_quantize_fp8"):
+                call = QuantizeCall(la, getattr(workloads, name[:-len("_quantize_fp8")])(), dev)
             elif name in PREFILL_WORKLOADS:
                 call = PrefillCall(la, getattr(workloads, name)(), dev)
             else:

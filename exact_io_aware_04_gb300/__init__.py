@@ -9,6 +9,7 @@ CUDA device, the calls raise.
     out, lse = attn_fwd(q, k, v, causal=True)                       # dense THD/BSHD
     out, lse = attn_fwd(q, k, v, causal=True, cu_seqlens_q=cq, cu_seqlens_k=ck)
     dq, dk, dv = attn_bwd(q, k, v, out, lse, dout, causal=True)
+    q8, qs = attn_quantize_fp8(q); ...; out, lse = attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)
     out, lse = attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens)
     out, lse = attn_decode_kvcache(q, k_cache, v_cache, block_table, seq_lens, k_new=kn, v_new=vn)
 """
@@ -26,7 +27,10 @@ from ._binding import (  # noqa: F401
     attn_decode_paged,
     attn_decode_paged_noalloc,
     attn_decode_workspace_size,
+    attn_quantize_fp8,
+    attn_fp8_scale_count,
     attn_fwd,
+    attn_fwd_fp8,
     attn_get_device_status,
     attn_set_validation,
     attn_status_string,

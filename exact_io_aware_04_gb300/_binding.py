@@ -66,6 +66,12 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_kvcache.restype = I
             L.attn_decode_kvcache_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
             L.attn_decode_kvcache_workspace_size.restype = Z
+            L.attn_fp8_scale_count.argtypes = [I, I]
+            L.attn_fp8_scale_count.restype = Z
+            L.attn_quantize_fp8.argtypes = [P, P, P, I, I, I, I, P, P]
+            L.attn_quantize_fp8.restype = I
+            L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P]
+            L.attn_fwd_fp8.restype = I
             L.attn_get_device_status.argtypes = [P]
             L.attn_get_device_status.restype = I
             L.attn_set_validation.argtypes = [I]
@@ -172,6 +178,89 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool,
         _check(lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d,
                                      float(scale), 1 if causal else 0, left, right, _ptr(cu_seqlens_q),
                                      _ptr(cu_seqlens_k), _stream_handle(stream)))
+    return out, lse
+
+
+def attn_fp8_scale_count(B: int, T: int) -> int:
+    """Scale entries per head of a per-tile 8-bit tensor of T tokens in B sequences."""
+    return int(lib().attn_fp8_scale_count(int(B), int(T)))
+
+
+def attn_quantize_fp8(x: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = None,
+                      out: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None, stream=None):
+    """Per-tile E4M3 quantization.  Dense: x [B, N, H, d] bf16; packed: x
+    [T, H, d] with int32 cu_seqlens [B+1].  Returns (codes uint8 shaped like
+    x, scales fp32 [H, attn_fp8_scale_count(B, T)])."""
+    _need(x, "x", torch.bfloat16)
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        if x.dim() != 3:
+            raise ValueError("packed mode takes x [T, H, d]")
+        B = int(cu_seqlens.numel()) - 1
+        T, H, d = (int(v) for v in x.shape)
+        N = T
+    else:
+        if x.dim() != 4:
+            raise ValueError("dense mode takes x [B, N, H, d]")
+        B, N, H, d = (int(v) for v in x.shape)
+        T = B * N
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.zeros((H, attn_fp8_scale_count(B, T)), dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.uint8)
+    _need(scale, "scale", torch.float32)
+    _check(lib().attn_quantize_fp8(_ptr(x), _ptr(out), _ptr(scale), B, H, N, d, _ptr(cu_seqlens),
+                                   _stream_handle(stream)))
+    return out, scale
+
+
+def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,
+                 k_scale: torch.Tensor, v_scale: torch.Tensor, *, causal: bool, scale: Optional[float] = None,
+                 cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+    """Prefill forward on per-tile E4M3 q8, k8, v8 (uint8 codes, shaped as
+    attn_fwd's q, k, v) with their fp32 tile scales from attn_quantize_fp8.
+    Returns (out bf16 shaped like q8, lse) as attn_fwd."""
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        _need(t, n, torch.uint8)
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        _need(t, n, torch.float32)
+    if k8.shape != v8.shape:
+        raise ValueError("k8 and v8 must have the same shape")
+    d = int(q8.shape[-1])
+    Hq, Hkv = int(q8.shape[-2]), int(k8.shape[-2])
+    if cu_seqlens_q is not None or cu_seqlens_k is not None:
+        if cu_seqlens_q is None or cu_seqlens_k is None:
+            raise ValueError("give both cu_seqlens or neither")
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+        if q8.dim() != 3 or k8.dim() != 3:
+            raise ValueError("packed mode takes q8 [T_q, Hq, d] and k8/v8 [T_k, Hkv, d]")
+        B = int(cu_seqlens_q.numel()) - 1
+        Nq, Nk = int(q8.shape[0]), int(k8.shape[0])
+        lse_shape = (Hq, Nq)
+        tq, tk = Nq, Nk
+    else:
+        if q8.dim() != 4 or k8.dim() != 4:
+            raise ValueError("dense mode takes q8 [B, Nq, Hq, d] and k8/v8 [B, Nk, Hkv, d]")
+        B, Nq, Nk = int(q8.shape[0]), int(q8.shape[1]), int(k8.shape[1])
+        lse_shape = (B, Hq, Nq)
+        tq, tk = B * Nq, B * Nk
+    if tuple(q_scale.shape) != (Hq, attn_fp8_scale_count(B, tq)) or \
+            tuple(k_scale.shape) != (Hkv, attn_fp8_scale_count(B, tk)) or k_scale.shape != v_scale.shape:
+        raise ValueError("scales must be [heads, attn_fp8_scale_count(B, T)]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q8.device)
+    _need(out, "out", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    _check(lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                              _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale), 1 if causal else 0,
+                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream_handle(stream)))
     return out, lse
 
 

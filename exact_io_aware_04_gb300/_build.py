@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libattn.so")
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "decode.cu", "decode_noalloc.cu", "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I" + os.path.join(HERE, "..", "include")]

@@ -85,6 +85,11 @@ attn_status current_device_info(DeviceInfo* info) {
 
 attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+    return encode_tma(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes, box, swizzle128);
+}
+
+attn_status encode_tma(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -104,7 +109,7 @@ attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const 
         estride[i] = 1;
         if (i + 1 < rank) gstride[i] = strides_bytes[i];
     }
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+    CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
                           gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -191,6 +196,7 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
     a.win_right = window_right;
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
+    a.q_scale = a.k_scale = a.v_scale = nullptr;
     return launch_fwd(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -199,6 +205,83 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
                      const int* cu_seqlens_k, void* stream) {
     return attn_fwd_window(q, k, v, out, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, -1, -1, cu_seqlens_q,
                            cu_seqlens_k, stream);
+}
+
+size_t attn_fp8_scale_count(int B, int T) {
+    if (B < 0 || T < 0) return 0;
+    return static_cast<size_t>(fp8_scale_count(B, T));
+}
+
+attn_status attn_quantize_fp8(const void* x, void* x8, float* x_scale, int B, int H, int N, int d,
+                              const int* cu_seqlens, void* stream) {
+    if (!x || !x8 || !x_scale) return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8: NULL pointer");
+    if (B < 0 || H <= 0 || N < 0) return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8: bad size");
+    if (!aligned16(x) || !aligned16(x8) || (reinterpret_cast<uintptr_t>(x_scale) & 3u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8: misaligned pointer");
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_quantize_fp8: head_dim %d (built: 64, 128)", d);
+    if (!cu_seqlens && static_cast<long long>(B) * N > INT32_MAX)
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_quantize_fp8: more than 2^31 tokens");
+    QuantArgs a;
+    a.x = x;
+    a.x8 = x8;
+    a.scale = x_scale;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.cu = cu_seqlens;
+    return launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                         const float* v_scale, void* out, float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                         float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream) {
+    if (!q8 || !out || !lse || !q_scale) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: NULL tensor pointer");
+    if ((!k8 || !v8 || !k_scale || !v_scale) && Nk > 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: NULL k/v or scales with keys present");
+    if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: give both cu_seqlens or neither");
+    if (B < 0 || Nq < 0 || Nk < 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: negative size");
+    if (Hq <= 0 || Hkv <= 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: head counts must be positive");
+    if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: Hq %% Hkv != 0 (%d, %d)", Hq, Hkv);
+    if (!isfinite(scale) || !(scale > 0.f))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: scale must be finite and > 0");
+    if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: causal must be 0 or 1");
+    if (Nk == 0) {  // no keys: K/V and their scales are never read
+        k8 = v8 = q8;
+        k_scale = v_scale = q_scale;
+    }
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(out) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(q_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: misaligned pointer");
+    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8: head_dim %d (built: 128)", d);
+    const bool varlen = cu_seqlens_q != nullptr;
+    if (!varlen && (static_cast<long long>(B) * Nq > INT32_MAX || static_cast<long long>(B) * Nk > INT32_MAX))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8: more than 2^31 tokens");
+    if (B == 0 || Nq == 0) return ATTN_OK;
+    FwdArgs a;
+    a.q = q8;
+    a.k = k8;
+    a.v = v8;
+    a.out = out;
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal;
+    a.win_left = -1;
+    a.win_right = -1;
+    a.cu_q = cu_seqlens_q;
+    a.cu_k = cu_seqlens_k;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
 }
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int packed) {

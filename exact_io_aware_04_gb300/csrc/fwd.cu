@@ -64,16 +64,24 @@ constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kMaxSortedPairs = 1024;        // packed mode: (seq, pair) entries sorted per CTA
 constexpr int kChunks = kThreads;            // packed mode: sequences scanned in this many chunks
 
-template <int HD>
+// F8: the 8-bit forward (E4M3 Q, K, V with per-tile scales).
+template <int HD, bool F8 = false>
 struct Cfg {
-    static constexpr int kPanels = HD / 64;          // 64-element (128-byte) column panels
+    // Q and K tiles: 128-byte column panels (64 bf16 or 128 E4M3 values wide)
+    static constexpr int kPanels = F8 ? HD / 128 : HD / 64;
     static constexpr int kPanelBytes = kBM * 128;    // 128 rows x 128 bytes
     static constexpr int kTileBytes = kPanels * kPanelBytes;
+    // the V tile as the PV product reads it: 16-bit values (bf16, or f16
+    // converted from E4M3), 64-element panels
+    static constexpr int kVBytes = (HD / 64) * kPanelBytes;
     // K/V ring: slot u of an item holds V_{u-1} and K_u (what one step of
     // the MMA issuer consumes), so each step needs one wait and one release
     static constexpr int kStages = HD == 128 ? 2 : 4;
-    static constexpr int kSlotBytes = 2 * kTileBytes;  // [K part][V part]
-    static constexpr int kSmemBytes = (2 + 2 * kStages) * kTileBytes + 1024;
+    static constexpr int kSlotBytes = kTileBytes + kVBytes;  // [K part][V part]
+    // 8-bit V tiles land in a ring of their own and are widened into the slot
+    static constexpr int kV8Stages = F8 ? 2 : 0;
+    static constexpr int kV8Bytes = F8 ? kBM * HD : 0;
+    static constexpr int kSmemBytes = 2 * kTileBytes + kStages * kSlotBytes + kV8Stages * kV8Bytes + 1024;
     static constexpr uint32_t kTmemCols = 512;
     // tensor-memory column of S_t / P_t and of O_t
     __device__ static constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
@@ -94,6 +102,10 @@ struct FwdParams {
     int varlen;
     float scale_log2;   // scale * log2(e)
     int* err;
+    // 8-bit forward: per-tile scales [heads, n_scale_q / n_scale_k], tile t
+    // of sequence b at entry q_base_b / 128 + b + t (k_base_b for K and V)
+    const float *q_scale, *k_scale, *v_scale;
+    long long n_scale_q, n_scale_k;
 };
 
 struct Seq {
@@ -287,16 +299,20 @@ __device__ __forceinline__ int snake(int round, int cta, int grid) {
 // Per query tile t: q_full+t, q_empty+t, s_full+t, p_ready+t, o_final+t,
 // o_empty+t, tok+t (issuer t has issued its MMAs of a ring slot), mma_done+t.
 // Per ring slot s: kv_full+s, kv_empty+s (one release from each issuer).
-template <int S>
+// 8-bit forward only: v8_full+s, v8_empty+s for the two 8-bit V staging
+// slots; kv_full then also waits for the converter warp's arrival.
+template <int S, bool F8 = false>
 struct BarIdx {
     static constexpr int q_full = 0, q_empty = 2;
     static constexpr int kv_full = 4, kv_empty = 4 + S;
     static constexpr int s_full = 4 + 2 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
     static constexpr int tok = o_empty + 2, mma_done = tok + 2;
-    static constexpr int count = mma_done + 2;
+    static constexpr int v8_full = mma_done + 2, v8_empty = v8_full + 2;
+    static constexpr int count = F8 ? v8_empty + 2 : mma_done + 2;
     __device__ static constexpr uint32_t arrivals(int i) {
         return (i >= p_ready && i < p_ready + 2) || (i >= o_empty && i < o_empty + 2) ? 4u
                : (i >= kv_empty && i < kv_empty + S)                                   ? 2u
+               : (F8 && i >= kv_full && i < kv_full + S)                               ? 2u
                                                                                        : 1u;
     }
 };
@@ -304,15 +320,17 @@ struct BarIdx {
 __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); }
 
 // ---------------------------------------------------------------- producer warp (one thread)
-template <int HD>
+template <int HD, bool F8>
 __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                            int n_items) {
-    using C = Cfg<HD>;
-    using BI = BarIdx<C::kStages>;
+    using C = Cfg<HD, F8>;
+    using BI = BarIdx<C::kStages, F8>;
     constexpr int S = C::kStages;
+    constexpr int kPanelElems = F8 ? 128 : 64;  // elements per 128-byte panel
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
+    const uint32_t v8_0 = ring0 + S * C::kSlotBytes;  // 8-bit V staging ring (F8)
     const int grid = gridDim.x, cta = blockIdx.x;
-    uint32_t uc = 0, qc[2] = {0, 0};
+    uint32_t uc = 0, vc = 0, qc[2] = {0, 0};
     bool ok = true;
     Item it;
     for (int r = 0; ok && r * grid < n_items; ++r) {
@@ -332,7 +350,7 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_2d(smem0 + t * C::kTileBytes + pn * C::kPanelBytes, &p.tm_q, bar_at(bar0, BI::q_full + t),
-                            it.h * HD + pn * 64, y);
+                            it.h * HD + pn * kPanelElems, y);
             ++qc[t];
         }
         if (!ok) break;
@@ -343,18 +361,30 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
             if (!ok) break;
             const uint32_t slot = ring0 + st * C::kSlotBytes;
             const uint32_t full = bar_at(bar0, BI::kv_full + st);
-            mbar_arrive_expect_tx(full, (u < n ? C::kTileBytes : 0) + (u >= 1 ? C::kTileBytes : 0));
+            // 8-bit: the converter warp writes the slot's V part and arrives itself
+            mbar_arrive_expect_tx(full, (u < n ? C::kTileBytes : 0) + (!F8 && u >= 1 ? C::kVBytes : 0));
             if (u < n) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * 64,
+                    tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * kPanelElems,
                                 it.s.k_base + (it.j0 + u) * kBN);
             }
             if (u >= 1) {
+                if constexpr (F8) {
+                    const uint32_t s8 = vc % C::kV8Stages;
+                    if (vc >= C::kV8Stages)
+                        ok = mbar_wait(bar_at(bar0, BI::v8_empty + s8), ((vc / C::kV8Stages) - 1) & 1, p.err);
+                    if (!ok) break;
+                    const uint32_t v8full = bar_at(bar0, BI::v8_full + s8);
+                    mbar_arrive_expect_tx(v8full, C::kV8Bytes);
+                    tma_load_2d(v8_0 + s8 * C::kV8Bytes, &p.tm_v, v8full, g * HD, it.s.k_base + (it.j0 + u - 1) * kBN);
+                    ++vc;
+                } else {
 #pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
-                                it.s.k_base + (it.j0 + u - 1) * kBN);
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
+                                    it.s.k_base + (it.j0 + u - 1) * kBN);
+                }
             }
             ++uc;
         }
@@ -362,8 +392,89 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
     // Drain: every load issued must have landed before the CTA exits.
     for (uint32_t i = (uc > S ? uc - S : 0); i < uc; ++i)
         mbar_wait(bar_at(bar0, BI::kv_full + i % S), (i / S) & 1, p.err);
+    if constexpr (F8) {
+        for (uint32_t i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
+            mbar_wait(bar_at(bar0, BI::v8_full + i % C::kV8Stages), (i / C::kV8Stages) & 1, p.err);
+    }
     for (int t = 0; t < 2; ++t)
         if (qc[t] > 0) mbar_wait(bar_at(bar0, BI::q_full + t), (qc[t] - 1) & 1, p.err);
+}
+
+// ---------------------------------------------------------------- converter warp (8-bit forward)
+// Widens each 8-bit V tile into the 16-bit (f16) layout the PV product reads
+// -- E4M3 values are exact in f16 -- so that P can stay a 16-bit operand.
+// The staging tile is [128 keys][128 bytes], 128-byte swizzled by TMA; the
+// slot's V part is two [128 keys][64 f16] panels, 128-byte swizzled the same
+// way as a TMA-loaded bf16 V tile.  Each lane converts 16-byte chunks
+// (16 values): eight lanes cover one key row, so each shared-memory request
+// touches every bank once.  The warp walks the same items and ring slots as
+// the producer and arrives on the slot's full barrier once its writes are
+// fenced for the tensor core; a slot without a V tile (u = 0) gets the
+// arrival at once.
+template <int HD>
+__device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
+                                          int n_items) {
+    using C = Cfg<HD, true>;
+    using BI = BarIdx<C::kStages, true>;
+    constexpr int S = C::kStages;
+    const int lane = threadIdx.x & 31;
+    const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
+    const uint32_t v8_0 = ring0 + S * C::kSlotBytes;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t uc = 0, vc = 0;
+    bool ok = true;
+    Item it;
+    for (int r = 0; ok && r * grid < n_items; ++r) {
+        const int k = snake(r, cta, grid);
+        if (k >= n_items) continue;
+        item_at(p, sc, k, it);
+        const int n = it.len;
+        if (n == 0) continue;
+        for (int u = 0; u <= n && ok; ++u) {
+            const uint32_t st = uc % S;
+            if (uc >= S) ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, BI::kv_empty + st), ((uc / S) - 1) & 1, p.err));
+            if (!ok) break;
+            if (u >= 1) {
+                const uint32_t s8 = vc % C::kV8Stages;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar_at(bar0, BI::v8_full + s8), (vc / C::kV8Stages) & 1, p.err));
+                if (!ok) break;
+                const uint32_t src0 = v8_0 + s8 * C::kV8Bytes;
+                const uint32_t dst0 = ring0 + st * C::kSlotBytes + C::kTileBytes;
+#pragma unroll 4
+                for (int i = 0; i < (kBN * HD / 16) / 32; ++i) {
+                    const int q = i * 32 + lane;
+                    const int row = q >> 3, kc = q & 7;  // key row, 16-byte chunk (values 16 kc .. 16 kc + 15)
+                    uint32_t w0, w1, w2, w3;
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                 : "r"(src0 + row * 128 + ((kc ^ (row & 7)) << 4))
+                                 : "memory");
+                    const uint32_t h0 = e4m3x2_to_f16x2(w0), h1 = e4m3x2_to_f16x2(w0 >> 16);
+                    const uint32_t h2 = e4m3x2_to_f16x2(w1), h3 = e4m3x2_to_f16x2(w1 >> 16);
+                    const uint32_t h4 = e4m3x2_to_f16x2(w2), h5 = e4m3x2_to_f16x2(w2 >> 16);
+                    const uint32_t h6 = e4m3x2_to_f16x2(w3), h7 = e4m3x2_to_f16x2(w3 >> 16);
+                    // values 16 kc .. +7 and +8 .. +15: panel kc / 4, 16-byte chunks 2 (kc % 4) and + 1
+                    const uint32_t prow = dst0 + (kc >> 2) * C::kPanelBytes + row * 128;
+                    const int c0 = 2 * (kc & 3);
+                    const uint32_t a0 = prow + ((c0 ^ (row & 7)) << 4), a1 = prow + (((c0 + 1) ^ (row & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h0), "r"(h1), "r"(h2),
+                                 "r"(h3)
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(h4), "r"(h5), "r"(h6),
+                                 "r"(h7)
+                                 : "memory");
+                }
+                fence_proxy_async_smem();  // the widened tile is read by the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_at(bar0, BI::v8_empty + s8));
+                ++vc;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_at(bar0, BI::kv_full + st));
+            ++uc;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- MMA warp (one thread)
@@ -372,20 +483,32 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
 // below 256 KB).  The tensor pipe's input queue is shallow, so issue is
 // close to synchronous with execution: the issuing thread keeps the work
 // between MMA groups to the minimum.
-template <int HD>
+template <int HD, bool F8>
 __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint64_t q_desc, uint64_t k_desc) {
-    using C = Cfg<HD>;
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+    using C = Cfg<HD, F8>;
+    if constexpr (F8) {
+        // E4M3 x E4M3: 32 values (32 bytes) of the head dimension per MMA
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
 #pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4);
-        mma_smem_smem(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0);
+        for (int kk = 0; kk < HD / 32; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4);
+            mma_f8_smem_smem(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0);
+        }
+    } else {
+        constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, false);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint64_t off = static_cast<uint64_t>(((kk >> 2) * C::kPanelBytes + (kk & 3) * 32) >> 4);
+            mma_smem_smem(tmem_d, q_desc + off, k_desc + off, idesc, kk > 0);
+        }
     }
 }
 
-template <int HD>
+// P (16-bit, tensor memory) x V (16-bit, shared memory): bf16, or f16 in the
+// 8-bit forward (P carries the V tile's scale there, V the exact E4M3 values).
+template <int HD, bool F8>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc, bool first) {
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, HD, true);
+    constexpr uint32_t idesc = F8 ? idesc_f16_f32(kBM, HD, true) : idesc_bf16_f32(kBM, HD, true);
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk)
         mma_tmem_smem(tmem_o, tmem_p + kk * 8, v_desc + static_cast<uint64_t>((kk * 2048) >> 4), idesc,
@@ -402,11 +525,11 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 // tensor pipe).  Slot u of an item holds V_{j-1} and K_j (j = j0 + u):
 // issuer t runs PV_t(j-1) and S_t(j) for the tiles inside its own range
 // [lo_t, hi_t), then releases the slot.
-template <int HD>
+template <int HD, bool F8>
 __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                       uint32_t tmem, int n_items, int t) {
-    using C = Cfg<HD>;
-    using BI = BarIdx<C::kStages>;
+    using C = Cfg<HD, F8>;
+    using BI = BarIdx<C::kStages, F8>;
     constexpr int S = C::kStages;
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const uint64_t dq = smem_desc_sw128(smem0 + t * C::kTileBytes, 16, 1024);
@@ -452,14 +575,14 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
             if (!ok) break;
             if (pv) {
                 tc_fence_after_sync();
-                issue_pv<HD>(to, ts, dv0 + st * kSlotDesc, u - 1 == ulo);
+                issue_pv<HD, F8>(to, ts, dv0 + st * kSlotDesc, u - 1 == ulo);
                 if (u == uhi) {
                     tc_commit(b_o_final);
                     ++oc;
                 }
             }
             if (sm) {
-                issue_s<HD>(ts, dq, dk0 + st * kSlotDesc);
+                issue_s<HD, F8>(ts, dq, dk0 + st * kSlotDesc);
                 tc_commit(b_s_full);
                 if (u == uhi - 1) tc_commit(b_q_empty);
             }
@@ -534,11 +657,18 @@ __device__ __forceinline__ void tmem_ld_wait128_f(float* r) {
 }
 
 // ---------------------------------------------------------------- softmax warpgroups
-template <int HD>
+// 8-bit forward: the scores of tile j are c_j * (Q8 K8_j^T) with
+// c_j = scale * log2(e) * s_q * s_k(j) (the tiles' scales), and the values
+// are s_v(j) * V8_j.  Each tile's scale ratio r_j = s_v(j) / s_v,max (the
+// item's largest V scale, so r_j <= 1) is folded into the exponent: the
+// softmax writes p * r_j (f16, at most 2^8) and the PV product adds
+// (p r_j) V8_j; the normaliser sums p itself, and the epilogue multiplies
+// by s_v,max / l.
+template <int HD, bool F8>
 __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc, uint32_t bar0, uint32_t tmem,
                                           int n_items, int t) {
-    using C = Cfg<HD>;
-    using BI = BarIdx<C::kStages>;
+    using C = Cfg<HD, F8>;
+    using BI = BarIdx<C::kStages, F8>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int wq = warp & 3;                 // lane quarter of tensor memory
@@ -573,6 +703,21 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
         const int kmin_last = key_first(q_tile0 + kBM - 1, nq, nk, p.win_left);
         float m_ref = -INFINITY;
         float l = 0.f;
+        // 8-bit: scale entries of this query tile and of the item's K/V tiles
+        float c_q = sl2, sv_max = 1.f, inv_sv_max = 1.f;
+        const float *ks_row = nullptr, *vs_row = nullptr;
+        if constexpr (F8) {
+            const int g = it.h / p.group;
+            c_q = sl2 * __ldg(p.q_scale + it.h * p.n_scale_q + it.s.q_base / kBM + it.b + it.pair * 2 + t);
+            ks_row = p.k_scale + g * p.n_scale_k + it.s.k_base / kBN + it.b;
+            vs_row = p.v_scale + g * p.n_scale_k + it.s.k_base / kBN + it.b;
+            float mx = 0.f;
+            for (int j = jlo + lane; j < jlo + nt; j += 32) mx = fmaxf(mx, __ldg(vs_row + j));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            sv_max = mx;
+            inv_sv_max = mx > 0.f ? 1.f / mx : 1.f;
+        }
         for (int j = jlo; j < jlo + nt; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, scnt & 1, p.err));
             ++scnt;
@@ -580,6 +725,14 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             tc_fence_after_sync();
             float x[128];
             tmem_ld_128cols_f(t_s, x);
+            // 8-bit: this tile's score coefficient, and log2 of its V scale ratio
+            float ct = sl2, lv = 0.f, inv_r = 1.f;
+            if constexpr (F8) {
+                ct = c_q * __ldg(ks_row + j);
+                const float r = __ldg(vs_row + j) * inv_sv_max;
+                asm("lg2.approx.f32 %0, %1;" : "=f"(lv) : "f"(r));
+                inv_r = 1.f / r;
+            }
             tmem_ld_wait128_f(x);
             const int k0 = j * kBN;
             if (k0 < kmin_last) {  // crosses the band's left edge (and maybe its right one)
@@ -606,14 +759,15 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                 }
                 const float mx =
                     fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-                return mx * sl2;
+                return mx * ct;
             };
-            // p = 2^(s*scale*log2e - m) into tensor memory (bf16): packed FMA
-            // for the argument, one ex2 per element, four independent packed
-            // partial sums; returns the row sum of p (fp32)
+            // p = 2^(s*scale*log2e - m) into tensor memory (bf16; 8-bit
+            // forward: p * r_j as f16): packed FMA for the argument, one ex2
+            // per element, four independent packed partial sums; returns the
+            // row sum of p (fp32)
             auto exp_pass = [&](float m) {
-                const float m_use = (m == -INFINITY) ? 0.f : m;
-                const uint64_t sc2 = f2_pack(sl2, sl2);
+                const float m_use = ((m == -INFINITY) ? 0.f : m) - lv;
+                const uint64_t sc2 = f2_pack(ct, ct);
                 const uint64_t nm2 = f2_pack(-m_use, -m_use);
                 uint64_t ls[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -626,14 +780,14 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                         a = fast_exp2(a);
                         b = fast_exp2(b);
                         ls[(c >> 1) & 3] = f2_add(ls[(c >> 1) & 3], f2_pack(a, b));
-                        pk[c >> 1] = pack_bf16x2(a, b);
+                        pk[c >> 1] = F8 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
                     }
                     tmem_st_32cols(t_s + h * 32, pk);
                 }
                 const uint64_t s01 = f2_add(ls[0], ls[1]), s23 = f2_add(ls[2], ls[3]);
                 float lo, hi;
                 f2_unpack(f2_add(s01, s23), lo, hi);
-                return lo + hi;
+                return F8 ? (lo + hi) * inv_r : lo + hi;
             };
             float lsum;
             if (j == jlo) {
@@ -690,7 +844,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             ++ocnt;
             if (!ok) break;
             tc_fence_after_sync();
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float inv_l = l > 0.f ? (F8 ? sv_max : 1.f) / l : 0.f;
 #pragma unroll 1
             for (int cc = 0; cc < HD; cc += 32) {
                 float o[32];
@@ -738,10 +892,10 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
     }
 }
 
-template <int HD>
+template <int HD, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
-    using C = Cfg<HD>;
-    using BI = BarIdx<C::kStages>;
+    using C = Cfg<HD, F8>;
+    using BI = BarIdx<C::kStages, F8>;
     extern __shared__ __align__(1024) uint8_t smem_dyn[];
     __shared__ __align__(8) uint64_t bars[BI::count];
     __shared__ uint32_t tmem_base_slot;
@@ -775,13 +929,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     if (warp >= 8) {
         regs_decrease<kControlRegs>();
-        if (warp == kProducerWarp && lane == 0) role_producer<HD>(p, sched, smem0, bar0, n_items);
-        if (warp == kMmaWarp && lane == 0) role_mma<HD>(p, sched, smem0, bar0, tmem, n_items, 0);
-        if (warp == kMmaWarp + 1 && lane == 0) role_mma<HD>(p, sched, smem0, bar0, tmem, n_items, 1);
+        if (warp == kProducerWarp && lane == 0) role_producer<HD, F8>(p, sched, smem0, bar0, n_items);
+        if (warp == kMmaWarp && lane == 0) role_mma<HD, F8>(p, sched, smem0, bar0, tmem, n_items, 0);
+        if (warp == kMmaWarp + 1 && lane == 0) role_mma<HD, F8>(p, sched, smem0, bar0, tmem, n_items, 1);
+        if constexpr (F8) {
+            if (warp == kMmaWarp + 2) role_convert<HD>(p, sched, smem0, bar0, n_items);
+        }
         __syncwarp();
     } else {
         regs_increase<kSoftmaxRegs>();
-        role_softmax<HD>(p, sched, bar0, tmem, n_items, warp >> 2);
+        role_softmax<HD, F8>(p, sched, bar0, tmem, n_items, warp >> 2);
     }
 
     tc_fence_before_sync();
@@ -800,9 +957,9 @@ __global__ void check_cu_seqlens_kernel(const int* cu, int B, int total, int* er
     }
 }
 
-template <int HD>
+template <int HD, bool F8>
 attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-    using C = Cfg<HD>;
+    using C = Cfg<HD, F8>;
     FwdParams p;
     memset(&p, 0, sizeof(p));
     const bool varlen = a.cu_q != nullptr;
@@ -811,21 +968,31 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     // encodable, so they get one row.
     uint64_t t_k = varlen ? static_cast<uint64_t>(a.Nk) : static_cast<uint64_t>(a.B) * a.Nk;
     if (t_k == 0) t_k = 1;
-    const uint32_t box[2] = {64, kBM};
+    // boxes of 128 bytes x 128 rows: 64 bf16 or 128 E4M3 values wide
+    constexpr uint64_t kElem = F8 ? 1 : 2;
+    const CUtensorMapDataType dtype = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t box[2] = {static_cast<uint32_t>(128 / kElem), kBM};
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(a.Hq) * HD, t_q};
-        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hq) * HD * 2};
-        attn_status st = encode_tma_bf16(&p.tm_q, a.q, 2, dims, strides, box, true);
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hq) * HD * kElem};
+        attn_status st = encode_tma(&p.tm_q, dtype, a.q, 2, dims, strides, box, true);
         if (st != ATTN_OK) return st;
     }
     {
         // with no keys the maps point at q (one row, never read)
         const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, t_k};
-        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * 2};
-        attn_status st = encode_tma_bf16(&p.tm_k, a.k, 2, dims, strides, box, true);
+        const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * kElem};
+        attn_status st = encode_tma(&p.tm_k, dtype, a.k, 2, dims, strides, box, true);
         if (st != ATTN_OK) return st;
-        st = encode_tma_bf16(&p.tm_v, a.v, 2, dims, strides, box, true);
+        st = encode_tma(&p.tm_v, dtype, a.v, 2, dims, strides, box, true);
         if (st != ATTN_OK) return st;
+    }
+    if constexpr (F8) {
+        p.q_scale = a.q_scale;
+        p.k_scale = a.k_scale;
+        p.v_scale = a.v_scale;
+        p.n_scale_q = fp8_scale_count(a.B, static_cast<long long>(t_q));
+        p.n_scale_k = fp8_scale_count(a.B, varlen ? static_cast<long long>(a.Nk) : static_cast<long long>(a.B) * a.Nk);
     }
     p.out = static_cast<__nv_bfloat16*>(a.out);
     p.lse = a.lse;
@@ -858,14 +1025,14 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     static std::atomic<bool> attr_set[kMaxDevices];  // per instantiation and device
     const bool cached = dev.device >= 0 && dev.device < kMaxDevices;
     if (!cached || !attr_set[dev.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<HD, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) {
             set_error_message("cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
         }
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<HD>);
+        e = cudaFuncGetAttributes(&fa, attn_fwd_kernel<HD, F8>);
         if (e != cudaSuccess) {
             set_error_message("cudaFuncGetAttributes: %s", cudaGetErrorString(e));
             return ATTN_ERR_CUDA;
@@ -878,7 +1045,7 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
         }
         if (cached) attr_set[dev.device].store(true, std::memory_order_release);
     }
-    attn_fwd_kernel<HD><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
+    attn_fwd_kernel<HD, F8><<<grid, kThreads, C::kSmemBytes, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_error_message("attn_fwd launch: %s", cudaGetErrorString(e));
@@ -893,8 +1060,16 @@ attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     DeviceInfo dev;
     attn_status st = current_device_info(&dev);
     if (st != ATTN_OK) return st;
-    if (a.d == 128) return launch_typed<128>(a, dev, stream);
-    if (a.d == 64) return launch_typed<64>(a, dev, stream);
+    if (a.d == 128) return launch_typed<128, false>(a, dev, stream);
+    if (a.d == 64) return launch_typed<64, false>(a, dev, stream);
+    return ATTN_ERR_UNSUPPORTED;
+}
+
+attn_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
+    DeviceInfo dev;
+    attn_status st = current_device_info(&dev);
+    if (st != ATTN_OK) return st;
+    if (a.d == 128) return launch_typed<128, true>(a, dev, stream);
     return ATTN_ERR_UNSUPPORTED;
 }
 

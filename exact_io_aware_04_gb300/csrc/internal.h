@@ -33,6 +33,9 @@ void set_error_message(const char* fmt, ...);
 // contiguous dimension; strides_bytes[i] is the byte stride of dims[i+1].
 attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+// The same for any element type (8-bit codes use CU_TENSOR_MAP_DATA_TYPE_UINT8).
+attn_status encode_tma(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
 
 bool validation_enabled();
 
@@ -49,8 +52,25 @@ struct FwdArgs {
     int causal;
     int win_left, win_right;  // local window, < 0 = unbounded
     const int *cu_q, *cu_k;
+    // 8-bit forward only (q, k, v then hold E4M3 codes): per-tile scales,
+    // [heads, fp8_scale_count(B, T)] each (tile t of sequence b at entry
+    // first_token_b / 128 + b + t)
+    const float *q_scale, *k_scale, *v_scale;
 };
 attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream);
+attn_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);
+
+// Scale entries per head of a per-tile 8-bit tensor of T tokens in B sequences.
+inline long long fp8_scale_count(long long B, long long T) { return T / 128 + B; }
+
+struct QuantArgs {
+    const void* x;       // [T, H, d] bf16
+    void* x8;            // [T, H, d] E4M3 codes
+    float* scale;        // [H, fp8_scale_count(B, T)]
+    int B, H, N, d;      // N: tokens per sequence (dense) or T (packed)
+    const int* cu;       // int32 [B + 1] or NULL (dense)
+};
+attn_status launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
     const void *q, *k, *v, *out, *dout;  // out = the forward output O, dout = dL/dO

@@ -170,6 +170,18 @@ __device__ __forceinline__ void mma_tmem_smem(uint32_t d_tmem, uint32_t a_tmem, 
         : "memory");
 }
 
+// D(tmem) (+)= A(smem desc) * B(smem desc), kind::f8f6f4 (8-bit operands as
+// the instruction descriptor names them, fp32 accumulate).
+__device__ __forceinline__ void mma_f8_smem_smem(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose
 // swizzle atoms (8 rows x 128 bytes) start on 1024-byte boundaries.
 //   lbo: byte offset between atoms along the leading dimension (used by
@@ -195,6 +207,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)
            | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f16 with f16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool b_mn_major) {
+    return (1u << 4)                            // D format: f32
+           | (0u << 7)                          // A format: f16
+           | (0u << 10)                         // B format: f16
+           | (0u << 15)                         // A K-major
+           | ((b_mn_major ? 1u : 0u) << 16)     // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A/B (both K-major) and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4)                            // D format: f32
+           | (0u << 7)                          // A format: E4M3
+           | (0u << 10)                         // B format: E4M3
+           | (static_cast<uint32_t>(N >> 3) << 17)
+           | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy accesses (tcgen05.mma operands, TMA) that a barrier hands them to.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // 32 lanes x 32 bits, 32 consecutive columns: thread t of the warp receives
@@ -321,6 +359,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Two floats to packed f16x2 (round to nearest even); `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Two E4M3 codes (bits 0..7 and 8..15) to packed f16x2 (exact); the code in
+// bits 0..7 becomes the f16 in bits 0..15.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+    uint32_t r;
+    const uint16_t c = static_cast<uint16_t>(codes16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+
 // 32-byte global store (one full sector per lane); dst must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&w)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),

@@ -122,6 +122,82 @@ attn_status attn_fwd_window(const void *q, const void *k, const void *v,
                             void *stream);
 
 /*
+ * attn_fp8_scale_count -- scale entries per head of a per-tile 8-bit tensor
+ * holding T tokens in B sequences: T / 128 + B (integer division).  Tile t of
+ * sequence b (its tokens [first_b + 128 t, first_b + 128 (t + 1)), cut at the
+ * sequence end) has entry first_b / 128 + b + t, first_b being the
+ * sequence's first token; entries between sequences are never used.  0 for
+ * B < 0 or T < 0.  Pure host arithmetic.
+ */
+size_t attn_fp8_scale_count(int B, int T);
+
+/*
+ * attn_quantize_fp8 -- per-tile 8-bit (E4M3) quantization of a bf16 tensor
+ * for attn_fwd_fp8.
+ *
+ * Operation: the per-tile quantization of "FP8 Path and Quantization" ("Flash
+ * Attention: A Complete Architectural Autopsy", part 4) -- the block
+ * quantization of "FlashAttention-3: asynchrony and low precision on Hopper"
+ * ("FlashAttention-3 and PagedAttention"): each tile gets a scale factor from
+ * its absolute maximum.  A tile is 128 consecutive tokens of one sequence
+ * (counted from its first token) for one head and all d channels.  In fp32:
+ *     amax = max |x| over the tile,  scale = amax / 448,  inv = 448 / amax,
+ *     code = E4M3(x * inv)  (round to nearest even, saturating at 448),
+ * so x is represented as E4M3(code) * scale.  A tile with amax < 2^-100 gets
+ * scale 1 and zero codes.  E4M3: 1 sign, 4 exponent (bias 7) and 3 mantissa
+ * bits, subnormals, no infinities, largest finite 448.  Inputs must be
+ * finite.
+ *
+ * Layout:
+ *   x        [T, H, d] bf16 (read); T = B * N (cu_seqlens NULL: sequence b
+ *            owns tokens [b N, (b+1) N)) or cu_seqlens[B] (packed: int32
+ *            [B+1], nondecreasing from 0, N = T)
+ *   x8       [T, H, d] E4M3 codes, one byte each (written)
+ *   x_scale  [H, attn_fp8_scale_count(B, T)] fp32 (tile entries written,
+ *            entries between sequences untouched)
+ *   d in {64, 128}.
+ * Rejects (ATTN_ERR_INVALID_ARG): NULL pointers, B < 0, H <= 0, N < 0, x or
+ * x8 not 16-byte aligned, x_scale not 4-byte aligned.  B == 0 or T == 0
+ * enqueues nothing.
+ */
+attn_status attn_quantize_fp8(const void *x, void *x8, float *x_scale,
+                              int B, int H, int N, int d,
+                              const int *cu_seqlens, void *stream);
+
+/*
+ * attn_fwd_fp8 -- prefill forward on per-tile 8-bit (E4M3) Q, K, V.
+ *
+ * Operation: attn_fwd (bottom-right causal corner, GQA, dense or packed) on
+ * the values q8, k8, v8 stand for -- E4M3(code) * the code's tile scale, as
+ * attn_quantize_fp8 writes them.  Following "FP8 Path and Quantization" (the
+ * score computed from 8-bit operands, then turned back into fp32 for the
+ * softmax) and "FlashAttention-3: asynchrony and low precision on Hopper":
+ * S = Q8 K8^T is an 8-bit tensor-core product with fp32 accumulation, and
+ * the tile scales are folded into the exponent's coefficient.  The
+ * probabilities stay 16-bit (f16, with the V tile's scale ratio folded in)
+ * and the PV product reads the V tile widened exactly to f16: an 8-bit P
+ * would add a relative error of up to 2^-4 per weight.  The output is bf16
+ * and lse fp32, exactly as attn_fwd.
+ *
+ * Layout: q8 [T_q, Hq, d], k8 and v8 [T_k, Hkv, d], E4M3 codes; q_scale
+ * [Hq, attn_fp8_scale_count(B, T_q)], k_scale and v_scale [Hkv,
+ * attn_fp8_scale_count(B, T_k)], fp32, tiles as attn_quantize_fp8 cuts them
+ * (from the same B, N or cu_seqlens).  out, lse, B, Hq, Hkv, Nq, Nk, scale,
+ * causal and the cu_seqlens as attn_fwd.  d == 128 only (others:
+ * ATTN_ERR_UNSUPPORTED).
+ * Rejects (ATTN_ERR_INVALID_ARG): attn_fwd's cases, NULL or misaligned
+ * (4-byte) scale pointers.  k8, v8, k_scale, v_scale may be NULL only when
+ * Nk == 0.
+ */
+attn_status attn_fwd_fp8(const void *q8, const void *k8, const void *v8,
+                         const float *q_scale, const float *k_scale, const float *v_scale,
+                         void *out, float *lse,
+                         int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                         float scale, int causal,
+                         const int *cu_seqlens_q, const int *cu_seqlens_k,
+                         void *stream);
+
+/*
  * attn_bwd -- gradients dQ, dK, dV of a loss L through attn_fwd /
  * attn_fwd_window, given G = dL/dO, by recomputation.
  *

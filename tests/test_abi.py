@@ -124,6 +124,32 @@ def test_decode_noalloc_host_rejections(lib):
     assert noalloc(lib, B=0, splits=16) == 0       # fits, nothing to do
 
 
+def test_fp8_host_rejections(lib):
+    def q(x=FAKE, x8=FAKE, sc=FAKE, B=2, H=4, N=256, d=128, cu=None):
+        return lib.attn_quantize_fp8(x, x8, sc, B, H, N, d, cu, None)
+    assert q(x=None) == -1
+    assert q(sc=ctypes.c_void_p(0x10002)) == -1        # scales must be 4-byte aligned
+    assert q(x8=ctypes.c_void_p(0x10008)) == -1        # codes must be 16-byte aligned
+    assert q(H=0) == -1
+    assert q(d=96) == -2
+    assert q(B=0) == 0 and q(N=0) == 0                 # nothing to do
+
+    def f(q8=FAKE, k8=FAKE, ks=FAKE, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, causal=1, cq=None, ck=None):
+        return lib.attn_fwd_fp8(q8, k8, FAKE, FAKE, ks, FAKE, FAKE, FAKE, B, Hq, Hkv, Nq, Nk, d, 0.1, causal, cq,
+                                ck, None)
+    assert f(q8=None) == -1
+    assert f(ks=None) == -1                            # K scales needed when keys exist
+    assert f(ks=None, k8=None, Nk=0, B=0) == 0         # no keys: K/V and their scales may be NULL
+    assert f(Hq=5) == -1
+    assert f(causal=3) == -1
+    assert f(cq=FAKE) == -1
+    assert f(d=64) == -2                               # the 8-bit forward is built for d = 128
+    assert f(B=0) == 0
+    # scale entries: T // 128 + B per head
+    assert lib.attn_fp8_scale_count(2, 512) == 6 and lib.attn_fp8_scale_count(16, 8192) == 80
+    assert lib.attn_fp8_scale_count(-1, 5) == 0
+
+
 def bwd(lib, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, causal=1, wl=-1, wr=-1, ws=ctypes.c_void_p(0x100000),
         ws_bytes=1 << 20, dout=FAKE):
     return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, dout, FAKE, FAKE, FAKE, FAKE, B, Hq, Hkv, Nq, Nk, d, 0.1, causal,

@@ -1,0 +1,188 @@
+"""GPU parity of the 8-bit (E4M3) path through the C ABI.
+
+attn_quantize_fp8 must reproduce the oracle's per-tile quantization bit for
+bit (codes and scales).  attn_fwd_fp8 is compared with the fp64 oracle run on
+the values the oracle's own codes stand for (E4M3(code) * tile scale), at the
+tolerances of every other forward test: the quantization of the inputs is the
+caller's choice of representation, not an error of the kernel; what the
+kernel adds (fp32 accumulation of the 8-bit products, f16 probabilities,
+bf16 output) must stay within max-abs 1e-2, relative RMS 5e-3 and lse 1e-3.
+Which keys are attended is checked bit-exactly with one-hot values."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import assert_close, gather_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def la():
+    import exact_io_aware_04_gb300 as m
+    m.build()
+    torch.cuda.set_device(0)
+    yield m
+    assert m.attn_get_device_status() == 0
+
+
+def gpu_quantize(la, x, B, N=None, cu=None):
+    """attn_quantize_fp8 on a host bf16 tensor [T, H, d]; returns host numpy (codes, scales)."""
+    g = x.to("cuda")
+    if cu is None:
+        codes, scales = la.attn_quantize_fp8(g.view(B, N, g.shape[1], g.shape[2]))
+    else:
+        codes, scales = la.attn_quantize_fp8(g, cu_seqlens=cu.to("cuda"))
+    torch.cuda.synchronize()
+    return codes.cpu().numpy().reshape(x.shape), scales.cpu().numpy()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_quantize_dense_bit_exact(la, d):
+    x = workloads.randn_bf16((2 * 300, 3, d), seed=51)
+    spread = torch.logspace(-4, 3, x.shape[0])[:, None, None]
+    x = (x.float() * spread).to(torch.bfloat16)
+    x[128:256, 1] = 0.0                       # an all-zero tile of one head
+    x[300 + 5, 2, 7] = -300.0                 # an outlier
+    ref_c, ref_s = oracle.quantize_fp8(x, B=2, N=300)
+    got_c, got_s = gpu_quantize(la, x, 2, N=300)
+    assert np.array_equal(got_c, ref_c)
+    assert np.array_equal(got_s.view(np.uint32), ref_s.view(np.uint32))
+
+
+def test_quantize_packed_bit_exact(la):
+    lens = [130, 1, 0, 257, 128, 3000]
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    x = workloads.randn_bf16((int(cu[-1]), 2, 128), seed=52)
+    x[140:200, 0] *= 1e-30                    # tiny values: subnormal codes
+    ref_c, ref_s = oracle.quantize_fp8(x, B=len(lens), cu=cu)
+    got_c, got_s = gpu_quantize(la, x, len(lens), cu=cu)
+    assert np.array_equal(got_c, ref_c)
+    assert np.array_equal(got_s.view(np.uint32), ref_s.view(np.uint32))
+
+
+def fp8_inputs(p, device="cuda"):
+    """The oracle's codes and scales of a prefill problem, uploaded, as
+    attn_fwd_fp8 arguments; and the quantized dict for the oracle."""
+    qz = oracle.quantize_problem_fp8(p)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    (qc, qs), (kc, ks), (vc, vs) = qz["q"], qz["k"], qz["v"]
+    if p.varlen:
+        args = (up(qc), up(kc), up(vc), up(qs), up(ks), up(vs))
+        kw = dict(cu_seqlens_q=p.cu_q.to(device), cu_seqlens_k=p.cu_k.to(device))
+    else:
+        args = (up(qc).view(p.B, p.Nq, p.Hq, p.d), up(kc).view(p.B, p.Nk, p.Hkv, p.d),
+                up(vc).view(p.B, p.Nk, p.Hkv, p.d), up(qs), up(ks), up(vs))
+        kw = {}
+    return args, kw, qz
+
+
+def check_fp8(la, p, rows=None):
+    args, kw, qz = fp8_inputs(p)
+    out, lse = la.attn_fwd_fp8(*args, causal=p.causal, scale=p.scale, **kw)
+    torch.cuda.synchronize()
+    if rows is None:
+        rows = oracle.all_rows(p)
+    ref_o, ref_lse = oracle.prefill_fp8(p, rows, quantized=qz)
+    go, gl = gather_prefill(p, out, lse, rows)
+    return assert_close(p.name + " fp8", go, gl, ref_o, ref_lse)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_all_rows(la, causal):
+    p = workloads.make_prefill(1, 2, 2, 256, 256, 128, causal=causal, seed=1000, name="tiny_d128")
+    check_fp8(la, p)
+
+
+# (B, Hq, Hkv, Nq, Nk, causal)
+SMALL = [
+    (2, 4, 4, 300, 300, True),
+    (2, 4, 4, 300, 300, False),
+    (1, 2, 2, 200, 517, True),      # Nq < Nk
+    (1, 2, 2, 517, 200, True),      # Nq > Nk: leading rows have no key
+    (2, 8, 2, 384, 384, True),      # GQA 4:1, exact tile multiple
+    (1, 6, 1, 129, 1000, True),     # MQA, one row past a tile
+    (3, 2, 1, 1, 700, True),        # single query row
+    (1, 4, 2, 640, 640, False),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: "B{}_Hq{}_Hkv{}_Nq{}_Nk{}_{}".format(*c[:5], "c" if c[5] else "n"))
+def test_small_problems(la, cfg):
+    B, Hq, Hkv, Nq, Nk, causal = cfg
+    check_fp8(la, workloads.make_prefill(B, Hq, Hkv, Nq, Nk, 128, causal=causal, seed=sum(cfg[:5]) + 7))
+
+
+@pytest.mark.parametrize("q_lens,k_lens", [
+    ([5, 1, 33, 0, 130, 300], [5, 9, 200, 4, 130, 1000]),
+    ([512, 512, 100], [1024, 4000, 100]),
+    ([7, 0, 300], [3, 0, 2]),                 # Nq > Nk and an empty sequence
+])
+def test_varlen(la, q_lens, k_lens):
+    check_fp8(la, workloads.make_varlen(q_lens, k_lens, 4, 2, 128, causal=True, seed=len(q_lens) + 60))
+
+
+def test_no_keys_gives_zero_rows(la):
+    p = workloads.make_varlen([40, 3], [0, 0], 2, 1, 128, causal=True, seed=64)
+    check_fp8(la, p)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_score_ladder_all_rows(la, causal):
+    """Tile maxima that hold, rise a little, jump and fall, with per-tile
+    scales that differ from tile to tile: every branch of the rescale runs
+    on its own tile coefficient."""
+    p = workloads.score_ladder(workloads.make_prefill(1, 4, 2, 256, 1024, 128, causal=causal, seed=65))
+    check_fp8(la, p)
+
+
+def test_one_hot_attended_keys(la):
+    """Q = 0 (every allowed key weighs 1/|A_i|), V one-hot by key index over a
+    window of d keys: the nonzero pattern of O is the allowed set exactly,
+    its magnitude names the K/V head, and exp(lse) is the allowed count."""
+    p = workloads.make_varlen([3, 130, 200], [70, 300, 128], 4, 2, 128, causal=True, seed=66)
+    for base in (0, 60, 200):
+        ph = workloads.one_hot_values(p, base)
+        args, kw, qz = fp8_inputs(ph)
+        out, lse = la.attn_fwd_fp8(*args, causal=True, scale=ph.scale, **kw)
+        torch.cuda.synchronize()
+        rows = oracle.all_rows(ph)
+        ref_o, ref_lse = oracle.prefill_fp8(ph, rows, quantized=qz)
+        go, gl = gather_prefill(ph, out, lse, rows)
+        assert np.array_equal(go != 0, ref_o != 0), f"base {base}: attended-key pattern differs"
+        cnt = np.where(np.isfinite(ref_lse), np.rint(np.exp(ref_lse)), 0)
+        g_of_h = (rows[:, 1] // (p.Hq // p.Hkv)) + 1
+        nz = go != 0
+        assert np.array_equal(np.rint((go * cnt[:, None])[nz]), np.broadcast_to(g_of_h[:, None], go.shape)[nz])
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.rint(np.exp(gl[fin])), cnt[fin])
+
+
+def test_quantize_then_forward_end_to_end(la):
+    """The GPU's own quantization feeds the GPU forward; the oracle quantizes
+    the same bf16 inputs itself."""
+    p = workloads.make_varlen([300, 77], [900, 77], 8, 2, 128, causal=True, seed=67)
+    g = p.to("cuda")
+    q8, qs = la.attn_quantize_fp8(g.q, cu_seqlens=g.cu_q)
+    k8, ks = la.attn_quantize_fp8(g.k, cu_seqlens=g.cu_k)
+    v8, vs = la.attn_quantize_fp8(g.v, cu_seqlens=g.cu_k)
+    out, lse = la.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, scale=p.scale, cu_seqlens_q=g.cu_q,
+                               cu_seqlens_k=g.cu_k)
+    torch.cuda.synchronize()
+    rows = oracle.all_rows(p)
+    ref_o, ref_lse = oracle.prefill_fp8(p, rows)
+    go, gl = gather_prefill(p, out, lse, rows)
+    assert_close(p.name + " fp8 end to end", go, gl, ref_o, ref_lse)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mha_causal", "gqa_causal", "varlen_chunked"])
+def test_full_size_sampled_rows(la, name):
+    p = getattr(workloads, name)()
+    per = 32 if name == "varlen_chunked" else 128
+    rows = workloads.sample_rows(None, [nq for nq, _ in p.seq_lens()], p.Hq, per, seed=p.seed + 800).numpy()
+    print(name, check_fp8(la, p, rows))
