@@ -79,7 +79,9 @@ struct Cfg {
     static constexpr int kStages = HD == 128 ? 2 : 4;
     static constexpr int kSlotBytes = kTileBytes + kVBytes;  // [K part][V part]
     // 8-bit V tiles land in a ring of their own and are widened into the slot
-    static constexpr int kV8Stages = F8 ? 2 : 0;
+    // (V_j is loaded with K_j, a slot ahead of its use: three stages keep the
+    // producer from waiting on the converter)
+    static constexpr int kV8Stages = F8 ? 3 : 0;
     static constexpr int kV8Bytes = F8 ? kBM * HD : 0;
     static constexpr int kSmemBytes = 2 * kTileBytes + kStages * kSlotBytes + kV8Stages * kV8Bytes + 1024;
     static constexpr uint32_t kTmemCols = 512;
@@ -299,16 +301,16 @@ __device__ __forceinline__ int snake(int round, int cta, int grid) {
 // Per query tile t: q_full+t, q_empty+t, s_full+t, p_ready+t, o_final+t,
 // o_empty+t, tok+t (issuer t has issued its MMAs of a ring slot), mma_done+t.
 // Per ring slot s: kv_full+s, kv_empty+s (one release from each issuer).
-// 8-bit forward only: v8_full+s, v8_empty+s for the two 8-bit V staging
+// 8-bit forward only: v8_full+s, v8_empty+s for the S8 8-bit V staging
 // slots; kv_full then also waits for the converter warp's arrival.
-template <int S, bool F8 = false>
+template <int S, bool F8 = false, int S8 = 0>
 struct BarIdx {
     static constexpr int q_full = 0, q_empty = 2;
     static constexpr int kv_full = 4, kv_empty = 4 + S;
     static constexpr int s_full = 4 + 2 * S, p_ready = s_full + 2, o_final = p_ready + 2, o_empty = o_final + 2;
     static constexpr int tok = o_empty + 2, mma_done = tok + 2;
-    static constexpr int v8_full = mma_done + 2, v8_empty = v8_full + 2;
-    static constexpr int count = F8 ? v8_empty + 2 : mma_done + 2;
+    static constexpr int v8_full = mma_done + 2, v8_empty = v8_full + S8;
+    static constexpr int count = F8 ? v8_empty + S8 : mma_done + 2;
     __device__ static constexpr uint32_t arrivals(int i) {
         return (i >= p_ready && i < p_ready + 2) || (i >= o_empty && i < o_empty + 2) ? 4u
                : (i >= kv_empty && i < kv_empty + S)                                   ? 2u
@@ -324,7 +326,7 @@ template <int HD, bool F8>
 __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                            int n_items) {
     using C = Cfg<HD, F8>;
-    using BI = BarIdx<C::kStages, F8>;
+    using BI = BarIdx<C::kStages, F8, C::kV8Stages>;
     constexpr int S = C::kStages;
     constexpr int kPanelElems = F8 ? 128 : 64;  // elements per 128-byte panel
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
@@ -369,22 +371,23 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
                     tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * kPanelElems,
                                 it.s.k_base + (it.j0 + u) * kBN);
             }
-            if (u >= 1) {
-                if constexpr (F8) {
+            if constexpr (F8) {
+                // the 8-bit V_{j0+u} goes with K_{j0+u}, a slot ahead of the slot (u + 1) it is widened into
+                if (u < n) {
                     const uint32_t s8 = vc % C::kV8Stages;
                     if (vc >= C::kV8Stages)
                         ok = mbar_wait(bar_at(bar0, BI::v8_empty + s8), ((vc / C::kV8Stages) - 1) & 1, p.err);
                     if (!ok) break;
                     const uint32_t v8full = bar_at(bar0, BI::v8_full + s8);
                     mbar_arrive_expect_tx(v8full, C::kV8Bytes);
-                    tma_load_2d(v8_0 + s8 * C::kV8Bytes, &p.tm_v, v8full, g * HD, it.s.k_base + (it.j0 + u - 1) * kBN);
+                    tma_load_2d(v8_0 + s8 * C::kV8Bytes, &p.tm_v, v8full, g * HD, it.s.k_base + (it.j0 + u) * kBN);
                     ++vc;
-                } else {
-#pragma unroll
-                    for (int pn = 0; pn < C::kPanels; ++pn)
-                        tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
-                                    it.s.k_base + (it.j0 + u - 1) * kBN);
                 }
+            } else if (u >= 1) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
+                                it.s.k_base + (it.j0 + u - 1) * kBN);
             }
             ++uc;
         }
@@ -415,12 +418,26 @@ template <int HD>
 __device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                           int n_items) {
     using C = Cfg<HD, true>;
-    using BI = BarIdx<C::kStages, true>;
+    using BI = BarIdx<C::kStages, true, C::kV8Stages>;
     constexpr int S = C::kStages;
     const int lane = threadIdx.x & 31;
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const uint32_t v8_0 = ring0 + S * C::kSlotBytes;
     const int grid = gridDim.x, cta = blockIdx.x;
+    // Lane l converts 16-byte chunk kc = l % 8 (values 16 kc .. 16 kc + 15) of
+    // key rows 4 i + l / 8; the rows' swizzle phase (row % 8) alternates
+    // between two values with i, so the byte offsets are set up once.
+    // Destination: panel kc / 4, 16-byte chunks 2 (kc % 4) and 2 (kc % 4) + 1.
+    const int kc = lane & 7, r0 = lane >> 3;
+    uint32_t src_off[2], dst_off[2][2];
+#pragma unroll
+    for (int par = 0; par < 2; ++par) {
+        const int ph = r0 + 4 * par;  // row % 8 for rows 4 i + r0 with i % 2 == par
+        src_off[par] = r0 * 128 + ((kc ^ ph) << 4);
+        const uint32_t prow = (kc >> 2) * C::kPanelBytes + r0 * 128;
+        dst_off[par][0] = prow + (((2 * (kc & 3)) ^ ph) << 4);
+        dst_off[par][1] = prow + (((2 * (kc & 3) + 1) ^ ph) << 4);
+    }
     uint32_t uc = 0, vc = 0;
     bool ok = true;
     Item it;
@@ -441,28 +458,24 @@ __device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc
                 if (!ok) break;
                 const uint32_t src0 = v8_0 + s8 * C::kV8Bytes;
                 const uint32_t dst0 = ring0 + st * C::kSlotBytes + C::kTileBytes;
-#pragma unroll 4
-                for (int i = 0; i < (kBN * HD / 16) / 32; ++i) {
-                    const int q = i * 32 + lane;
-                    const int row = q >> 3, kc = q & 7;  // key row, 16-byte chunk (values 16 kc .. 16 kc + 15)
+#pragma unroll
+                for (int i = 0; i < (kBN * HD / 16) / 32; ++i) {  // key rows 4 i + lane / 8
+                    const int par = i & 1;
                     uint32_t w0, w1, w2, w3;
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                 : "r"(src0 + row * 128 + ((kc ^ (row & 7)) << 4))
+                                 : "r"(src0 + src_off[par] + i * 512)
                                  : "memory");
-                    const uint32_t h0 = e4m3x2_to_f16x2(w0), h1 = e4m3x2_to_f16x2(w0 >> 16);
-                    const uint32_t h2 = e4m3x2_to_f16x2(w1), h3 = e4m3x2_to_f16x2(w1 >> 16);
-                    const uint32_t h4 = e4m3x2_to_f16x2(w2), h5 = e4m3x2_to_f16x2(w2 >> 16);
-                    const uint32_t h6 = e4m3x2_to_f16x2(w3), h7 = e4m3x2_to_f16x2(w3 >> 16);
-                    // values 16 kc .. +7 and +8 .. +15: panel kc / 4, 16-byte chunks 2 (kc % 4) and + 1
-                    const uint32_t prow = dst0 + (kc >> 2) * C::kPanelBytes + row * 128;
-                    const int c0 = 2 * (kc & 3);
-                    const uint32_t a0 = prow + ((c0 ^ (row & 7)) << 4), a1 = prow + (((c0 + 1) ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(h0), "r"(h1), "r"(h2),
-                                 "r"(h3)
+                    uint32_t h[8];
+                    e4m3x4_to_f16x2x2(w0, h[0], h[1]);
+                    e4m3x4_to_f16x2x2(w1, h[2], h[3]);
+                    e4m3x4_to_f16x2x2(w2, h[4], h[5]);
+                    e4m3x4_to_f16x2x2(w3, h[6], h[7]);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][0] + i * 512),
+                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
                                  : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(h4), "r"(h5), "r"(h6),
-                                 "r"(h7)
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][1] + i * 512),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
                                  : "memory");
                 }
                 fence_proxy_async_smem();  // the widened tile is read by the tensor core
@@ -529,7 +542,7 @@ template <int HD, bool F8>
 __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                       uint32_t tmem, int n_items, int t) {
     using C = Cfg<HD, F8>;
-    using BI = BarIdx<C::kStages, F8>;
+    using BI = BarIdx<C::kStages, F8, C::kV8Stages>;
     constexpr int S = C::kStages;
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const uint64_t dq = smem_desc_sw128(smem0 + t * C::kTileBytes, 16, 1024);
@@ -668,7 +681,7 @@ template <int HD, bool F8>
 __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc, uint32_t bar0, uint32_t tmem,
                                           int n_items, int t) {
     using C = Cfg<HD, F8>;
-    using BI = BarIdx<C::kStages, F8>;
+    using BI = BarIdx<C::kStages, F8, C::kV8Stages>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int wq = warp & 3;                 // lane quarter of tensor memory
@@ -895,7 +908,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
 template <int HD, bool F8>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = Cfg<HD, F8>;
-    using BI = BarIdx<C::kStages, F8>;
+    using BI = BarIdx<C::kStages, F8, C::kV8Stages>;
     extern __shared__ __align__(1024) uint8_t smem_dyn[];
     __shared__ __align__(8) uint64_t bars[BI::count];
     __shared__ uint32_t tmem_base_slot;

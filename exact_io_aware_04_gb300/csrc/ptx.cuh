@@ -374,6 +374,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
     return r;
 }
 
+// Four E4M3 codes (bytes 0..3 of w) to two packed f16x2 words (exact): codes
+// 0, 1 into `lo` and codes 2, 3 into `hi`, the lower byte into the lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 c01, c23;\n\t"
+        "mov.b32 {c01, c23}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c01;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, c23;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 // 32-byte global store (one full sector per lane); dst must be 32-byte aligned.
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&w)[8]) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]),
