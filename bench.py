@@ -22,7 +22,8 @@ several queries with the in-place append) are timed on their own.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
                   [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|swa_causal|tiny|
-                              paged_decode|paged_decode_small|spec_decode|mha_causal_bwd|gqa_causal_bwd]
+                              paged_decode|paged_decode_small|spec_decode|mha_causal_bwd|gqa_causal_bwd|
+                              gqa_causal_fp8|mha_causal_fp8|varlen_chunked_fp8]
                   [--no-next]
 
 --impl reference times the fp64 CPU oracle on the host cores (bounded row
@@ -126,6 +127,8 @@ def backward_flops(p) -> float:
 
 KERNEL_SOURCES = {
     "attn_fwd": ["exact_io_aware_04_gb300/csrc/fwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
+    "attn_fwd_fp8": ["exact_io_aware_04_gb300/csrc/fwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
+    "attn_quantize_fp8": ["exact_io_aware_04_gb300/csrc/quant.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
     "attn_bwd": ["exact_io_aware_04_gb300/csrc/bwd.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
     "attn_decode_paged": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
     "attn_decode_kvcache": ["exact_io_aware_04_gb300/csrc/decode.cu", "exact_io_aware_04_gb300/csrc/ptx.cuh"],
@@ -561,12 +564,13 @@ def kernel_roofline(calls, ms, peaks, peaks_kind):
     steps = len(ms[idx[0]])
     units = sum(calls[c].units for c in idx) * steps
     ach = units / (tot_ms * 1e-3) * first.unit_scale
-    peak = peaks["bf16_tflops"] if first.bound == "tensor" else peaks["hbm_gbs"]
+    peak = (peaks["bf16_tflops"] if first.bound == "tensor" else peaks["hbm_gbs"]) * getattr(first, "peak_scale", 1.0)
     traffic = [measured_traffic(calls[c].kernel, calls[c].name) for c in idx]
     n_launch = sum(calls[c].launches for c in idx)
     return {"kernel": kern, "bound": first.bound, "achieved": ach, "peak": peak, "unit": first.unit,
-            "frac": ach / peak, "peak_source": f"{peaks_kind} " + ("bf16 burst" if first.bound == "tensor"
-                                                                 else "copy bandwidth"),
+            "frac": ach / peak, "peak_source": getattr(first, "peak_note", None) or
+                                               (f"{peaks_kind} " + ("bf16 burst" if first.bound == "tensor"
+                                                                    else "copy bandwidth")),
             "traffic": (sum(traffic) / len(traffic)) if all(t is not None for t in traffic) else None,
             "launches_per_step": n_launch, "configs": [calls[c].name for c in idx],
             "ms_per_launch_mean": tot_ms / (steps * len(idx))}
@@ -639,7 +643,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["libattn", "reference"], default="libattn")
     ap.add_argument("--workload", default="hot_path",
-                    choices=["hot_path"] + list(DECODE_WORKLOADS) + list(PREFILL_WORKLOADS) + list(BWD_WORKLOADS))
+                    choices=["hot_path"] + list(DECODE_WORKLOADS) + list(PREFILL_WORKLOADS) + list(BWD_WORKLOADS)
+                    + list(FP8_WORKLOADS))
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-next", action="store_true", help="skip the separately timed next rows")
     args = ap.parse_args(argv)
@@ -656,8 +661,12 @@ def main(argv=None):
     if args.workload in BWD_WORKLOADS:
         return run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind)
 
-    prefills, decode = make_workloads(args.workload, dev)
-    calls = [PrefillCall(la, p, dev) for p in prefills] + ([DecodeCall(la, decode, dev)] if decode else [])
+    if args.workload in FP8_WORKLOADS:
+        prefills, decode = [getattr(workloads, FP8_WORKLOADS[args.workload])()], None
+        calls = [Fp8Call(la, prefills[0], dev, peaks_kind)]
+    else:
+        prefills, decode = make_workloads(args.workload, dev)
+        calls = [PrefillCall(la, p, dev) for p in prefills] + ([DecodeCall(la, decode, dev)] if decode else [])
     head = calls[0]   # the headline: the largest prefill configuration (or the one workload asked for)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -942,6 +951,17 @@ class Fp8Call(PrefillCall):
         self.la.attn_fwd_fp8(self.q8, self.k8, self.v8, self.qs, self.ks, self.vs, out=self.out, lse=self.lse,
                              **self.fkw)
 
+    def e2e_parts(self):
+        src = [self.q8, self.k8, self.v8, self.qs, self.ks, self.vs]
+        host_in = [t.cpu().pin_memory() for t in src]
+        kw = dict(self.fkw)
+
+        def compute(dev_in, dev_out):
+            self.la.attn_fwd_fp8(*dev_in, out=dev_out[0], lse=dev_out[1], **kw)
+        shapes = [(tuple(self.out.shape), self.out.dtype), (tuple(self.lse.shape), self.lse.dtype)]
+        return host_in, compute, shapes, ("8-bit q, k, v codes and their scales copied from pinned host memory "
+                                          "and out, lse copied back every step")
+
 
 class QuantizeCall:
     """attn_quantize_fp8 on q, k and v of a prefill problem (three launches):
@@ -1054,7 +1074,10 @@ def accuracy(call):
             per = 16 if p.varlen else 64
             rows = workloads.sample_rows(None, [nq for nq, _ in p.seq_lens()], p.Hq, per,
                                          seed=p.seed + 700).numpy()
-            ref_o, ref_lse = oracle.prefill(p, rows)
+            if isinstance(call, Fp8Call):   # against the values the oracle's own 8-bit codes stand for
+                ref_o, ref_lse = oracle.prefill_fp8(p, rows)
+            else:
+                ref_o, ref_lse = oracle.prefill(p, rows)
             got_o, got_lse = _gather_prefill(p, call.out, call.lse, rows)
             what = f"{len(rows)} seeded rows ({per} per sequence and head)"
         elif is_kvcache(call.d):
