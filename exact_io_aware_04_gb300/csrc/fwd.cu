@@ -9,6 +9,9 @@
 //   warp  9    MMA issuer of query tile 0 (one thread), tensor-memory owner
 //   warp  10   MMA issuer of query tile 1 (one thread)
 //   warp  11   idle (it completes the third warpgroup)
+// The 8-bit forward (E4M3 Q, K, V with per-tile scales; F8 = true) keeps
+// this layout; there warps 11 and 8 also widen each 8-bit V tile to f16 for
+// the PV product, and the softmax folds the tile scales into its exponent.
 // The softmax warpgroups raise their register budget to kSoftmaxRegs and the
 // third warpgroup lowers its own to kControlRegs (setmaxnreg).
 // Tensor memory (512 columns x 128 lanes x 32 bit):
@@ -302,7 +305,8 @@ __device__ __forceinline__ int snake(int round, int cta, int grid) {
 // o_empty+t, tok+t (issuer t has issued its MMAs of a ring slot), mma_done+t.
 // Per ring slot s: kv_full+s, kv_empty+s (one release from each issuer).
 // 8-bit forward only: v8_full+s, v8_empty+s for the S8 8-bit V staging
-// slots; kv_full then also waits for the converter warp's arrival.
+// slots (each staging slot is freed by both widening warps); kv_full then
+// also waits for the two widening warps' arrivals.
 template <int S, bool F8 = false, int S8 = 0>
 struct BarIdx {
     static constexpr int q_full = 0, q_empty = 2;
@@ -314,25 +318,25 @@ struct BarIdx {
     __device__ static constexpr uint32_t arrivals(int i) {
         return (i >= p_ready && i < p_ready + 2) || (i >= o_empty && i < o_empty + 2) ? 4u
                : (i >= kv_empty && i < kv_empty + S)                                   ? 2u
-               : (F8 && i >= kv_full && i < kv_full + S)                               ? 2u
+               : (F8 && i >= kv_full && i < kv_full + S)                               ? 3u
+               : (F8 && i >= v8_empty && i < v8_empty + S8)                            ? 2u
                                                                                        : 1u;
     }
 };
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t bar0, int idx) { return bar0 + 8u * static_cast<uint32_t>(idx); }
 
-// ---------------------------------------------------------------- producer warp (one thread)
-template <int HD, bool F8>
+// ---------------------------------------------------------------- producer warp (one thread; bf16)
+template <int HD>
 __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                            int n_items) {
-    using C = Cfg<HD, F8>;
-    using BI = BarIdx<C::kStages, F8, C::kV8Stages>;
+    using C = Cfg<HD>;
+    using BI = BarIdx<C::kStages>;
     constexpr int S = C::kStages;
-    constexpr int kPanelElems = F8 ? 128 : 64;  // elements per 128-byte panel
+    constexpr int kPanelElems = 64;  // bf16 values per 128-byte panel
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
-    const uint32_t v8_0 = ring0 + S * C::kSlotBytes;  // 8-bit V staging ring (F8)
     const int grid = gridDim.x, cta = blockIdx.x;
-    uint32_t uc = 0, vc = 0, qc[2] = {0, 0};
+    uint32_t uc = 0, qc[2] = {0, 0};
     bool ok = true;
     Item it;
     for (int r = 0; ok && r * grid < n_items; ++r) {
@@ -363,27 +367,14 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
             if (!ok) break;
             const uint32_t slot = ring0 + st * C::kSlotBytes;
             const uint32_t full = bar_at(bar0, BI::kv_full + st);
-            // 8-bit: the converter warp writes the slot's V part and arrives itself
-            mbar_arrive_expect_tx(full, (u < n ? C::kTileBytes : 0) + (!F8 && u >= 1 ? C::kVBytes : 0));
+            mbar_arrive_expect_tx(full, (u < n ? C::kTileBytes : 0) + (u >= 1 ? C::kVBytes : 0));
             if (u < n) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
                     tma_load_2d(slot + pn * C::kPanelBytes, &p.tm_k, full, g * HD + pn * kPanelElems,
                                 it.s.k_base + (it.j0 + u) * kBN);
             }
-            if constexpr (F8) {
-                // the 8-bit V_{j0+u} goes with K_{j0+u}, a slot ahead of the slot (u + 1) it is widened into
-                if (u < n) {
-                    const uint32_t s8 = vc % C::kV8Stages;
-                    if (vc >= C::kV8Stages)
-                        ok = mbar_wait(bar_at(bar0, BI::v8_empty + s8), ((vc / C::kV8Stages) - 1) & 1, p.err);
-                    if (!ok) break;
-                    const uint32_t v8full = bar_at(bar0, BI::v8_full + s8);
-                    mbar_arrive_expect_tx(v8full, C::kV8Bytes);
-                    tma_load_2d(v8_0 + s8 * C::kV8Bytes, &p.tm_v, v8full, g * HD, it.s.k_base + (it.j0 + u) * kBN);
-                    ++vc;
-                }
-            } else if (u >= 1) {
+            if (u >= 1) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
                     tma_load_2d(slot + C::kTileBytes + pn * C::kPanelBytes, &p.tm_v, full, g * HD + pn * 64,
@@ -395,25 +386,72 @@ __device__ __noinline__ void role_producer(const FwdParams& p, const Schedule& s
     // Drain: every load issued must have landed before the CTA exits.
     for (uint32_t i = (uc > S ? uc - S : 0); i < uc; ++i)
         mbar_wait(bar_at(bar0, BI::kv_full + i % S), (i / S) & 1, p.err);
-    if constexpr (F8) {
-        for (uint32_t i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
-            mbar_wait(bar_at(bar0, BI::v8_full + i % C::kV8Stages), (i / C::kV8Stages) & 1, p.err);
-    }
     for (int t = 0; t < 2; ++t)
         if (qc[t] > 0) mbar_wait(bar_at(bar0, BI::q_full + t), (qc[t] - 1) & 1, p.err);
 }
 
-// ---------------------------------------------------------------- converter warp (8-bit forward)
-// Widens each 8-bit V tile into the 16-bit (f16) layout the PV product reads
-// -- E4M3 values are exact in f16 -- so that P can stay a 16-bit operand.
-// The staging tile is [128 keys][128 bytes], 128-byte swizzled by TMA; the
-// slot's V part is two [128 keys][64 f16] panels, 128-byte swizzled the same
-// way as a TMA-loaded bf16 V tile.  Each lane converts 16-byte chunks
+// ---------------------------------------------------------------- widening of 8-bit V tiles (8-bit forward)
+// Each 8-bit V tile is widened into the 16-bit (f16) layout the PV product
+// reads -- E4M3 values are exact in f16 -- so that P can stay a 16-bit
+// operand.  The staging tile is [128 keys][128 bytes], 128-byte swizzled by
+// TMA; the slot's V part is two [128 keys][64 f16] panels, 128-byte swizzled
+// the same way as a TMA-loaded bf16 V tile.  Two warps share the work: warp 11
+// (idle in the bf16 kernel) widens key rows 0-63 and the producer warp rows
+// 64-127, right after issuing its loads.  Each lane converts 16-byte chunks
 // (16 values): eight lanes cover one key row, so each shared-memory request
-// touches every bank once.  The warp walks the same items and ring slots as
-// the producer and arrives on the slot's full barrier once its writes are
-// fenced for the tensor core; a slot without a V tile (u = 0) gets the
-// arrival at once.
+// touches every bank once.  Lane l converts chunk kc = l % 8 (values 16 kc ..
+// 16 kc + 15) of key rows 4 i + l / 8; the rows' swizzle phase (row % 8)
+// alternates between two values with i, so the byte offsets are set up once.
+// Destination: panel kc / 4, 16-byte chunks 2 (kc % 4) and 2 (kc % 4) + 1.
+template <int HD>
+struct Widen {
+    using C = Cfg<HD, true>;
+    uint32_t src_off[2], dst_off[2][2];
+
+    __device__ __forceinline__ explicit Widen(int lane) {
+        const int kc = lane & 7, r0 = lane >> 3;
+#pragma unroll
+        for (int par = 0; par < 2; ++par) {
+            const int ph = r0 + 4 * par;  // row % 8 for rows 4 i + r0 with i % 2 == par
+            src_off[par] = r0 * 128 + ((kc ^ ph) << 4);
+            const uint32_t prow = (kc >> 2) * C::kPanelBytes + r0 * 128;
+            dst_off[par][0] = prow + (((2 * (kc & 3)) ^ ph) << 4);
+            dst_off[par][1] = prow + (((2 * (kc & 3) + 1) ^ ph) << 4);
+        }
+    }
+
+    // Key rows 64 half .. 64 half + 63 of the staged tile at src0 into the
+    // slot's V part at dst0; the writes are fenced for the tensor core.
+    __device__ __forceinline__ void run(uint32_t src0, uint32_t dst0, int half) const {
+#pragma unroll
+        for (int i2 = 0; i2 < kBN * HD / 16 / 32 / 2; ++i2) {
+            const int i = half * (kBN * HD / 16 / 32 / 2) + i2;
+            const int par = i2 & 1;  // i2 and i have the same parity (the half offset is even)
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(src0 + src_off[par] + i * 512)
+                         : "memory");
+            uint32_t h[8];
+            e4m3x4_to_f16x2x2(w0, h[0], h[1]);
+            e4m3x4_to_f16x2x2(w1, h[2], h[3]);
+            e4m3x4_to_f16x2x2(w2, h[4], h[5]);
+            e4m3x4_to_f16x2x2(w3, h[6], h[7]);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][0] + i * 512),
+                         "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][1] + i * 512),
+                         "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+    }
+};
+
+// Warp 11: widens key rows 0-63 of every 8-bit V tile.  It walks the same
+// items and ring slots as the producer and arrives on the slot's full barrier
+// once its half is written; a slot without a V tile (u = 0) gets the arrival
+// at once.
 template <int HD>
 __device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
                                           int n_items) {
@@ -424,20 +462,7 @@ __device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
     const uint32_t v8_0 = ring0 + S * C::kSlotBytes;
     const int grid = gridDim.x, cta = blockIdx.x;
-    // Lane l converts 16-byte chunk kc = l % 8 (values 16 kc .. 16 kc + 15) of
-    // key rows 4 i + l / 8; the rows' swizzle phase (row % 8) alternates
-    // between two values with i, so the byte offsets are set up once.
-    // Destination: panel kc / 4, 16-byte chunks 2 (kc % 4) and 2 (kc % 4) + 1.
-    const int kc = lane & 7, r0 = lane >> 3;
-    uint32_t src_off[2], dst_off[2][2];
-#pragma unroll
-    for (int par = 0; par < 2; ++par) {
-        const int ph = r0 + 4 * par;  // row % 8 for rows 4 i + r0 with i % 2 == par
-        src_off[par] = r0 * 128 + ((kc ^ ph) << 4);
-        const uint32_t prow = (kc >> 2) * C::kPanelBytes + r0 * 128;
-        dst_off[par][0] = prow + (((2 * (kc & 3)) ^ ph) << 4);
-        dst_off[par][1] = prow + (((2 * (kc & 3) + 1) ^ ph) << 4);
-    }
+    const Widen<HD> wd(lane);
     uint32_t uc = 0, vc = 0;
     bool ok = true;
     Item it;
@@ -456,29 +481,7 @@ __device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(bar_at(bar0, BI::v8_full + s8), (vc / C::kV8Stages) & 1, p.err));
                 if (!ok) break;
-                const uint32_t src0 = v8_0 + s8 * C::kV8Bytes;
-                const uint32_t dst0 = ring0 + st * C::kSlotBytes + C::kTileBytes;
-#pragma unroll
-                for (int i = 0; i < (kBN * HD / 16) / 32; ++i) {  // key rows 4 i + lane / 8
-                    const int par = i & 1;
-                    uint32_t w0, w1, w2, w3;
-                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                 : "r"(src0 + src_off[par] + i * 512)
-                                 : "memory");
-                    uint32_t h[8];
-                    e4m3x4_to_f16x2x2(w0, h[0], h[1]);
-                    e4m3x4_to_f16x2x2(w1, h[2], h[3]);
-                    e4m3x4_to_f16x2x2(w2, h[4], h[5]);
-                    e4m3x4_to_f16x2x2(w3, h[6], h[7]);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][0] + i * 512),
-                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][1] + i * 512),
-                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                                 : "memory");
-                }
-                fence_proxy_async_smem();  // the widened tile is read by the tensor core
+                wd.run(v8_0 + s8 * C::kV8Bytes, ring0 + st * C::kSlotBytes + C::kTileBytes, 0);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_at(bar0, BI::v8_empty + s8));
                 ++vc;
@@ -488,6 +491,97 @@ __device__ __noinline__ void role_convert(const FwdParams& p, const Schedule& sc
             ++uc;
         }
     }
+}
+
+// Producer warp of the 8-bit forward (all 32 lanes): lane 0 issues the TMA
+// loads as the bf16 producer does -- the 8-bit V_{j0+u} with K_{j0+u}, a
+// slot ahead of the slot it is widened into -- and then the whole warp widens
+// key rows 64-127 of the V tile that slot u takes.
+template <int HD>
+__device__ __noinline__ void role_producer_f8(const FwdParams& p, const Schedule& sc, uint32_t smem0, uint32_t bar0,
+                                              int n_items) {
+    using C = Cfg<HD, true>;
+    using BI = BarIdx<C::kStages, true, C::kV8Stages>;
+    constexpr int S = C::kStages;
+    const int lane = threadIdx.x & 31;
+    const bool leader = lane == 0;
+    const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
+    const uint32_t v8_0 = ring0 + S * C::kSlotBytes;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    const Widen<HD> wd(lane);
+    uint32_t uc = 0, vc = 0, cc = 0, qc[2] = {0, 0};  // ring slots, V8 loads, V8 tiles widened, Q loads
+    bool ok = true;
+    Item it;
+    for (int r = 0; ok && r * grid < n_items; ++r) {
+        const int k = snake(r, cta, grid);
+        if (k >= n_items) continue;
+        item_at(p, sc, k, it);
+        const int n = it.len;
+        if (n == 0) continue;
+        const int g = it.h / p.group;
+        if (leader) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (it.n[t] == 0) continue;
+                if (qc[t] > 0) ok = mbar_wait(bar_at(bar0, BI::q_empty + t), (qc[t] - 1) & 1, p.err);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_at(bar0, BI::q_full + t), C::kTileBytes);
+                tma_load_2d(smem0 + t * C::kTileBytes, &p.tm_q, bar_at(bar0, BI::q_full + t), it.h * HD,
+                            it.s.q_base + it.pair * kPairRows + t * kBM);
+                ++qc[t];
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        for (int u = 0; u <= n && ok; ++u) {
+            const uint32_t st = uc % S;
+            if (uc >= S) ok = __all_sync(0xffffffffu, mbar_wait(bar_at(bar0, BI::kv_empty + st), ((uc / S) - 1) & 1, p.err));
+            if (!ok) break;
+            const uint32_t slot = ring0 + st * C::kSlotBytes;
+            if (leader) {
+                const uint32_t full = bar_at(bar0, BI::kv_full + st);
+                mbar_arrive_expect_tx(full, u < n ? C::kTileBytes : 0);
+                if (u < n) {
+                    tma_load_2d(slot, &p.tm_k, full, g * HD, it.s.k_base + (it.j0 + u) * kBN);
+                    const uint32_t s8 = vc % C::kV8Stages;
+                    if (vc >= C::kV8Stages)
+                        ok = mbar_wait(bar_at(bar0, BI::v8_empty + s8), ((vc / C::kV8Stages) - 1) & 1, p.err);
+                    if (ok) {
+                        const uint32_t v8full = bar_at(bar0, BI::v8_full + s8);
+                        mbar_arrive_expect_tx(v8full, C::kV8Bytes);
+                        tma_load_2d(v8_0 + s8 * C::kV8Bytes, &p.tm_v, v8full, g * HD,
+                                    it.s.k_base + (it.j0 + u) * kBN);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (u < n) ++vc;
+            if (u >= 1) {  // rows 64-127 of V_{j0+u-1} into this slot
+                const uint32_t s8 = cc % C::kV8Stages;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar_at(bar0, BI::v8_full + s8), (cc / C::kV8Stages) & 1, p.err));
+                if (!ok) break;
+                wd.run(v8_0 + s8 * C::kV8Bytes, slot + C::kTileBytes, 1);
+                __syncwarp();
+                if (leader) mbar_arrive(bar_at(bar0, BI::v8_empty + s8));
+                ++cc;
+            }
+            __syncwarp();
+            if (leader) mbar_arrive(bar_at(bar0, BI::kv_full + st));
+            ++uc;
+        }
+    }
+    // Drain: every load issued must have landed before the CTA exits.
+    if (leader) {
+        for (uint32_t i = (uc > S ? uc - S : 0); i < uc; ++i)
+            mbar_wait(bar_at(bar0, BI::kv_full + i % S), (i / S) & 1, p.err);
+        for (uint32_t i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
+            mbar_wait(bar_at(bar0, BI::v8_full + i % C::kV8Stages), (i / C::kV8Stages) & 1, p.err);
+        for (int t = 0; t < 2; ++t)
+            if (qc[t] > 0) mbar_wait(bar_at(bar0, BI::q_full + t), (qc[t] - 1) & 1, p.err);
+    }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------- MMA warp (one thread)
@@ -942,7 +1036,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     if (warp >= 8) {
         regs_decrease<kControlRegs>();
-        if (warp == kProducerWarp && lane == 0) role_producer<HD, F8>(p, sched, smem0, bar0, n_items);
+        if constexpr (F8) {
+            if (warp == kProducerWarp) role_producer_f8<HD>(p, sched, smem0, bar0, n_items);
+        } else {
+            if (warp == kProducerWarp && lane == 0) role_producer<HD>(p, sched, smem0, bar0, n_items);
+        }
         if (warp == kMmaWarp && lane == 0) role_mma<HD, F8>(p, sched, smem0, bar0, tmem, n_items, 0);
         if (warp == kMmaWarp + 1 && lane == 0) role_mma<HD, F8>(p, sched, smem0, bar0, tmem, n_items, 1);
         if constexpr (F8) {
