@@ -17,10 +17,11 @@
 // entry first_token_b / 128 + b + t (the entries never collide, and the ones
 // between sequences are never written).
 //
-// One CTA per (tile, head), one thread per token row: the row's d values are
-// read once into registers (whole 32-byte sectors), reduced to the tile's
-// amax through shared memory, and written back as d bytes.  HBM-bound: 2 d
-// bytes read and d bytes written per element row.
+// One CTA per (tile, head): the tile's values are read once into registers
+// (lanes sharing rows, so each warp request is whole consecutive rows),
+// reduced to the tile's amax through shared memory, and written back as
+// codes, 8 bytes per lane per row chunk.  HBM-bound: 2 bytes read and 1
+// written per value.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -68,6 +69,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 
 template <int HD>
 __global__ void __launch_bounds__(kRows) quantize_fp8_kernel(const __grid_constant__ QuantParams p) {
+    // Lanes share rows: a row is HD / 8 sixteen-byte chunks (8 values each),
+    // so one warp request covers 32 * 16 / (2 HD) consecutive-in-memory rows'
+    // worth of whole chunks; the CTA's 4 warps take interleaved row groups.
+    constexpr int kChunksPerRow = HD / 8;
+    constexpr int kRowsPerWarp = 32 / kChunksPerRow;     // rows per warp request
+    constexpr int kRowsPerIter = 4 * kRowsPerWarp;       // rows per CTA request
+    constexpr int kIters = kRows / kRowsPerIter;
     const long long idx = blockIdx.x;
     const int h = blockIdx.y;
     // the sequence owning scale entry idx: the largest b with tile_base(b) <= idx
@@ -83,51 +91,54 @@ __global__ void __launch_bounds__(kRows) quantize_fp8_kernel(const __grid_consta
     const long long t = idx - (first / kRows + b);
     if (t < 0 || t * kRows >= len) return;  // an entry between sequences
     const int rows = static_cast<int>(len - t * kRows < kRows ? len - t * kRows : kRows);
-    const int r = threadIdx.x;
-    const bool active = r < rows;
-    const long long row = first + t * kRows + r;
-    const size_t at = (static_cast<size_t>(row) * p.H + h) * HD;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunk = lane % kChunksPerRow;
+    const int row0 = warp * kRowsPerWarp + lane / kChunksPerRow;  // this lane's row in iteration 0
+    const long long tile_row0 = first + t * kRows;
 
-    constexpr int kWords = HD / 2;  // bf16 pairs per row
-    uint32_t w[kWords];
+    uint32_t w[kIters][4];
     float amax = 0.f;
-    if (active) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + at);
 #pragma unroll
-        for (int i = 0; i < HD / 8; ++i) {
-            const uint4 v = src[i];
-            w[4 * i + 0] = v.x;
-            w[4 * i + 1] = v.y;
-            w[4 * i + 2] = v.z;
-            w[4 * i + 3] = v.w;
+    for (int it = 0; it < kIters; ++it) {
+        const int r = row0 + it * kRowsPerIter;
+        if (r < rows) {
+            const uint4 v = *reinterpret_cast<const uint4*>(
+                p.x + (static_cast<size_t>(tile_row0 + r) * p.H + h) * HD + chunk * 8);
+            w[it][0] = v.x;
+            w[it][1] = v.y;
+            w[it][2] = v.z;
+            w[it][3] = v.w;
+        } else {
+            w[it][0] = w[it][1] = w[it][2] = w[it][3] = 0u;
         }
 #pragma unroll
-        for (int i = 0; i < kWords; ++i)
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        for (int k = 0; k < 4; ++k)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[it][k])), fabsf(bf16_hi(w[it][k]))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     __shared__ float warp_max[kRows / 32];
-    if ((r & 31) == 0) warp_max[r >> 5] = amax;
+    if (lane == 0) warp_max[warp] = amax;
     __syncthreads();
     amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
 
     const bool zero = !(amax >= 0x1p-100f);
     const float inv = zero ? 0.f : __fdiv_rn(448.f, amax);
-    if (r == 0) p.scale[static_cast<size_t>(h) * p.n_scale + idx] = zero ? 1.f : __fdiv_rn(amax, 448.f);
-    if (!active) return;
-    uint4* dst = reinterpret_cast<uint4*>(p.x8 + at);
+    if (threadIdx.x == 0) p.scale[static_cast<size_t>(h) * p.n_scale + idx] = zero ? 1.f : __fdiv_rn(amax, 448.f);
 #pragma unroll
-    for (int i = 0; i < HD / 16; ++i) {  // 16 codes per 16-byte store
-        uint32_t c[4];
+    for (int it = 0; it < kIters; ++it) {
+        const int r = row0 + it * kRowsPerIter;
+        if (r >= rows) continue;
+        uint32_t c[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t a = w[8 * i + 2 * k], bb = w[8 * i + 2 * k + 1];
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t a = w[it][2 * k], bb = w[it][2 * k + 1];
             const uint32_t c01 = e4m3x2(__fmul_rn(bf16_lo(a), inv), __fmul_rn(bf16_hi(a), inv));
             const uint32_t c23 = e4m3x2(__fmul_rn(bf16_lo(bb), inv), __fmul_rn(bf16_hi(bb), inv));
             c[k] = zero ? 0u : (c01 | (c23 << 16));
         }
-        dst[i] = make_uint4(c[0], c[1], c[2], c[3]);
+        *reinterpret_cast<uint2*>(p.x8 + (static_cast<size_t>(tile_row0 + r) * p.H + h) * HD + chunk * 8) =
+            make_uint2(c[0], c[1]);
     }
 }
 
