@@ -936,7 +936,7 @@ __device__ __noinline__ void q_mma(const BwdParams& p, const QItem& it, uint32_t
         ok = mbar_wait(bar_at(bar0, Q_FULL), 0, p.err);
         for (int u = 0; u < n && ok; ++u) {  // S(u) and dP(u)
             const int ks = u % C::kKStages, vs = u % C::kVStages;
-            ok = (u == 0 || mbar_wait(bar_at(bar0, Q_S_FREE), (u - 1) & 1, p.err)) &&
+            ok = (u == 0 || mbar_wait_spin(bar_at(bar0, Q_S_FREE), (u - 1) & 1, p.err)) &&
                  mbar_wait(bar_at(bar0, Q_K_FULL + ks), (u / C::kKStages) & 1, p.err);
             if (!ok) break;
             tc_fence_after_sync();
@@ -959,7 +959,7 @@ __device__ __noinline__ void q_mma(const BwdParams& p, const QItem& it, uint32_t
         const uint32_t t_dq = tmem + C::kColDQ;
         for (int u = 0; u < n && ok; ++u) {  // dQ(u)
             const int ks = u % C::kKStages;
-            ok = mbar_wait(bar_at(bar0, Q_DS_READY + (u & 1)), (u >> 1) & 1, p.err) &&
+            ok = mbar_wait_spin(bar_at(bar0, Q_DS_READY + (u & 1)), (u >> 1) & 1, p.err) &&
                  mbar_wait(bar_at(bar0, Q_K_FULL + ks), (u / C::kKStages) & 1, p.err);
             if (!ok) break;
             tc_fence_after_sync();

@@ -673,7 +673,12 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
             const bool sm = u >= ulo && u < uhi;
             ok = mbar_wait(bar_at(bar0, BI::kv_full + st), (uc / S) & 1, p.err);
             if (ok && pv) {
-                ok = mbar_wait(b_p_ready, pc & 1, p.err);
+                // the softmax's hand-off is the chain's critical link: the bf16
+                // kernel's issuer keeps polling for it (measured +4-5%); in the
+                // 8-bit kernel the widening warps need issue slots too, so the
+                // issuer polls briefly and then sleeps
+                ok = F8 ? mbar_wait_poll_then_sleep(b_p_ready, pc & 1, p.err)
+                        : mbar_wait_spin(b_p_ready, pc & 1, p.err);
                 ++pc;
                 if (ok && u - 1 == ulo && oc > 0) ok = mbar_wait(b_o_empty, (oc - 1) & 1, p.err);
             }

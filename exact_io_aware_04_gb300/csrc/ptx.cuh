@@ -76,6 +76,24 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
     return done != 0;
 }
 
+// mbar_wait without the suspend hint: the thread keeps polling, so it sees
+// the phase complete a few cycles after it does instead of when the
+// scheduler wakes it; for a wait on the critical chain of a kernel whose
+// waiting thread shares its sub-partition with little else.  The same bound
+// applies.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            record_error(err, ATTN_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 // Wait until the barrier's phase with the given parity has completed.
 // Returns false (and records ATTN_ERR_TIMEOUT) after kWaitTimeoutNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
@@ -88,6 +106,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
             return false;
         }
     }
+}
+
+// A short poll (16 probes) before the sleeping wait: a phase that completes
+// within a few hundred cycles is seen at once, a longer wait gives its issue
+// slots away as mbar_wait does.
+__device__ __forceinline__ bool mbar_wait_poll_then_sleep(uint32_t bar, uint32_t parity, int* err) {
+    for (int k = 0; k < 16; ++k)
+        if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait(bar, parity, err);
 }
 
 // ---------------------------------------------------------------- TMA
