@@ -771,11 +771,13 @@ __device__ __forceinline__ void tmem_ld_wait128_f(float* r) {
 // ---------------------------------------------------------------- softmax warpgroups
 // 8-bit forward: the scores of tile j are c_j * (Q8 K8_j^T) with
 // c_j = scale * log2(e) * s_q * s_k(j) (the tiles' scales), and the values
-// are s_v(j) * V8_j.  Each tile's scale ratio r_j = s_v(j) / s_v,max (the
-// item's largest V scale, so r_j <= 1) is folded into the exponent: the
-// softmax writes p * r_j (f16, at most 2^8) and the PV product adds
-// (p r_j) V8_j; the normaliser sums p itself, and the epilogue multiplies
-// by s_v,max / l.
+// are s_v(j) * V8_j.  Each tile's scale ratio r_j = s_v(j) / s_ref (s_ref
+// the item's first tile's) is folded into the exponent: the exponent of p
+// r_j is t + log2 r_j (t = the score in log2 units), the row's running max
+// is taken over those, the softmax writes p * r_j / 2^m (f16, at most 2^8)
+// and the PV product adds that times V8_j; the normaliser sums p / 2^m
+// (the stored value times 1 / r_j), and the epilogue multiplies by
+// s_ref / l.
 template <int HD, bool F8>
 __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc, uint32_t bar0, uint32_t tmem,
                                           int n_items, int t) {
@@ -815,20 +817,23 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
         const int kmin_last = key_first(q_tile0 + kBM - 1, nq, nk, p.win_left);
         float m_ref = -INFINITY;
         float l = 0.f;
-        // 8-bit: scale entries of this query tile and of the item's K/V tiles
-        float c_q = sl2, sv_max = 1.f, inv_sv_max = 1.f;
+        // 8-bit: scale entries of this query tile and of the item's K/V tiles.
+        // V tile j's scale enters as lv_j = log2(s_v(j) / s_ref), s_ref the
+        // scale of the item's first tile, added to the exponent of every p of
+        // the tile.  The row max then tracks p * s_v rather than p, so P (f16)
+        // is normalised to the row's largest contribution to O, whatever the
+        // spread of the V scales.
+        float c_q = sl2, s_ref = 1.f, lg_ref = 0.f;
         const float *ks_row = nullptr, *vs_row = nullptr;
         if constexpr (F8) {
             const int g = it.h / p.group;
             c_q = sl2 * __ldg(p.q_scale + it.h * p.n_scale_q + it.s.q_base / kBM + it.b + it.pair * 2 + t);
             ks_row = p.k_scale + g * p.n_scale_k + it.s.k_base / kBN + it.b;
             vs_row = p.v_scale + g * p.n_scale_k + it.s.k_base / kBN + it.b;
-            float mx = 0.f;
-            for (int j = jlo + lane; j < jlo + nt; j += 32) mx = fmaxf(mx, __ldg(vs_row + j));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            sv_max = mx;
-            inv_sv_max = mx > 0.f ? 1.f / mx : 1.f;
+            if (nt > 0) {
+                s_ref = __ldg(vs_row + jlo);
+                asm("lg2.approx.f32 %0, %1;" : "=f"(lg_ref) : "f"(s_ref));
+            }
         }
         for (int j = jlo; j < jlo + nt; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(b_s_full, scnt & 1, p.err));
@@ -837,13 +842,16 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             tc_fence_after_sync();
             float x[128];
             tmem_ld_128cols_f(t_s, x);
-            // 8-bit: this tile's score coefficient, and log2 of its V scale ratio
+            // 8-bit: this tile's score coefficient, lv_j and 2^-lv_j.  Ratios
+            // beyond 2^+-64 are clamped, which keeps every row sum term
+            // 2^(t - m) <= 2^72 and 2^-lv finite.
             float ct = sl2, lv = 0.f, inv_r = 1.f;
             if constexpr (F8) {
                 ct = c_q * __ldg(ks_row + j);
-                const float r = __ldg(vs_row + j) * inv_sv_max;
-                asm("lg2.approx.f32 %0, %1;" : "=f"(lv) : "f"(r));
-                inv_r = 1.f / r;
+                float lg;
+                asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(__ldg(vs_row + j)));
+                lv = fminf(fmaxf(lg - lg_ref, -64.f), 64.f);
+                inv_r = fast_exp2(-lv);
             }
             tmem_ld_wait128_f(x);
             const int k0 = j * kBN;
@@ -871,12 +879,12 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                 }
                 const float mx =
                     fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-                return mx * ct;
+                return F8 ? mx * ct + lv : mx * ct;
             };
             // p = 2^(s*scale*log2e - m) into tensor memory (bf16; 8-bit
-            // forward: p * r_j as f16): packed FMA for the argument, one ex2
-            // per element, four independent packed partial sums; returns the
-            // row sum of p (fp32)
+            // forward: p * 2^lv_j as f16): packed FMA for the argument, one
+            // ex2 per element, four independent packed partial sums; returns
+            // the row sum of the stored values (fp32)
             auto exp_pass = [&](float m) {
                 const float m_use = ((m == -INFINITY) ? 0.f : m) - lv;
                 const uint64_t sc2 = f2_pack(ct, ct);
@@ -899,7 +907,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                 const uint64_t s01 = f2_add(ls[0], ls[1]), s23 = f2_add(ls[2], ls[3]);
                 float lo, hi;
                 f2_unpack(f2_add(s01, s23), lo, hi);
-                return F8 ? (lo + hi) * inv_r : lo + hi;
+                return lo + hi;
             };
             float lsum;
             if (j == jlo) {
@@ -940,7 +948,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                     }
                 }
             }
-            l += lsum;
+            l += F8 ? lsum * inv_r : lsum;  // 8-bit: the row sum counts p, not p * 2^lv_j
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
@@ -956,7 +964,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             ++ocnt;
             if (!ok) break;
             tc_fence_after_sync();
-            const float inv_l = l > 0.f ? (F8 ? sv_max : 1.f) / l : 0.f;
+            const float inv_l = l > 0.f ? (F8 ? s_ref : 1.f) / l : 0.f;
 #pragma unroll 1
             for (int cc = 0; cc < HD; cc += 32) {
                 float o[32];

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import workloads
-from parity import assert_close, gather_prefill
+from parity import LSE_ABS, O_REL_RMS, assert_close, gather_prefill
 
 pytestmark = pytest.mark.gpu
 
@@ -186,3 +186,92 @@ def test_full_size_sampled_rows(la, name):
     per = 32 if name == "varlen_chunked" else 128
     rows = workloads.sample_rows(None, [nq for nq, _ in p.seq_lens()], p.Hq, per, seed=p.seed + 800).numpy()
     print(name, check_fp8(la, p, rows))
+
+
+def check_rows_on_own_scale(la, p, row_bound=2e-2):
+    """Every row of attn_fwd_fp8 against the oracle, each on its own scale.
+
+    For inputs whose tiles differ by powers of two the outputs span many
+    octaves, so the absolute bound of the other tests says nothing; instead
+    the relative RMS over all rows, the lse, and each row's error norm over
+    its reference norm are bounded.  The per-row bound is 2e-2: a bf16 output
+    rounds each element by at most 2^-9 relative (2e-3), the f16 weights by
+    2^-12, and the rest leaves room for rows whose values partly cancel.  A
+    row whose weight sits on tiles with small V scales has a small output,
+    which the global measures cannot see; the per-row one does."""
+    args, kw, qz = fp8_inputs(p)
+    out, lse = la.attn_fwd_fp8(*args, causal=p.causal, scale=p.scale, **kw)
+    torch.cuda.synchronize()
+    rows = oracle.all_rows(p)
+    ref_o, ref_lse = oracle.prefill_fp8(p, rows, quantized=qz)
+    go, gl = gather_prefill(p, out, lse, rows)
+    go = np.asarray(go, dtype=np.float64)
+    gl = np.asarray(gl, dtype=np.float64)
+    assert np.isfinite(go).all(), "non-finite output values"
+    fin = np.isfinite(ref_lse)
+    assert (np.isfinite(gl) == fin).all() and (gl[~fin] == -np.inf).all()
+    lse_err = float(np.abs(gl[fin] - ref_lse[fin]).max(initial=0.0))
+    rel = float(np.sqrt(((go - ref_o) ** 2).sum() / (ref_o ** 2).sum()))
+    ref_n = np.sqrt((ref_o ** 2).sum(axis=1))
+    err_n = np.sqrt(((go - ref_o) ** 2).sum(axis=1))
+    nz = ref_n > 0
+    assert (err_n[~nz] == 0).all(), "rows whose reference is zero must be zero"
+    worst = float((err_n[nz] / ref_n[nz]).max(initial=0.0))
+    assert rel <= O_REL_RMS, f"O rel-RMS {rel:.3e}"
+    assert lse_err <= LSE_ABS, f"lse err {lse_err:.3e}"
+    assert worst <= row_bound, f"worst row relative error {worst:.3e}"
+    return {"rel_rms": rel, "lse_abs": lse_err, "worst_row": worst}
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_scales_spanning_many_octaves(la, causal):
+    """V tiles whose values (hence scales) differ by up to 2^+-20, so that the
+    ratio of a tile's scale to the largest reaches 2^-40, far below f16's
+    normal range; Q and K tiles differ by up to 2^+-3, so that each K tile's
+    score coefficient differs while the logits stay in the range an fp32
+    softmax resolves.  Values are multiplied by powers of two, exact in bf16,
+    so the inputs stay on the oracle's grid."""
+    p = workloads.make_varlen([300, 77], [900, 300], 4, 2, 128, causal=causal, seed=68)
+    g = torch.Generator().manual_seed(69)
+    for t, lens, span in ((p.q, [300, 77], 3), (p.k, [900, 300], 3), (p.v, [900, 300], 20)):
+        start = 0
+        for L in lens:
+            for r0 in range(0, L, 128):
+                e = int(torch.randint(-span, span + 1, (1,), generator=g))
+                t[start + r0:start + min(L, r0 + 128)] = (t[start + r0:start + min(L, r0 + 128)].float()
+                                                          * 2.0 ** e).to(torch.bfloat16)
+            start += L
+    check_rows_on_own_scale(la, p)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_outlier_value_tile_with_little_weight(la, causal):
+    """The first K/V tile of every sequence holds V values 2^16 times larger
+    than the rest but scores about 14 below them (q . k = -160 on channel 0
+    at scale 1/sqrt(128)), so its weights are about 2^-20 of the others': the
+    rows' outputs come from tiles whose V scales are 2^-16 of the item's
+    largest.  Each row must still be right on its own scale."""
+    p = workloads.make_varlen([300, 200], [700, 400], 4, 2, 128, causal=causal, seed=70)
+    q = p.q.float() * 0.25
+    k = p.k.float() * 0.25
+    v = p.v.float()
+    q[:, :, 0] = 16.0
+    cq, ck = p.cu_q.tolist(), p.cu_k.tolist()
+    for b in range(p.B):
+        k[ck[b]:ck[b + 1], :, 0] = 0.0
+        k[ck[b]:ck[b] + 128, :, 0] = -10.0
+        v[ck[b]:ck[b] + 128] *= 2.0 ** 16
+    p = dataclasses.replace(p, q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v.to(torch.bfloat16))
+    check_rows_on_own_scale(la, p)
+
+
+def test_large_value_tile_unseen_by_early_rows(la):
+    """Causal, 128 queries over 300 keys: row i sees keys up to i + 172, so
+    rows 0..83 never see the last K/V tile (keys 256..299), whose values are
+    2^30 times larger.  The V scale those rows' weights are normalised to
+    must come from tiles they see, or their outputs vanish in f16."""
+    p = workloads.make_prefill(2, 4, 2, 128, 300, 128, causal=True, seed=71)
+    v = p.v.float().reshape(p.B, p.Nk, p.Hkv, p.d)
+    v[:, 256:] *= 2.0 ** 30
+    p = dataclasses.replace(p, v=v.reshape(-1, p.Hkv, p.d).to(torch.bfloat16))
+    check_rows_on_own_scale(la, p)
