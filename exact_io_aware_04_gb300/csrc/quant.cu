@@ -17,7 +17,9 @@
 // entry first_token_b / 128 + b + t (the entries never collide, and the ones
 // between sequences are never written).
 //
-// One CTA per (tile, head): the tile's values are read once into registers
+// One CTA per (tile, head), the head varying fastest so that the CTAs in
+// flight cover whole token rows (H * d contiguous values) rather than one
+// head's 2d-byte pieces of many rows: the tile's values are read once into registers
 // (lanes sharing rows, so each warp request is whole consecutive rows),
 // reduced to the tile's amax through shared memory, and written back as
 // codes, 8 bytes per lane per row chunk.  HBM-bound: 2 bytes read and 1
@@ -76,8 +78,8 @@ __global__ void __launch_bounds__(kRows) quantize_fp8_kernel(const __grid_consta
     constexpr int kRowsPerWarp = 32 / kChunksPerRow;     // rows per warp request
     constexpr int kRowsPerIter = 4 * kRowsPerWarp;       // rows per CTA request
     constexpr int kIters = kRows / kRowsPerIter;
-    const long long idx = blockIdx.x;
-    const int h = blockIdx.y;
+    const long long idx = blockIdx.x / p.H;
+    const int h = static_cast<int>(blockIdx.x - idx * p.H);
     // the sequence owning scale entry idx: the largest b with tile_base(b) <= idx
     // (tile_base strictly increases with b)
     int lo = 0, hi = p.B;
@@ -148,8 +150,8 @@ attn_status launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
     const long long T = a.cu ? static_cast<long long>(a.N) : static_cast<long long>(a.B) * a.N;
     const long long n_scale = fp8_scale_count(a.B, T);
     if (a.B == 0 || T == 0) return ATTN_OK;
-    if (n_scale > 0x7fffffffLL) {
-        set_error_message("attn_quantize_fp8: more than 2^31 tiles");
+    if (n_scale * a.H > 0x7fffffffLL) {
+        set_error_message("attn_quantize_fp8: more than 2^31 (tile, head) pairs");
         return ATTN_ERR_UNSUPPORTED;
     }
     QuantParams p;
@@ -161,7 +163,7 @@ attn_status launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
     p.H = a.H;
     p.N = a.N;
     p.cu = a.cu;
-    const dim3 grid(static_cast<unsigned>(n_scale), static_cast<unsigned>(a.H));
+    const dim3 grid(static_cast<unsigned>(n_scale * a.H));
     if (a.d == 128)
         quantize_fp8_kernel<128><<<grid, kRows, 0, stream>>>(p);
     else
