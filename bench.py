@@ -781,7 +781,7 @@ def run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind):
     ach = flops / (tot / args.steps * 1e-3) / 1e12
     roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
             "frac": ach / peaks["bf16_tflops"], "frac_nominal": ach / NOMINAL["bf16_tflops"],
-            "traffic": measured_traffic("attn_bwd", p.name), "peak_source": f"{peaks_kind} bf16 burst",
+            "traffic": measured_traffic("attn_bwd", p.name + "_backward"), "peak_source": f"{peaks_kind} bf16 burst",
             "ms_per_call_median": statistics.median(ms), "ms_per_call_p95": sorted(ms)[int(0.95 * (len(ms) - 1))],
             "flops_per_call": flops, "flops_executed_per_call": 14.0 * p.d * attended_pairs(p),
             "launches_per_call": 3, "kernel": "attn_bwd"}
