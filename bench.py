@@ -170,73 +170,146 @@ def load_peaks():
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every `period_ms`, each
-    sample stamped with the host clock when it arrives so that the samples of
-    a window (the timed region) can be summarised on their own."""
+    """SM clock, its maximum and the clock-event (throttle) reasons, sampled
+    about every `period_ms` while the region runs, each sample stamped with
+    the host clock so that the samples of a window (the timed region) can be
+    summarised on their own.  Reads NVML directly (the driver's
+    libnvidia-ml, through ctypes: a query takes microseconds, so even a
+    50 ms timed region gets dozens of samples); where NVML cannot be loaded it
+    falls back to `nvidia-smi -lms`.  Reading only: no setting is changed."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvmlClocksEventReason*), the ones reported
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int, period_ms: int = 20):
+    def __init__(self, gpu_index: int, period_ms: float = 1.0):
         self.gpu = gpu_index
         self.period_ms = period_ms
         self.proc = None
-        self.samples = []   # (host time, csv line)
+        self.nvml = None
+        self.stop = threading.Event()
+        self.thread = None
+        self.samples = []   # (host time, sm MHz, max sm MHz, set of reasons)
+        self.source = None
+        self.pci = None
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        # the CUDA device's PCI address picks the NVML device (NVML may order
+        # the GPUs differently); its index is the fallback
+        found = False
+        try:
+            pr = torch.cuda.get_device_properties(self.gpu)
+            self.pci = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+            found = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci.encode(), ctypes.byref(handle)) == 0
+        except Exception:
+            self.pci = None
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(handle)) != 0:
+            lib.nvmlShutdown()
+            raise RuntimeError("no NVML handle")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        SM = ctypes.c_int(1)   # NVML_CLOCK_SM
+
+        def query():
+            if lib.nvmlDeviceGetClockInfo(handle, SM, ctypes.byref(mhz)) != 0:
+                return None
+            if lib.nvmlDeviceGetMaxClockInfo(handle, SM, ctypes.byref(mx)) != 0:
+                return None
+            if reasons_fn(handle, ctypes.byref(bits)) != 0:
+                return None
+            return float(mhz.value), float(mx.value), {n for n, b in self.REASON_BITS.items() if bits.value & b}
+        if query() is None:
+            lib.nvmlShutdown()
+            raise RuntimeError("NVML queries failed")
+        self.nvml = (lib, query)
+
+    def _poll_nvml(self):
+        query = self.nvml[1]
+        while not self.stop.is_set():
+            r = query()
+            if r is not None:
+                self.samples.append((time.perf_counter(),) + r)
+            time.sleep(self.period_ms * 1e-3)
 
     def __enter__(self):
         try:
+            self._open_nvml()
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self.thread.start()
+            return self
+        except Exception:
+            self.nvml = None
+        try:
+            self.period_ms = 20
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
             self.thread.start()
         except Exception:
             self.proc = None
         return self
 
-    def _read(self):
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.samples.append((time.perf_counter(), line.strip()))
+            f = [x.strip() for x in line.strip().split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")}
+            self.samples.append((time.perf_counter(), sm, mx, reasons))
 
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
+        if self.nvml is not None:
+            self.nvml[0].nvmlShutdown()
 
     def summary(self, t0=None, t1=None):
-        """Median SM clock, max clock and throttle reasons of the samples that
-        arrived in [t0, t1] (all samples when no window is given)."""
+        """Median SM clock, max clock and throttle reasons of the samples taken
+        in [t0, t1] (all samples when no window is given)."""
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for t, ln in self.samples:
+        for t, s, m, r in list(self.samples):
             if (t0 is not None and t < t0) or (t1 is not None and t > t1):
                 continue
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+            sm.append(s)
+            mx.append(m)
+            reasons |= r
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_min_mhz": min(sm),
+                "reasons": sorted(reasons), "samples": len(sm)}
 
     def record(self, t0, t1):
         """The timed window's summary, with the whole run (warm-up included,
         sampler started before it) beside it."""
         rec = self.summary(t0, t1)
         rec["period_ms"] = self.period_ms
+        rec["source"] = self.source
+        if self.pci:
+            rec["gpu_pci"] = self.pci
         rec["whole_run"] = self.summary()
         return rec
 

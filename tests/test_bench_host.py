@@ -104,3 +104,24 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_clock_summary_windows_and_reasons():
+    """The clock record keeps only the samples of the timed window, reports
+    their median and the union of the clock-event reasons, and the whole run
+    beside it."""
+    c = bench.ClockSampler(0)
+    c.source = "test"
+    c.samples = [(0.0, 1000.0, 2070.0, set()), (1.0, 2070.0, 2070.0, set()), (2.0, 2055.0, 2070.0, {"sw_power_cap"}),
+                 (3.0, 2070.0, 2070.0, set()), (9.0, 800.0, 2070.0, {"hw_slowdown"})]
+    rec = c.record(1.0, 3.0)
+    assert rec["samples"] == 3 and rec["sm_mhz"] == 2070.0 and rec["sm_min_mhz"] == 2055.0
+    assert rec["reasons"] == ["sw_power_cap"] and rec["source"] == "test"
+    assert rec["whole_run"]["samples"] == 5 and rec["whole_run"]["reasons"] == ["hw_slowdown", "sw_power_cap"]
+
+
+def test_clock_sampler_without_a_gpu_records_nothing():
+    with bench.ClockSampler(0) as c:
+        pass
+    rec = c.record(0.0, 1e18)
+    assert rec["samples"] == rec["whole_run"]["samples"] == len(c.samples)
