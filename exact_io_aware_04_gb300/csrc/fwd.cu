@@ -965,11 +965,7 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
             if (!ok) break;
             tc_fence_after_sync();
             const float inv_l = l > 0.f ? (F8 ? s_ref : 1.f) / l : 0.f;
-#pragma unroll 1
-            for (int cc = 0; cc < HD; cc += 32) {
-                float o[32];
-                tmem_ld_32cols_f(t_o + cc, o);
-                tmem_ld_wait_f(o);
+            auto store_chunk = [&](const float* o, int cc) {
                 if (row_valid && out32) {  // whole 32-byte sectors
 #pragma unroll
                     for (int c = 0; c < 32; c += 16) {
@@ -990,10 +986,42 @@ __device__ __noinline__ void role_softmax(const FwdParams& p, const Schedule& sc
                         d4[c >> 3] = w;
                     }
                 }
+            };
+            if constexpr (F8) {
+                // 8-bit kernel: chunk k+1's load is in flight while chunk k is
+                // stored, and the accumulator is released once the last
+                // chunk is in registers (+1.5% there; the bf16 kernel ran
+                // 1-2% slower with it, so it keeps one chunk at a time)
+                float o0[32], o1[32];
+                tmem_ld_32cols_f(t_o, o0);
+                tmem_ld_wait_f(o0);
+#pragma unroll
+                for (int k = 0; k < HD / 32; k += 2) {
+                    tmem_ld_32cols_f(t_o + (k + 1) * 32, o1);
+                    store_chunk(o0, k * 32);
+                    tmem_ld_wait_f(o1);
+                    if (k + 2 < HD / 32) {
+                        tmem_ld_32cols_f(t_o + (k + 2) * 32, o0);
+                    } else {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(b_o_empty);
+                    }
+                    store_chunk(o1, (k + 1) * 32);
+                    if (k + 2 < HD / 32) tmem_ld_wait_f(o0);
+                }
+            } else {
+#pragma unroll 1
+                for (int cc = 0; cc < HD; cc += 32) {
+                    float o[32];
+                    tmem_ld_32cols_f(t_o + cc, o);
+                    tmem_ld_wait_f(o);
+                    store_chunk(o, cc);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_o_empty);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_o_empty);
         } else if (row_valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
             for (int c = 0; c < HD / 8; ++c) d4[c] = make_uint4(0, 0, 0, 0);
