@@ -1201,6 +1201,10 @@ attn_status launch_typed(const BwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     p.scale_log2 = a.scale * kLog2e;
     p.err = dev.err_word;
 
+    if (varlen && validation_enabled()) {
+        launch_check_cu_seqlens(a.cu_q, a.B, a.Nq, stream);
+        launch_check_cu_seqlens(a.cu_k, a.B, a.Nk, stream);
+    }
     // D = rowsum(G o O)
     if (t_q > 0) {
         constexpr int kRowsPerBlock = 256 / (HD / 8);

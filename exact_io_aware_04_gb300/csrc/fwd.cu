@@ -1208,6 +1208,12 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
 
 }  // namespace
 
+void launch_check_cu_seqlens(const int* cu, int B, int total, cudaStream_t stream) {
+    DeviceInfo dev;
+    if (current_device_info(&dev) != ATTN_OK) return;
+    check_cu_seqlens_kernel<<<1, 256, 0, stream>>>(cu, B, total, dev.err_word);
+}
+
 attn_status launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     DeviceInfo dev;
     attn_status st = current_device_info(&dev);

@@ -38,6 +38,10 @@ attn_status encode_tma(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
                        const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
 
 bool validation_enabled();
+// With validation on: checks packed offsets cu[0..B] (start 0, nondecreasing,
+// end == total) on the stream and records ATTN_ERR_BAD_INDEX in the device
+// error word if they are malformed.
+void launch_check_cu_seqlens(const int* cu, int B, int total, cudaStream_t stream);
 
 // One-shot test switch: the next paged-decode launch drops one page copy.
 int set_drop_page_load(int enabled);

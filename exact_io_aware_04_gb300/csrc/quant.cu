@@ -44,11 +44,15 @@ struct QuantParams {
     const int* cu;
 };
 
-// First token of sequence b and its length.
+// First token of sequence b and its length.  Packed offsets are clamped into
+// [0, N] (each end no lower than the start), so malformed cu_seqlens cannot
+// move any access outside x and x8.
 __device__ __forceinline__ void seq_span(const QuantParams& p, int b, long long& first, long long& len) {
     if (p.cu) {
-        first = __ldg(p.cu + b);
-        len = static_cast<long long>(__ldg(p.cu + b + 1)) - first;
+        const long long a = __ldg(p.cu + b), e = __ldg(p.cu + b + 1);
+        first = a < 0 ? 0 : (a > p.N ? p.N : a);
+        const long long end = e < first ? first : (e > p.N ? p.N : e);
+        len = end - first;
     } else {
         first = static_cast<long long>(b) * p.N;
         len = p.N;
@@ -163,6 +167,7 @@ attn_status launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream) {
     p.H = a.H;
     p.N = a.N;
     p.cu = a.cu;
+    if (a.cu != nullptr && validation_enabled()) launch_check_cu_seqlens(a.cu, a.B, a.N, stream);
     const dim3 grid(static_cast<unsigned>(n_scale * a.H));
     if (a.d == 128)
         quantize_fp8_kernel<128><<<grid, kRows, 0, stream>>>(p);
