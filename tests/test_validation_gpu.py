@@ -89,3 +89,18 @@ def test_decode_lengths_past_the_table(la):
         la.attn_decode_paged(dd.q, dd.k_cache, dd.v_cache, dd.block_table, lens)
     assert with_validation(la, True, dec) == la.ATTN_ERR_BAD_INDEX
     assert with_validation(la, False, dec) == la.ATTN_OK
+
+
+@pytest.mark.parametrize("bad", sorted(BAD_CU))
+def test_fp8_forward_packed(la, bad):
+    T, Hq, Hkv, d = 500, 4, 2, 128
+    cu_ok = torch.tensor([0, 100, 300, 500], dtype=torch.int32, device="cuda")
+    cu_bad = torch.tensor(BAD_CU[bad], dtype=torch.int32, device="cuda")
+    q8, qs = la.attn_quantize_fp8(workloads.randn_bf16((T, Hq, d), seed=1930).cuda(), cu_seqlens=cu_ok)
+    k8, ks = la.attn_quantize_fp8(workloads.randn_bf16((T, Hkv, d), seed=1931).cuda(), cu_seqlens=cu_ok)
+    v8, vs = la.attn_quantize_fp8(workloads.randn_bf16((T, Hkv, d), seed=1932).cuda(), cu_seqlens=cu_ok)
+    for cq, ck in ((cu_bad, cu_ok), (cu_ok, cu_bad)):
+        def fwd():
+            la.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, cu_seqlens_q=cq, cu_seqlens_k=ck)
+        assert with_validation(la, True, fwd) == la.ATTN_ERR_BAD_INDEX
+        assert with_validation(la, False, fwd) == la.ATTN_OK
