@@ -22,7 +22,8 @@ several queries with the in-place append) are timed on their own.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libattn|reference]
                   [--workload hot_path|mha_causal|gqa_causal|varlen_chunked|swa_causal|tiny|
-                              paged_decode|paged_decode_small|spec_decode|mha_causal_bwd|gqa_causal_bwd|
+                              paged_decode|paged_decode_small|spec_decode|spec_decode_small|
+                              mha_causal_bwd|gqa_causal_bwd|
                               gqa_causal_fp8|mha_causal_fp8|varlen_chunked_fp8]
                   [--no-next]
 
@@ -466,7 +467,7 @@ def oracle_decode_rate(d, target_s: float, seed: int):
 # The default step: the three single-GPU prefill configurations (the largest,
 # GQA causal N8192, first: it carries the headline value) and the paged decode.
 HOT_PREFILL = ("gqa_causal", "mha_causal", "varlen_chunked")
-DECODE_WORKLOADS = ("paged_decode", "paged_decode_small", "spec_decode")
+DECODE_WORKLOADS = ("paged_decode", "paged_decode_small", "spec_decode", "spec_decode_small")
 # Measured after the step on their own (backward, window, several queries with append).
 NEXT_ROWS = ("mha_causal_bwd", "gqa_causal_bwd", "swa_causal", "spec_decode", "gqa_causal_fp8", "mha_causal_fp8",
              "gqa_causal_quantize_fp8")

@@ -349,6 +349,16 @@ def spec_decode(device="cpu", nan_fill_unused=False) -> KVCacheDecode:
                                name="spec_decode_b64_nq4_hq32_hkv8_d128", device=device)
 
 
+def spec_decode_small(device="cpu", nan_fill_unused=False) -> KVCacheDecode:
+    """The speculative-decoding layout at one eighth of the lengths (U[512,
+    4096]) in a 25,000-page pool (1.6 GB of K+V): a case small enough for
+    profiler captures of the same kernels."""
+    lens = decode_lengths(seed=SEED_BASE + 8, lo=512, hi=4096)
+    return make_kvcache_decode(lens, 4, 32, 8, 128, num_pages=25_000, seed=SEED_BASE + 8, causal=True,
+                               append=True, max_pages=256, nan_fill_unused=nan_fill_unused,
+                               name="spec_decode_small_b64_nq4_hq32_hkv8_d128", device=device)
+
+
 # --------------------------------------------------------------------------
 # row samples and structured inputs
 # --------------------------------------------------------------------------
