@@ -217,3 +217,26 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 8, 2, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         la.attn_fwd(q, q, q, causal=True)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/attn.h compiles as C99 with warnings as errors, and a C caller
+    of the prefill and decode entry points type-checks against it."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(
+        '#include <stddef.h>\n#include "attn.h"\n'
+        "attn_status call(const void* q, const void* k, const void* v, void* out, float* lse, void* s,\n"
+        "                 const int* bt, const int* lens, void* ws, size_t ws_bytes) {\n"
+        "    attn_status st = attn_fwd(q, k, v, out, lse, 2, 32, 8, 1024, 1024, 128, 0.0884f, 1, NULL, NULL, s);\n"
+        "    if (st != ATTN_OK) return st;\n"
+        "    return attn_decode_paged(q, k, v, bt, 64, lens, out, lse, 2, 32, 8, 128, 16, 1000, 0.0884f, 0,\n"
+        "                             ws, ws_bytes, s);\n"
+        "}\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I",
+                        os.path.join(ROOT, "include"), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
