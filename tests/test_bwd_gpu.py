@@ -165,6 +165,13 @@ def test_full_size_mha_sampled_heads(la):
     check(la, p, pairs=[(0, 0), (3, 15), (1, 7)])
 
 
+def test_full_size_gqa_one_kv_head(la):
+    """The full GQA causal workload (B2 Hq32 Hkv8 N8192, hot channel): every
+    row of one (sequence, K/V head) pair and its four query heads, so dK and
+    dV sum over the whole group."""
+    check(la, workloads.gqa_causal(), pairs=[(1, 7)])
+
+
 def test_varlen_many_sequences(la):
     """The packed-mode tile lookup scans cu_seqlens 32 sequences at a time:
     100 sequences take several rounds."""
