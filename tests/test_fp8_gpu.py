@@ -275,3 +275,21 @@ def test_large_value_tile_unseen_by_early_rows(la):
     v[:, 256:] *= 2.0 ** 30
     p = dataclasses.replace(p, v=v.reshape(-1, p.Hkv, p.d).to(torch.bfloat16))
     check_rows_on_own_scale(la, p)
+
+
+@pytest.mark.parametrize("name", ["gqa_causal", "varlen_chunked"])
+def test_quantize_full_size_bit_exact(la, name):
+    """The quantizer on the q, k and v of the full workloads the benchmark
+    times (GQA causal with its hot channel; the packed chunked prefill), bit
+    for bit against the oracle's codes and scales."""
+    p = getattr(workloads, name)()
+    qz = oracle.quantize_problem_fp8(p)
+    for key, x, n in (("q", p.q, p.Nq), ("k", p.k, p.Nk), ("v", p.v, p.Nk)):
+        ref_c, ref_s = qz[key]
+        if p.varlen:
+            got_c, got_s = gpu_quantize(la, x, p.B, cu=p.cu_q if key == "q" else p.cu_k)
+        else:
+            got_c, got_s = gpu_quantize(la, x, p.B, N=n)
+        assert np.array_equal(got_c, np.asarray(ref_c).reshape(got_c.shape)), f"{name} {key}: codes differ"
+        assert np.array_equal(got_s.view(np.uint32), np.asarray(ref_s).view(np.uint32).reshape(got_s.shape)), \
+            f"{name} {key}: scales differ"
