@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.attn_quantize_fp8.restype = I
             L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P]
             L.attn_fwd_fp8.restype = I
+            L.attn_fwd_fp8_window.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P, P]
+            L.attn_fwd_fp8_window.restype = I
             L.attn_get_device_status.argtypes = [P]
             L.attn_get_device_status.restype = I
             L.attn_set_validation.argtypes = [I]
@@ -218,9 +220,11 @@ def attn_quantize_fp8(x: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = N
 def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,
                  k_scale: torch.Tensor, v_scale: torch.Tensor, *, causal: bool, scale: Optional[float] = None,
                  cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
-                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, stream=None):
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 window: Optional[tuple] = None, stream=None):
     """Prefill forward on per-tile E4M3 q8, k8, v8 (uint8 codes, shaped as
     attn_fwd's q, k, v) with their fp32 tile scales from attn_quantize_fp8.
+    window = (left, right) selects the local band mask (attn_fwd_fp8_window).
     Returns (out bf16 shaped like q8, lse) as attn_fwd."""
     for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
         _need(t, n, torch.uint8)
@@ -258,9 +262,16 @@ def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: 
         lse = torch.empty(lse_shape, dtype=torch.float32, device=q8.device)
     _need(out, "out", torch.bfloat16)
     _need(lse, "lse", torch.float32)
-    _check(lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
-                              _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale), 1 if causal else 0,
-                              _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream_handle(stream)))
+    if window is None:
+        _check(lib().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                  _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale), 1 if causal else 0,
+                                  _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream_handle(stream)))
+    else:
+        left, right = (int(x) for x in window)
+        _check(lib().attn_fwd_fp8_window(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale),
+                                         _ptr(v_scale), _ptr(out), _ptr(lse), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                                         1 if causal else 0, left, right, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                         _stream_handle(stream)))
     return out, lse
 
 

@@ -233,9 +233,10 @@ attn_status attn_quantize_fp8(const void* x, void* x8, float* x_scale, int B, in
     return launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
 }
 
-attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
-                         const float* v_scale, void* out, float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
-                         float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream) {
+attn_status attn_fwd_fp8_window(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                                const float* k_scale, const float* v_scale, void* out, float* lse, int B, int Hq,
+                                int Hkv, int Nq, int Nk, int d, float scale, int causal, int window_left,
+                                int window_right, const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream) {
     if (!q8 || !out || !lse || !q_scale) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: NULL tensor pointer");
     if ((!k8 || !v8 || !k_scale || !v_scale) && Nk > 0)
         return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: NULL k/v or scales with keys present");
@@ -247,6 +248,9 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const f
     if (!isfinite(scale) || !(scale > 0.f))
         return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: scale must be finite and > 0");
     if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: causal must be 0 or 1");
+    if (window_left < -1 || window_right < -1)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: window sides must be >= 0, or -1 for unbounded (%d, %d)",
+                    window_left, window_right);
     if (Nk == 0) {  // no keys: K/V and their scales are never read
         k8 = v8 = q8;
         k_scale = v_scale = q_scale;
@@ -274,14 +278,21 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const f
     a.d = d;
     a.scale = scale;
     a.causal = causal;
-    a.win_left = -1;
-    a.win_right = -1;
+    a.win_left = window_left;
+    a.win_right = window_right;
     a.cu_q = cu_seqlens_q;
     a.cu_k = cu_seqlens_k;
     a.q_scale = q_scale;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale, const float* k_scale,
+                         const float* v_scale, void* out, float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                         float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream) {
+    return attn_fwd_fp8_window(q8, k8, v8, q_scale, k_scale, v_scale, out, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal,
+                               -1, -1, cu_seqlens_q, cu_seqlens_k, stream);
 }
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Nq, int packed) {

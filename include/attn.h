@@ -198,6 +198,22 @@ attn_status attn_fwd_fp8(const void *q8, const void *k8, const void *v8,
                          void *stream);
 
 /*
+ * attn_fwd_fp8_window -- attn_fwd_fp8 with attn_fwd_window's local band mask
+ * (window_left, window_right; -1 = unbounded side; causal = 1 keeps the
+ * causal corner).  K/V tiles outside every row's band are never loaded.
+ * window_left = window_right = -1 is attn_fwd_fp8.  Everything else: as
+ * attn_fwd_fp8.
+ * Rejects (ATTN_ERR_INVALID_ARG) in addition: window_left or window_right < -1.
+ */
+attn_status attn_fwd_fp8_window(const void *q8, const void *k8, const void *v8,
+                                const float *q_scale, const float *k_scale, const float *v_scale,
+                                void *out, float *lse,
+                                int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                float scale, int causal, int window_left, int window_right,
+                                const int *cu_seqlens_q, const int *cu_seqlens_k,
+                                void *stream);
+
+/*
  * attn_bwd -- gradients dQ, dK, dV of a loss L through attn_fwd /
  * attn_fwd_window, given G = dL/dO, by recomputation.
  *

@@ -149,6 +149,13 @@ def test_fp8_host_rejections(lib):
     assert lib.attn_fp8_scale_count(2, 512) == 6 and lib.attn_fp8_scale_count(16, 8192) == 80
     assert lib.attn_fp8_scale_count(-1, 5) == 0
 
+    def w(left, right, B=1, d=128):
+        return lib.attn_fwd_fp8_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, 4, 2, 8, 8, d, 0.1, 0,
+                                       left, right, None, None, None)
+    assert w(-2, 5) == -1 and w(5, -3) == -1          # window sides below -1
+    assert w(5, 5, d=64) == -2
+    assert w(5, 5, B=0) == 0 and w(-1, -1, B=0) == 0
+
 
 def bwd(lib, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, causal=1, wl=-1, wr=-1, ws=ctypes.c_void_p(0x100000),
         ws_bytes=1 << 20, dout=FAKE):

@@ -83,6 +83,8 @@ def fp8_inputs(p, device="cuda"):
 
 def check_fp8(la, p, rows=None):
     args, kw, qz = fp8_inputs(p)
+    if tuple(getattr(p, "window", (-1, -1))) != (-1, -1):
+        kw["window"] = tuple(p.window)
     out, lse = la.attn_fwd_fp8(*args, causal=p.causal, scale=p.scale, **kw)
     torch.cuda.synchronize()
     if rows is None:
@@ -293,3 +295,32 @@ def test_quantize_full_size_bit_exact(la, name):
         assert np.array_equal(got_c, np.asarray(ref_c).reshape(got_c.shape)), f"{name} {key}: codes differ"
         assert np.array_equal(got_s.view(np.uint32), np.asarray(ref_s).view(np.uint32).reshape(got_s.shape)), \
             f"{name} {key}: scales differ"
+
+
+@pytest.mark.parametrize("window,causal", [((100, -1), True), ((40, 25), False), ((0, 0), False), ((300, 300), False)])
+def test_window_dense(la, window, causal):
+    """attn_fwd_fp8_window on a dense problem: the band of attn_fwd_window
+    (Nq < Nk, both edges inside and across tiles), every row."""
+    check_fp8(la, workloads.make_prefill(1, 4, 2, 400, 700, 128, causal=causal, seed=1950, window=window))
+
+
+def test_window_varlen(la):
+    check_fp8(la, workloads.make_varlen([200, 5, 300, 0], [700, 5, 300, 9], 4, 2, 128, causal=False, seed=1951,
+                                        window=(90, 40)))
+
+
+def test_window_attended_keys_one_hot(la):
+    """Which keys each row attends under a two-sided band, bit for bit: Q = 0
+    (codes 0, scale 1) and V one-hot by key index (exact in E4M3)."""
+    p = workloads.make_prefill(1, 4, 2, 300, 500, 128, causal=False, seed=1952, window=(70, 30))
+    for base in (0, 128, 250):
+        ph = workloads.one_hot_values(p, base)
+        args, kw, qz = fp8_inputs(ph)
+        out, lse = la.attn_fwd_fp8(*args, causal=False, scale=ph.scale, window=(70, 30))
+        torch.cuda.synchronize()
+        rows = oracle.all_rows(ph)
+        ref_o, ref_lse = oracle.prefill_fp8(ph, rows, quantized=qz)
+        go, gl = gather_prefill(ph, out, lse, rows)
+        assert np.array_equal(go != 0, ref_o != 0), f"base {base}: attended-key pattern differs"
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(gl), fin)

@@ -48,7 +48,7 @@ def prefill_case(i, fp8=False, bwd=False):
     Hq, Hkv = heads(r, 8 if bwd else 16)
     d = 128 if fp8 else int(r.choice([64, 128]))
     causal = bool(r.rand() < 0.6)
-    win = None if fp8 else window(r)
+    win = window(r)
     if win is not None and causal:
         win = (win[0], 0)   # causal fixes the right side at 0
     lim_q, lim_k = (300, 400) if bwd else (700, 1500)
