@@ -100,8 +100,11 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
     // soon as every CTA here has started; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int chunk = blockIdx.x;
-    const int b = blockIdx.y / p.head_groups;
-    const int hg = blockIdx.y - b * p.head_groups;
+    // (sequence, head group) units run over grid y and z (y at most 65535)
+    const long long unit = static_cast<long long>(blockIdx.z) * gridDim.y + blockIdx.y;
+    if (unit >= static_cast<long long>(p.B) * p.head_groups) return;  // padding of the last z slice
+    const int b = static_cast<int>(unit / p.head_groups);
+    const int hg = static_cast<int>(unit - static_cast<long long>(b) * p.head_groups);
     const int cap = p.max_pages * kPage;
     const int len = min(max(__ldg(p.seq_lens + b), 0), cap);
     const int tok0 = chunk * p.pages_per_chunk * kPage;
@@ -553,6 +556,15 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     p.drop_first_page = set_drop_page_load(0);  // consume the one-shot test switch
     p.err = dev.err_word;
 
+    // the split grid: (sequence, head group) units over y and z, checked
+    // before anything is launched (the append writes the cache)
+    const long long units = static_cast<long long>(a.B) * plan.head_groups;
+    const unsigned gy = static_cast<unsigned>(std::min<long long>(std::max<long long>(units, 1), 65535));
+    const unsigned gz = static_cast<unsigned>((units + gy - 1) / gy);
+    if (gz > 65535) {
+        set_error_message("attn_decode: %lld (sequence, head group) units exceed the grid", units);
+        return ATTN_ERR_UNSUPPORTED;
+    }
     if (p.validate)
         check_pages_kernel<<<a.B, 128, 0, stream>>>(a.block_table, a.seq_lens, a.max_pages, a.num_pages,
                                                     dev.err_word);
@@ -582,7 +594,7 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
         if (cached) attr_set[dev.device].store(true, std::memory_order_release);
     }
     const int threads = 32 * (1 + HG * p.m_tiles);
-    dim3 grid(plan.max_chunks, a.B * plan.head_groups);
+    dim3 grid(plan.max_chunks, gy, gz);
     attn_decode_split_kernel<HD><<<grid, threads, smem, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {

@@ -160,3 +160,17 @@ def test_full_size_spec_decode(la):
     go, gl = gpu_rows(p, out.cpu(), lse.cpu())
     stats = assert_close(p.name, go, gl, ref_o, ref_lse)
     print(p.name, stats)
+
+
+def test_more_sequences_than_one_grid_dimension(la):
+    """70,000 sequences, two new tokens each with the append: the split
+    kernel's units run over two grid dimensions; outputs and the cache after
+    the append against the oracle."""
+    g = torch.Generator().manual_seed(2010)
+    lens = torch.randint(2, 41, (70_000,), generator=g).tolist()
+    num_pages = sum(-(-L // 16) for L in lens) + 5
+    p = workloads.make_kvcache_decode(lens, 2, 4, 1, 64, num_pages=num_pages, seed=2011, causal=True, append=True)
+    # V/4 (exact in bf16): rows over a few keys keep |O| below 2, where the
+    # 1e-2 bound is larger than a bf16 output's rounding
+    p = dataclasses.replace(p, v_cache=p.v_cache * 0.25, v_new=p.v_new * 0.25)
+    check(la, p)
