@@ -100,11 +100,12 @@ __global__ void __launch_bounds__(288, 1) attn_decode_split_kernel(const __grid_
     // soon as every CTA here has started; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int chunk = blockIdx.x;
-    // (sequence, head group) units run over grid y and z (y at most 65535)
-    const long long unit = static_cast<long long>(blockIdx.z) * gridDim.y + blockIdx.y;
-    if (unit >= static_cast<long long>(p.B) * p.head_groups) return;  // padding of the last z slice
-    const int b = static_cast<int>(unit / p.head_groups);
-    const int hg = static_cast<int>(unit - static_cast<long long>(b) * p.head_groups);
+    // (sequence, head group) units run over grid y and z (y at most 65535;
+    // the host keeps B * head_groups below 2^31)
+    const int unit = static_cast<int>(blockIdx.z * gridDim.y + blockIdx.y);
+    if (unit >= p.B * p.head_groups) return;  // padding of the last z slice
+    const int b = unit / p.head_groups;
+    const int hg = unit - b * p.head_groups;
     const int cap = p.max_pages * kPage;
     const int len = min(max(__ldg(p.seq_lens + b), 0), cap);
     const int tok0 = chunk * p.pages_per_chunk * kPage;
@@ -561,7 +562,7 @@ attn_status launch_typed(const DecodeArgs& a, const DecodePlan& plan, const Devi
     const long long units = static_cast<long long>(a.B) * plan.head_groups;
     const unsigned gy = static_cast<unsigned>(std::min<long long>(std::max<long long>(units, 1), 65535));
     const unsigned gz = static_cast<unsigned>((units + gy - 1) / gy);
-    if (gz > 65535) {
+    if (gz > 65535 || units > 0x7fffffffLL) {
         set_error_message("attn_decode: %lld (sequence, head group) units exceed the grid", units);
         return ATTN_ERR_UNSUPPORTED;
     }
