@@ -137,3 +137,14 @@ def test_more_sequences_than_one_grid_dimension(la):
     # (exact in bf16) keeps the bound meaningful
     dd = dataclasses.replace(dd, v_cache=dd.v_cache * 0.25)
     check(la, dd)
+
+
+def test_million_token_context(la):
+    """Sequences of 1,000,000 and 300,000 tokens (MQA 8:1): the plan cuts
+    the long one into about 245 chunks, more than the combine takes in one
+    round (128), so its rounds and the split at that scale are covered;
+    every row against the oracle."""
+    lens = [1_000_000, 300_000]
+    num_pages = sum(-(-L // 16) for L in lens) + 3
+    dd = workloads.make_decode(lens, 8, 1, 128, num_pages=num_pages, seed=2110)
+    check(la, dd)

@@ -1,4 +1,6 @@
 """GPU parity of attn_fwd against the fp64 oracle (through the C ABI)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -186,3 +188,22 @@ def test_varlen_thousands_of_sequences_every_row_written(la):
     ref_o, ref_lse = oracle.prefill(p, rows.numpy())
     go, gl = gather_prefill(p, out, lse, rows.numpy())
     assert_close(p.name, go, gl, ref_o, ref_lse)
+
+
+def test_long_sequence_65536(la):
+    """One causal sequence of 65,536 tokens (GQA 8:2, q doubled for larger
+    logits and more rescales): the last rows run the recurrence over all
+    512 K/V tiles.  Rows at both ends, around tile boundaries, in the
+    middle, and seeded draws, against the oracle."""
+    N, Hq, Hkv, d = 65536, 8, 2, 128
+    p = workloads.make_prefill(1, Hq, Hkv, N, N, d, causal=True, seed=2100)
+    p = dataclasses.replace(p, q=(p.q.float() * 2.0).to(torch.bfloat16))
+    out, lse = run_prefill(la, p)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(2101)
+    fixed = [0, 1, 127, 128, 129, N // 2 - 1, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rows = [(0, h, i) for h in range(Hq) for i in sorted(set(fixed + torch.randint(0, N, (12,), generator=g).tolist()))]
+    rows = np.asarray(rows, dtype=np.int32)
+    ref_o, ref_lse = oracle.prefill(p, rows)
+    go, gl = gather_prefill(p, out, lse, rows)
+    print(assert_close("long_65536", go, gl, ref_o, ref_lse))
