@@ -14,7 +14,8 @@ Prefill throughput is TFLOP/s of exact attended query-key pairs x 4 x d
 (causal-adjusted); decode bandwidth is GB/s of algorithmic bytes (every K/V
 row the sequences own, read once, plus q, out, lse and the block-table rows).
 Every call is timed with CUDA events on the launching stream; L2 is flushed
-(a 256 MB write) at the start of each step, outside the timed calls.  Each
+at the start of each step, outside the timed calls: a 256 MB write, then a
+256 MB read that writes the flush's dirty lines back before the call starts.  Each
 configuration gets its own roofline record and, on rank 0 with one GPU, an
 accuracy record against the fp64 oracle on a seeded row sample (the CPU
 baseline leg).  After the step, the next rows (backward, local window,
@@ -579,13 +580,34 @@ class DecodeCall:
         return host_in, compute, shapes, "decode queries (and new K/V rows) copied each step; the paged cache stays resident"
 
 
+class L2Flush:
+    """Run between steps, outside the timed calls.  A 256 MB write evicts
+    every input from the 126 MB L2; a 256 MB read of a second buffer then
+    evicts the write's dirty lines, so their write-back happens here and not
+    inside the next timed call (a short HBM-bound call, such as the 300 MB
+    quantization, would otherwise pay for up to an L2's worth of it)."""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1)
+        torch.amax(self.r, dim=0, out=self.sink)
+
+
+L2_NOTE = ("flushed between steps (256 MB write, then a 256 MB read so the write's dirty lines are written back; "
+           "outside the timed calls)")
+
+
 def time_calls(calls, steps, warmup, stream, flush, sampler=None):
-    """W untimed steps, then `steps` timed ones.  A step flushes L2 (a 256 MB
-    write) and runs every call once; each call is bracketed by CUDA events on
+    """W untimed steps, then `steps` timed ones.  A step flushes L2
+    (L2Flush) and runs every call once; each call is bracketed by CUDA events on
     the launching stream.  Returns (ms per call per step, wall seconds and
     host window of the timed region)."""
     def step(ev=None):
-        flush.fill_(1)
+        flush()
         for c, fn in enumerate(calls):
             if ev is not None:
                 ev[c][0].record(stream)
@@ -742,7 +764,7 @@ def main(argv=None):
         prefills, decode = make_workloads(args.workload, dev)
         calls = [PrefillCall(la, p, dev) for p in prefills] + ([DecodeCall(la, decode, dev)] if decode else [])
     head = calls[0]   # the headline: the largest prefill configuration (or the one workload asked for)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     barrier(world)
     with ClockSampler(local) as clocks:   # started before the warm-up
@@ -774,8 +796,7 @@ def main(argv=None):
                           "frac_of_8TBs": dval / world / NOMINAL["hbm_gbs"]}
     line["gpu_launches"] = args.steps * sum(c.launches for c in calls)
     line["config"] = {"workload": " + ".join(c.name for c in calls), "headline": head.name,
-                      "l2": "flushed between steps (256 MB write, outside the timed calls); every input is also "
-                            "larger than L2",
+                      "l2": L2_NOTE + "; every input is also larger than L2",
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                       "calls": {c.name: c.describe() for c in calls}}
     line["clocks"] = clocks.record(*window)
@@ -820,10 +841,10 @@ def run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind):
     ws = torch.empty(la.lib().attn_bwd_workspace_size(p.B, p.Hq, p.Nq, 0), dtype=torch.uint8, device=dev)
     kw = dict(causal=p.causal, scale=p.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
     flops = backward_flops(p)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step(ev=None):
-        flush.fill_(1)
+        flush()
         if ev is not None:
             ev[0].record(stream)
         la.attn_bwd(q, k, v, out, lse, g, **kw)
@@ -864,7 +885,7 @@ def run_backward(args, la, dev, stream, world, rank, local, peaks, peaks_kind):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) rounded to bf16)",
             "value": value, "unit": "TFLOP/s", "roofline": roof, "ms_per_step": tot / args.steps,
             "gpu_launches": 3 * args.steps,
-            "config": {"workload": p.name + "_backward", "l2": "flushed between steps (256 MB write, outside the timed calls)",
+            "config": {"workload": p.name + "_backward", "l2": L2_NOTE,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "prefill": {"B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "Nq": p.Nq, "Nk": p.Nk, "d": p.d,
                                    "causal": p.causal}},
@@ -1002,7 +1023,7 @@ class BwdCall:
 
 class Fp8Call(PrefillCall):
     """attn_fwd_fp8 on the per-tile E4M3 quantization of a prefill problem
-    (quantized on the device by attn_quantize_fp8 before timing).  Work is
+    (quantized on the device by attn_quantize_fp8_qkv before timing).  Work is
     the same 4 d FLOP per attended pair; the S product runs at the 8-bit rate
     and the PV product at the 16-bit rate, so the peak for this kernel is
     4/3 of the bf16 peak (half the FLOPs at twice the rate)."""
@@ -1012,11 +1033,8 @@ class Fp8Call(PrefillCall):
         super().__init__(la, p, dev)
         self.name = p.name + "_fp8"
         q, k, v = self.args
-        kw = dict(cu_seqlens=self.kw["cu_seqlens_q"]) if p.varlen else {}
-        kwk = dict(cu_seqlens=self.kw["cu_seqlens_k"]) if p.varlen else {}
-        self.q8, self.qs = la.attn_quantize_fp8(q, **kw)
-        self.k8, self.ks = la.attn_quantize_fp8(k, **kwk)
-        self.v8, self.vs = la.attn_quantize_fp8(v, **kwk)
+        kw = dict(cu_seqlens_q=self.kw["cu_seqlens_q"], cu_seqlens_k=self.kw["cu_seqlens_k"]) if p.varlen else {}
+        (self.q8, self.qs), (self.k8, self.ks), (self.v8, self.vs) = la.attn_quantize_fp8_qkv(q, k, v, **kw)
         self.fkw = {x: y for x, y in self.kw.items() if x != "window"}
         self.peak_note = (f"{peaks_kind} bf16 burst x 4/3 (S at the 8-bit rate, nominally 2x bf16; "
                           "PV at the 16-bit rate)")
@@ -1038,9 +1056,9 @@ class Fp8Call(PrefillCall):
 
 
 class QuantizeCall:
-    """attn_quantize_fp8 on q, k and v of a prefill problem (three launches):
+    """attn_quantize_fp8_qkv on q, k and v of a prefill problem (one launch):
     every bf16 element read once, every code written once, plus the scales."""
-    kind, kernel, unit, unit_scale, launches, bound = "quantize", "attn_quantize_fp8", "GB/s", 1e-9, 3, "hbm"
+    kind, kernel, unit, unit_scale, launches, bound = "quantize", "attn_quantize_fp8", "GB/s", 1e-9, 1, "hbm"
 
     def __init__(self, la, p, dev):
         self.la, self.p, self.name = la, p, p.name + "_quantize_fp8"
@@ -1057,19 +1075,21 @@ class QuantizeCall:
 
     def __call__(self):
         p = self.p
-        for x, cu, (o8, osc) in zip(self.xs, self.cu, self.outs):
-            if p.varlen:
-                self.la.attn_quantize_fp8(x, cu_seqlens=cu, out=o8, scale=osc)
-            else:
-                T, H, d = x.shape
-                self.la.attn_quantize_fp8(x.view(p.B, T // p.B, H, d), out=o8.view(p.B, T // p.B, H, d), scale=osc)
+        outs = tuple(o8 for o8, _ in self.outs)
+        scales = tuple(osc for _, osc in self.outs)
+        if p.varlen:
+            self.la.attn_quantize_fp8_qkv(*self.xs, cu_seqlens_q=self.cu[0], cu_seqlens_k=self.cu[1], out=outs,
+                                          scales=scales)
+        else:
+            xs = [x.view(p.B, x.shape[0] // p.B, *x.shape[1:]) for x in self.xs]
+            self.la.attn_quantize_fp8_qkv(*xs, out=tuple(o.view(x.shape) for o, x in zip(outs, xs)), scales=scales)
 
     def describe(self):
         return {"B": self.p.B, "tokens_q": int(self.xs[0].shape[0]), "tokens_k": int(self.xs[1].shape[0]),
                 "Hq": self.p.Hq, "Hkv": self.p.Hkv, "d": self.p.d}
 
     def roofline_extra(self):
-        return {"bytes_per_call": self.units, "launches_per_call": 3}
+        return {"bytes_per_call": self.units, "launches_per_call": 1}
 
 
 def measure_next_rows(la, dev, stream, flush, steps, warmup, peaks, peaks_kind):

@@ -9,7 +9,8 @@ CUDA device, the calls raise.
     out, lse = attn_fwd(q, k, v, causal=True)                       # dense THD/BSHD
     out, lse = attn_fwd(q, k, v, causal=True, cu_seqlens_q=cq, cu_seqlens_k=ck)
     dq, dk, dv = attn_bwd(q, k, v, out, lse, dout, causal=True)
-    q8, qs = attn_quantize_fp8(q); ...; out, lse = attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)
+    (q8, qs), (k8, ks), (v8, vs) = attn_quantize_fp8_qkv(q, k, v)  # one launch
+    out, lse = attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True)
     out, lse = attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens)
     out, lse = attn_decode_kvcache(q, k_cache, v_cache, block_table, seq_lens, k_new=kn, v_new=vn)
 """
@@ -28,6 +29,7 @@ from ._binding import (  # noqa: F401
     attn_decode_paged_noalloc,
     attn_decode_workspace_size,
     attn_quantize_fp8,
+    attn_quantize_fp8_qkv,
     attn_fp8_scale_count,
     attn_fwd,
     attn_fwd_fp8,

@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.attn_fp8_scale_count.restype = Z
             L.attn_quantize_fp8.argtypes = [P, P, P, I, I, I, I, P, P]
             L.attn_quantize_fp8.restype = I
+            L.attn_quantize_fp8_qkv.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
+            L.attn_quantize_fp8_qkv.restype = I
             L.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, P]
             L.attn_fwd_fp8.restype = I
             L.attn_fwd_fp8_window.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, P, P, P]
@@ -215,6 +217,57 @@ def attn_quantize_fp8(x: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = N
     _check(lib().attn_quantize_fp8(_ptr(x), _ptr(out), _ptr(scale), B, H, N, d, _ptr(cu_seqlens),
                                    _stream_handle(stream)))
     return out, scale
+
+
+def attn_quantize_fp8_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
+                          cu_seqlens_q: Optional[torch.Tensor] = None, cu_seqlens_k: Optional[torch.Tensor] = None,
+                          out: Optional[tuple] = None, scales: Optional[tuple] = None, stream=None):
+    """attn_quantize_fp8 of q, k and v in one launch (bit-identical to three
+    calls).  Dense: q [B, Nq, Hq, d], k and v [B, Nk, Hkv, d]; packed: q
+    [T_q, Hq, d], k and v [T_k, Hkv, d] with both int32 cu_seqlens.  out and
+    scales, if given, are (q8, k8, v8) and (q_scale, k_scale, v_scale).
+    Returns ((q8, q_scale), (k8, k_scale), (v8, v_scale))."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    if (cu_seqlens_q is None) != (cu_seqlens_k is None):
+        raise ValueError("give both cu_seqlens or neither")
+    if cu_seqlens_q is not None:
+        _need(cu_seqlens_q, "cu_seqlens_q", torch.int32)
+        _need(cu_seqlens_k, "cu_seqlens_k", torch.int32)
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("packed mode takes q [T_q, Hq, d] and k, v [T_k, Hkv, d]")
+        B = int(cu_seqlens_q.numel()) - 1
+        if int(cu_seqlens_k.numel()) - 1 != B:
+            raise ValueError("cu_seqlens_q and cu_seqlens_k must describe the same batch")
+        Nq, Hq, d = (int(x) for x in q.shape)
+        Nk, Hkv = int(k.shape[0]), int(k.shape[1])
+        Tq, Tk = Nq, Nk
+    else:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense mode takes q [B, Nq, Hq, d] and k, v [B, Nk, Hkv, d]")
+        B, Nq, Hq, d = (int(x) for x in q.shape)
+        if int(k.shape[0]) != B:
+            raise ValueError("q and k must have the same batch")
+        Nk, Hkv = int(k.shape[1]), int(k.shape[2])
+        Tq, Tk = B * Nq, B * Nk
+    if int(k.shape[-1]) != d:
+        raise ValueError("q and k must have the same head_dim")
+    if out is None:
+        out = tuple(torch.empty(x.shape, dtype=torch.uint8, device=x.device) for x in (q, k, v))
+    if scales is None:
+        scales = (torch.zeros((Hq, attn_fp8_scale_count(B, Tq)), dtype=torch.float32, device=q.device),
+                  torch.zeros((Hkv, attn_fp8_scale_count(B, Tk)), dtype=torch.float32, device=q.device),
+                  torch.zeros((Hkv, attn_fp8_scale_count(B, Tk)), dtype=torch.float32, device=q.device))
+    for t, n in zip(out, ("q8", "k8", "v8")):
+        _need(t, n, torch.uint8)
+    for t, n in zip(scales, ("q_scale", "k_scale", "v_scale")):
+        _need(t, n, torch.float32)
+    _check(lib().attn_quantize_fp8_qkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out[0]), _ptr(out[1]), _ptr(out[2]),
+                                       _ptr(scales[0]), _ptr(scales[1]), _ptr(scales[2]), B, Hq, Hkv, Nq, Nk, d,
+                                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _stream_handle(stream)))
+    return (out[0], scales[0]), (out[1], scales[1]), (out[2], scales[2])
 
 
 def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: torch.Tensor,

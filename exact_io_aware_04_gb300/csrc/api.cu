@@ -230,7 +230,44 @@ attn_status attn_quantize_fp8(const void* x, void* x8, float* x_scale, int B, in
     a.N = N;
     a.d = d;
     a.cu = cu_seqlens;
-    return launch_quantize_fp8(a, static_cast<cudaStream_t>(stream));
+    return launch_quantize_fp8(&a, 1, static_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_quantize_fp8_qkv(const void* q, const void* k, const void* v, void* q8, void* k8, void* v8,
+                                  float* q_scale, float* k_scale, float* v_scale, int B, int Hq, int Hkv, int Nq,
+                                  int Nk, int d, const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream) {
+    if (!q || !q8 || !q_scale) return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8_qkv: NULL pointer");
+    if ((!k || !v || !k8 || !v8 || !k_scale || !v_scale) && Nk > 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8_qkv: NULL k/v pointer with keys present");
+    if ((cu_seqlens_q == nullptr) != (cu_seqlens_k == nullptr))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8_qkv: give both cu_seqlens or neither");
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Nq < 0 || Nk < 0)
+        return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8_qkv: bad size");
+    if (d != 64 && d != 128)
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_quantize_fp8_qkv: head_dim %d (built: 64, 128)", d);
+    const bool keys = Nk > 0;
+    if (!aligned16(q) || !aligned16(q8) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) != 0 ||
+        (keys && (!aligned16(k) || !aligned16(v) || !aligned16(k8) || !aligned16(v8) ||
+                  (reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)))
+        return fail(ATTN_ERR_INVALID_ARG, "attn_quantize_fp8_qkv: misaligned pointer");
+    if (!cu_seqlens_q && (static_cast<long long>(B) * Nq > INT32_MAX || static_cast<long long>(B) * Nk > INT32_MAX))
+        return fail(ATTN_ERR_UNSUPPORTED, "attn_quantize_fp8_qkv: more than 2^31 tokens");
+    QuantArgs a[3];
+    const void* src[3] = {q, k, v};
+    void* dst[3] = {q8, k8, v8};
+    float* sc[3] = {q_scale, k_scale, v_scale};
+    const int n = keys ? 3 : 1;
+    for (int i = 0; i < n; ++i) {
+        a[i].x = src[i];
+        a[i].x8 = dst[i];
+        a[i].scale = sc[i];
+        a[i].B = B;
+        a[i].H = i == 0 ? Hq : Hkv;
+        a[i].N = i == 0 ? Nq : Nk;
+        a[i].d = d;
+        a[i].cu = i == 0 ? cu_seqlens_q : cu_seqlens_k;
+    }
+    return launch_quantize_fp8(a, n, static_cast<cudaStream_t>(stream));
 }
 
 attn_status attn_fwd_fp8_window(const void* q8, const void* k8, const void* v8, const float* q_scale,

@@ -74,7 +74,9 @@ struct QuantArgs {
     int B, H, N, d;      // N: tokens per sequence (dense) or T (packed)
     const int* cu;       // int32 [B + 1] or NULL (dense)
 };
-attn_status launch_quantize_fp8(const QuantArgs& a, cudaStream_t stream);
+// Quantizes n (1..kMaxQuantTensors) tensors of the same head_dim in one launch.
+constexpr int kMaxQuantTensors = 3;
+attn_status launch_quantize_fp8(const QuantArgs* a, int n, cudaStream_t stream);
 
 struct BwdArgs {
     const void *q, *k, *v, *out, *dout;  // out = the forward output O, dout = dL/dO

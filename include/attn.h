@@ -165,6 +165,33 @@ attn_status attn_quantize_fp8(const void *x, void *x8, float *x_scale,
                               const int *cu_seqlens, void *stream);
 
 /*
+ * attn_quantize_fp8_qkv -- attn_quantize_fp8 of q, k and v in one launch.
+ *
+ * Operation: exactly three attn_quantize_fp8 calls -- q with (B, Hq, Nq,
+ * cu_seqlens_q), k and v with (B, Hkv, Nk, cu_seqlens_k) -- with
+ * bit-identical codes and scales; one kernel launch does all three, which
+ * saves the launch gaps and the thin tails of the two smaller tensors.  This
+ * is the preparation attn_fwd_fp8 needs ("FP8 Path and Quantization": Q, K
+ * and V are quantized per tile).
+ *
+ * Layout: q [T_q, Hq, d], k and v [T_k, Hkv, d] bf16; q8, k8, v8 the E4M3
+ * codes shaped alike; q_scale [Hq, attn_fp8_scale_count(B, T_q)], k_scale
+ * and v_scale [Hkv, attn_fp8_scale_count(B, T_k)] fp32.  T and the
+ * cu_seqlens as attn_fwd_fp8 (dense: T = B * N; packed: give both
+ * cu_seqlens, Nq and Nk the totals).  d in {64, 128}.
+ * Rejects (ATTN_ERR_INVALID_ARG): NULL pointers (k, v, k8, v8, k_scale and
+ * v_scale may be NULL only when Nk == 0), only one cu_seqlens given, B < 0,
+ * head counts <= 0, Nq < 0, Nk < 0, tensors or codes not 16-byte aligned,
+ * scales not 4-byte aligned.  Nk == 0 quantizes q alone.
+ */
+attn_status attn_quantize_fp8_qkv(const void *q, const void *k, const void *v,
+                                  void *q8, void *k8, void *v8,
+                                  float *q_scale, float *k_scale, float *v_scale,
+                                  int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                                  const int *cu_seqlens_q, const int *cu_seqlens_k,
+                                  void *stream);
+
+/*
  * attn_fwd_fp8 -- prefill forward on per-tile 8-bit (E4M3) Q, K, V.
  *
  * Operation: attn_fwd (bottom-right causal corner, GQA, dense or packed) on

@@ -134,6 +134,19 @@ def test_fp8_host_rejections(lib):
     assert q(d=96) == -2
     assert q(B=0) == 0 and q(N=0) == 0                 # nothing to do
 
+    def qkv(q=FAKE, k=FAKE, q8=FAKE, ks=FAKE, B=2, Hq=4, Hkv=2, Nq=256, Nk=256, d=128, cq=None, ck=None):
+        return lib.attn_quantize_fp8_qkv(q, k, FAKE, q8, FAKE, FAKE, FAKE, ks, FAKE, B, Hq, Hkv, Nq, Nk, d, cq, ck,
+                                         None)
+    assert qkv(q=None) == -1 and qkv(q8=None) == -1
+    assert qkv(k=None) == -1                           # K needed when keys exist
+    assert qkv(k=None, ks=None, Nk=0, B=0) == 0        # no keys: K/V and their scales may be NULL
+    assert qkv(ks=ctypes.c_void_p(0x10002)) == -1      # scales must be 4-byte aligned
+    assert qkv(k=ctypes.c_void_p(0x10008)) == -1       # tensors must be 16-byte aligned
+    assert qkv(cq=FAKE) == -1                          # both cu_seqlens or neither
+    assert qkv(Hkv=0) == -1 and qkv(Nq=-1) == -1
+    assert qkv(d=96) == -2
+    assert qkv(B=0) == 0 and qkv(Nq=0, Nk=0) == 0      # nothing to do
+
     def f(q8=FAKE, k8=FAKE, ks=FAKE, B=1, Hq=4, Hkv=2, Nq=8, Nk=8, d=128, causal=1, cq=None, ck=None):
         return lib.attn_fwd_fp8(q8, k8, FAKE, FAKE, ks, FAKE, FAKE, FAKE, B, Hq, Hkv, Nq, Nk, d, 0.1, causal, cq,
                                 ck, None)

@@ -65,6 +65,108 @@ def test_quantize_packed_bit_exact(la):
     assert np.array_equal(got_s.view(np.uint32), ref_s.view(np.uint32))
 
 
+def gpu_quantize_qkv(la, q, k, v, B, Nq=None, Nk=None, cu_q=None, cu_k=None, sentinel=None):
+    """attn_quantize_fp8_qkv on host bf16 tensors [T, H, d]; returns host numpy
+    ((q codes, q scales), (k ...), (v ...)).  With `sentinel`, the scale arrays
+    start filled with it, so entries the call must leave alone can be checked."""
+    g = [x.to("cuda") for x in (q, k, v)]
+    scales = None
+    if sentinel is not None:
+        Tq, Tk = q.shape[0], k.shape[0]
+        scales = tuple(torch.full((x.shape[1], la.attn_fp8_scale_count(B, T)), sentinel, dtype=torch.float32,
+                                  device="cuda") for x, T in ((q, Tq), (k, Tk), (v, Tk)))
+    if cu_q is None:
+        res = la.attn_quantize_fp8_qkv(g[0].view(B, Nq, *q.shape[1:]), g[1].view(B, Nk, *k.shape[1:]),
+                                       g[2].view(B, Nk, *v.shape[1:]), scales=scales)
+    else:
+        res = la.attn_quantize_fp8_qkv(*g, cu_seqlens_q=cu_q.to("cuda"), cu_seqlens_k=cu_k.to("cuda"), scales=scales)
+    torch.cuda.synchronize()
+    return [(c.cpu().numpy().reshape(x.shape), sc.cpu().numpy()) for (c, sc), x in zip(res, (q, k, v))]
+
+
+def assert_quantized_equal(got, ref, what):
+    got_c, got_s = got
+    ref_c, ref_s = ref
+    assert np.array_equal(got_c, np.asarray(ref_c).reshape(got_c.shape)), f"{what}: codes differ"
+    assert np.array_equal(got_s.view(np.uint32), np.asarray(ref_s, dtype=np.float32).view(np.uint32)
+                          .reshape(got_s.shape)), f"{what}: scales differ"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_quantize_qkv_dense_bit_exact(la, d):
+    """One launch over q (Hq heads, Nq tokens) and k, v (Hkv heads, Nk
+    tokens) gives the oracle's codes and scales for each of the three."""
+    B, Nq, Nk, Hq, Hkv = 3, 300, 517, 6, 2
+    q = workloads.randn_bf16((B * Nq, Hq, d), seed=81)
+    k = workloads.randn_bf16((B * Nk, Hkv, d), seed=82)
+    v = (workloads.randn_bf16((B * Nk, Hkv, d), seed=83).float()
+         * torch.logspace(-5, 4, B * Nk)[:, None, None]).to(torch.bfloat16)
+    q[128:256, 4] = 0.0                       # an all-zero tile of one head
+    k[Nk + 3, 1, 5] = 400.0                   # an outlier
+    got = gpu_quantize_qkv(la, q, k, v, B, Nq=Nq, Nk=Nk)
+    for name, x, n, g in (("q", q, Nq, got[0]), ("k", k, Nk, got[1]), ("v", v, Nk, got[2])):
+        assert_quantized_equal(g, oracle.quantize_fp8(x, B=B, N=n), f"dense d={d} {name}")
+
+
+def test_quantize_qkv_packed_bit_exact_and_gaps_untouched(la):
+    """Packed sequences of unequal q and k lengths (some empty, some a single
+    token, some crossing many tiles); the scale entries between sequences keep
+    the sentinel."""
+    q_lens = [130, 1, 0, 257, 128, 3000, 5]
+    k_lens = [900, 64, 7, 0, 129, 3000, 1]
+    cq = torch.tensor([0] + list(np.cumsum(q_lens)), dtype=torch.int32)
+    ck = torch.tensor([0] + list(np.cumsum(k_lens)), dtype=torch.int32)
+    q = workloads.randn_bf16((int(cq[-1]), 8, 128), seed=84)
+    k = workloads.randn_bf16((int(ck[-1]), 2, 128), seed=85)
+    v = workloads.randn_bf16((int(ck[-1]), 2, 128), seed=86)
+    v[1000:1100, 0] *= 1e-30                  # tiny values: subnormal codes
+    sentinel = -7.0
+    got = gpu_quantize_qkv(la, q, k, v, len(q_lens), cu_q=cq, cu_k=ck, sentinel=sentinel)
+    for name, x, cu, g in (("q", q, cq, got[0]), ("k", k, ck, got[1]), ("v", v, ck, got[2])):
+        ref_c, ref_s = oracle.quantize_fp8(x, B=len(q_lens), cu=cu)
+        assert np.array_equal(g[0], np.asarray(ref_c).reshape(g[0].shape)), f"packed {name}: codes differ"
+        written = np.zeros(g[1].shape[1], dtype=bool)
+        for b in range(len(q_lens)):
+            first, last = int(cu[b]), int(cu[b + 1])
+            base = first // 128 + b
+            written[base:base + (last - first + 127) // 128] = True
+        assert np.array_equal(g[1][:, written].view(np.uint32),
+                              np.asarray(ref_s, dtype=np.float32)[:, written].view(np.uint32)), \
+            f"packed {name}: scales differ"
+        assert (g[1][:, ~written] == sentinel).all(), f"packed {name}: an entry between sequences was written"
+
+
+def test_quantize_qkv_many_short_sequences(la):
+    """2,000 packed sequences of 0-300 tokens: many more (entry, head) units
+    than CTAs, with gaps between sequences everywhere."""
+    gen = torch.Generator().manual_seed(87)
+    lens = torch.randint(0, 301, (2000,), generator=gen).tolist()
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    q = workloads.randn_bf16((int(cu[-1]), 4, 64), seed=88)
+    k = workloads.randn_bf16((int(cu[-1]), 1, 64), seed=89)
+    v = workloads.randn_bf16((int(cu[-1]), 1, 64), seed=90)
+    got = gpu_quantize_qkv(la, q, k, v, len(lens), cu_q=cu, cu_k=cu)
+    for name, x, g in (("q", q, got[0]), ("k", k, got[1]), ("v", v, got[2])):
+        ref_c, ref_s = oracle.quantize_fp8(x, B=len(lens), cu=cu)
+        assert np.array_equal(g[0], np.asarray(ref_c).reshape(g[0].shape)), f"{name}: codes differ"
+        for b in range(0, len(lens), 97):       # every 97th sequence's entries
+            first, last = int(cu[b]), int(cu[b + 1])
+            base, n = first // 128 + b, (last - first + 127) // 128
+            assert np.array_equal(g[1][:, base:base + n].view(np.uint32),
+                                  np.asarray(ref_s, dtype=np.float32)[:, base:base + n].view(np.uint32)), name
+
+
+def test_quantize_qkv_no_keys(la):
+    """Nk == 0 quantizes q alone; k, v and their codes may be empty."""
+    q = workloads.randn_bf16((2 * 200, 4, 128), seed=91)
+    g = q.to("cuda").view(2, 200, 4, 128)
+    e = torch.empty((2, 0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    (q8, qs), _, _ = la.attn_quantize_fp8_qkv(g, e, e)
+    torch.cuda.synchronize()
+    assert_quantized_equal((q8.cpu().numpy().reshape(q.shape), qs.cpu().numpy()),
+                           oracle.quantize_fp8(q, B=2, N=200), "q alone")
+
+
 def fp8_inputs(p, device="cuda"):
     """The oracle's codes and scales of a prefill problem, uploaded, as
     attn_fwd_fp8 arguments; and the quantized dict for the oracle."""
@@ -169,9 +271,7 @@ def test_quantize_then_forward_end_to_end(la):
     the same bf16 inputs itself."""
     p = workloads.make_varlen([300, 77], [900, 77], 8, 2, 128, causal=True, seed=67)
     g = p.to("cuda")
-    q8, qs = la.attn_quantize_fp8(g.q, cu_seqlens=g.cu_q)
-    k8, ks = la.attn_quantize_fp8(g.k, cu_seqlens=g.cu_k)
-    v8, vs = la.attn_quantize_fp8(g.v, cu_seqlens=g.cu_k)
+    (q8, qs), (k8, ks), (v8, vs) = la.attn_quantize_fp8_qkv(g.q, g.k, g.v, cu_seqlens_q=g.cu_q, cu_seqlens_k=g.cu_k)
     out, lse = la.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, scale=p.scale, cu_seqlens_q=g.cu_q,
                                cu_seqlens_k=g.cu_k)
     torch.cuda.synchronize()
@@ -286,15 +386,17 @@ def test_quantize_full_size_bit_exact(la, name):
     for bit against the oracle's codes and scales."""
     p = getattr(workloads, name)()
     qz = oracle.quantize_problem_fp8(p)
-    for key, x, n in (("q", p.q, p.Nq), ("k", p.k, p.Nk), ("v", p.v, p.Nk)):
-        ref_c, ref_s = qz[key]
+    if p.varlen:
+        qkv = gpu_quantize_qkv(la, p.q, p.k, p.v, p.B, cu_q=p.cu_q, cu_k=p.cu_k)
+    else:
+        qkv = gpu_quantize_qkv(la, p.q, p.k, p.v, p.B, Nq=p.Nq, Nk=p.Nk)
+    for i, (key, x, n) in enumerate((("q", p.q, p.Nq), ("k", p.k, p.Nk), ("v", p.v, p.Nk))):
         if p.varlen:
-            got_c, got_s = gpu_quantize(la, x, p.B, cu=p.cu_q if key == "q" else p.cu_k)
+            one = gpu_quantize(la, x, p.B, cu=p.cu_q if key == "q" else p.cu_k)
         else:
-            got_c, got_s = gpu_quantize(la, x, p.B, N=n)
-        assert np.array_equal(got_c, np.asarray(ref_c).reshape(got_c.shape)), f"{name} {key}: codes differ"
-        assert np.array_equal(got_s.view(np.uint32), np.asarray(ref_s).view(np.uint32).reshape(got_s.shape)), \
-            f"{name} {key}: scales differ"
+            one = gpu_quantize(la, x, p.B, N=n)
+        assert_quantized_equal(one, qz[key], f"{name} {key}")
+        assert_quantized_equal(qkv[i], qz[key], f"{name} {key} (one launch for q, k, v)")
 
 
 @pytest.mark.parametrize("window,causal", [((100, -1), True), ((40, 25), False), ((0, 0), False), ((300, 300), False)])

@@ -81,6 +81,30 @@ def test_quantizer_packed_stays_inside_its_buffers(la, bad):
         assert bool((scales[H * n_scale:] == -7.0).all()), "a scale was written past the array"
 
 
+@pytest.mark.parametrize("bad", sorted(BAD_CU))
+def test_quantizer_qkv_packed_stays_inside_its_buffers(la, bad):
+    """The one-launch q, k, v quantizer with malformed offsets for the keys:
+    nothing is written past any of the six outputs."""
+    T, Hq, Hkv, d = 500, 4, 2, 128
+    cu_ok = torch.tensor([0, 100, 300, 500], dtype=torch.int32, device="cuda")
+    cu = torch.tensor(BAD_CU[bad], dtype=torch.int32, device="cuda")
+    B = cu.numel() - 1
+    n_scale = la.attn_fp8_scale_count(B, T)
+    xs = [workloads.randn_bf16((T, H, d), seed=1940 + i).cuda() for i, H in enumerate((Hq, Hkv, Hkv))]
+    codes = [torch.full((T + 256, H, d), 0x5A, dtype=torch.uint8, device="cuda") for H in (Hq, Hkv, Hkv)]
+    scales = [torch.full((H * n_scale + 256,), -7.0, dtype=torch.float32, device="cuda") for H in (Hq, Hkv, Hkv)]
+
+    def quant():
+        la.attn_quantize_fp8_qkv(*xs, cu_seqlens_q=cu_ok, cu_seqlens_k=cu, out=tuple(c[:T] for c in codes),
+                                 scales=tuple(s[:H * n_scale].view(H, n_scale) for s, H in zip(scales, (Hq, Hkv, Hkv))))
+    for on in (True, False):
+        st = with_validation(la, on, quant)
+        assert st == (la.ATTN_ERR_BAD_INDEX if on else la.ATTN_OK)
+        for c, s, H in zip(codes, scales, (Hq, Hkv, Hkv)):
+            assert bool((c[T:] == 0x5A).all()), "a code was written past the tensor"
+            assert bool((s[H * n_scale:] == -7.0).all()), "a scale was written past the array"
+
+
 def test_decode_lengths_past_the_table(la):
     dd = workloads.make_decode([100, 300, 50], 8, 2, 128, num_pages=64, seed=1920).to("cuda")
     lens = torch.tensor([100, 300 + 16 * 64, 50], dtype=torch.int32, device="cuda")   # beyond max_pages * 16
