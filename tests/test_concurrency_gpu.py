@@ -4,9 +4,10 @@ A serving process overlaps prefill, decode and training work on separate
 streams, often from separate threads.  The library's host state is a
 thread-local error message, a mutex-guarded device-info cache and atomic
 launch-attribute flags; its kernels share nothing but the device error word.
-Three threads each loop over one call (prefill, paged decode, backward) on
-their own stream, and every result must equal a single-threaded reference
-bit for bit (the kernels are deterministic)."""
+Four threads each loop over one call (prefill, paged decode, backward, and
+the 8-bit path: quantization of q, k, v then the 8-bit forward) on their own
+stream, and every result must equal a single-threaded reference bit for bit
+(the kernels are deterministic)."""
 import threading
 
 import pytest
@@ -26,7 +27,7 @@ def la():
     assert m.attn_get_device_status() == 0
 
 
-def test_three_threads_three_streams(la):
+def test_four_threads_four_streams(la):
     p = workloads.make_prefill(2, 16, 4, 700, 900, 128, causal=True, seed=1800).to("cuda")
     q = p.q.view(2, 700, 16, 128)
     k = p.k.view(2, 900, 4, 128)
@@ -47,7 +48,12 @@ def test_three_threads_three_streams(la):
     def backward():
         return la.attn_bwd(q, k, v, out0, lse0, g, causal=True, scale=scale)
 
-    calls = {"prefill": prefill, "decode": decode, "backward": backward}
+    def fp8():
+        (q8, qs), (k8, ks), (v8, vs) = la.attn_quantize_fp8_qkv(q, k, v)
+        o, l = la.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, scale=scale)
+        return q8, qs, k8, ks, v8, vs, o, l
+
+    calls = {"prefill": prefill, "decode": decode, "backward": backward, "fp8": fp8}
     refs = {name: [t.clone() for t in fn()] for name, fn in calls.items()}
     torch.cuda.synchronize()
     errors = []

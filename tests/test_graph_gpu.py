@@ -151,3 +151,49 @@ def test_noalloc_decode_in_a_graph(la):
         ref_o, ref_l = la.attn_decode_paged(q, g_.k_cache, g_.v_cache, g_.block_table, g_.seq_lens)
         torch.cuda.synchronize()
         assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+
+
+def test_quantize_and_fp8_forward_in_one_graph(la):
+    """The 8-bit path as a serving step: q, k, v quantized in one launch, then
+    the 8-bit forward, captured once and replayed on new bf16 inputs.  Each
+    replay's codes and scales equal the oracle's bit for bit, and its output
+    meets the forward tolerances against the oracle on those codes."""
+    B, Hq, Hkv, Nq, Nk, d = 2, 8, 2, 300, 700, 128
+    shp_q, shp_k = (B, Nq, Hq, d), (B, Nk, Hkv, d)
+    q = torch.empty(shp_q, dtype=torch.bfloat16, device="cuda")
+    k = torch.empty(shp_k, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    codes = tuple(torch.empty(x.shape, dtype=torch.uint8, device="cuda") for x in (q, k, v))
+    scales = (torch.zeros((Hq, la.attn_fp8_scale_count(B, B * Nq)), dtype=torch.float32, device="cuda"),
+              torch.zeros((Hkv, la.attn_fp8_scale_count(B, B * Nk)), dtype=torch.float32, device="cuda"),
+              torch.zeros((Hkv, la.attn_fp8_scale_count(B, B * Nk)), dtype=torch.float32, device="cuda"))
+    out, lse = torch.empty_like(q), torch.empty((B, Hq, Nq), dtype=torch.float32, device="cuda")
+    scale = d ** -0.5
+
+    def step():
+        la.attn_quantize_fp8_qkv(q, k, v, out=codes, scales=scales)
+        la.attn_fwd_fp8(*codes, *scales, causal=True, scale=scale, out=out, lse=lse)
+
+    def load(seed):
+        p = workloads.make_prefill(B, Hq, Hkv, Nq, Nk, d, causal=True, seed=seed)
+        q.copy_(p.q.view(shp_q))
+        k.copy_(p.k.view(shp_k))
+        v.copy_(p.v.view(shp_k))
+        return p
+
+    load(1800)
+    g = capture(step)
+    for rep in range(3):
+        p = load(1810 + 10 * rep)
+        g.replay()
+        torch.cuda.synchronize()
+        qz = oracle.quantize_problem_fp8(p)
+        for name, c, sc in zip(("q", "k", "v"), codes, scales):
+            ref_c, ref_s = qz[name]
+            assert np.array_equal(c.cpu().numpy().reshape(np.asarray(ref_c).shape), ref_c), f"replay {rep} {name}"
+            assert np.array_equal(sc.cpu().numpy().view(np.uint32),
+                                  np.asarray(ref_s, dtype=np.float32).view(np.uint32)), f"replay {rep} {name}"
+        rows = oracle.all_rows(p)
+        ref_o, ref_lse = oracle.prefill_fp8(p, rows, quantized=qz)
+        go, gl = gather_prefill(p, out, lse, rows)
+        assert_close(f"fp8 graph replay {rep}", go, gl, ref_o, ref_lse)
