@@ -143,3 +143,28 @@ def test_backward(la, i):
 def test_fp8_forward(la, i):
     from test_fp8_gpu import check_fp8
     check_fp8(la, prefill_case(i, fp8=True))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_quantize_qkv(la, i):
+    """The one-launch q, k, v quantizer on the sweep's prefill shapes (d = 64
+    or 128, dense or packed with empty sequences), bit for bit against the
+    oracle's codes and scales, with a tile of zeros and a spread of
+    magnitudes across the tokens drawn in."""
+    r = np.random.RandomState(8800 + i)
+    p = prefill_case(i + 100)
+    tq, tk = p.q.shape[0], p.k.shape[0]
+    spread = torch.from_numpy(10.0 ** r.uniform(-6, 4, size=(tq, 1, 1))).float()
+    q = (p.q.float() * spread).to(torch.bfloat16)
+    v = p.v.clone()
+    if tk > 130:
+        v[128:256 if tk >= 256 else tk, int(r.randint(0, p.Hkv))] = 0.0
+    from test_fp8_gpu import gpu_quantize_qkv, assert_quantized_equal
+    if p.varlen:
+        got = gpu_quantize_qkv(la, q, p.k, v, p.B, cu_q=p.cu_q, cu_k=p.cu_k)
+        seq = [dict(B=p.B, cu=p.cu_q), dict(B=p.B, cu=p.cu_k), dict(B=p.B, cu=p.cu_k)]
+    else:
+        got = gpu_quantize_qkv(la, q, p.k, v, p.B, Nq=p.Nq, Nk=p.Nk)
+        seq = [dict(B=p.B, N=p.Nq), dict(B=p.B, N=p.Nk), dict(B=p.B, N=p.Nk)]
+    for name, x, kw, g in zip(("q", "k", "v"), (q, p.k, v), seq, got):
+        assert_quantized_equal(g, oracle.quantize_fp8(x, **kw), f"sweep {i} {name}")
