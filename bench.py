@@ -692,20 +692,24 @@ def run_reference(args, world, rank):
         prefill = prefills[0] if prefills else None
     if name in BWD_WORKLOADS:
         rate_fn = lambda s: oracle_bwd_rate(prefill, grad, per_step, seed=s)[0]
-        unit, metric_scale = "TFLOP/s", 1e-12
+        unit, metric_scale, full_units = "TFLOP/s", 1e-12, backward_flops(prefill)
     elif prefill is not None:
         rate_fn = lambda s: oracle_sample_rate(prefill, per_step, seed=s)[0]
-        unit, metric_scale = "TFLOP/s", 1e-12
+        unit, metric_scale, full_units = "TFLOP/s", 1e-12, prefill_flops(prefill)
     elif is_kvcache(decode):
         decode = appended_host_copy(decode)
         rate_fn = lambda s: oracle_kvcache_rate(decode, per_step, seed=s)[0]
-        unit, metric_scale = "GB/s", 1e-9
+        unit, metric_scale, full_units = "GB/s", 1e-9, kvcache_bytes(decode)
     else:
         rate_fn = lambda s: oracle_decode_rate(decode, per_step, seed=s)[0]
-        unit, metric_scale = "GB/s", 1e-9
+        unit, metric_scale, full_units = "GB/s", 1e-9, decode_bytes(decode)
     for w in range(args.warmup):
         rate_fn(10_000 + w)
-    rates = [rate_fn(20_000 + s) for s in range(args.steps)]
+    rates, walls = [], []
+    for s in range(args.steps):
+        t0 = time.perf_counter()
+        rates.append(rate_fn(20_000 + s))
+        walls.append(time.perf_counter() - t0)
     value = statistics.median(rates) * metric_scale
     import oracle
     cores = oracle.num_threads()
@@ -715,10 +719,13 @@ def run_reference(args, world, rank):
         wname += "_backward"
         metric = BWD_METRIC
     sample = (f"each step: seeded rows of the {wname} workload, "
-              f"about {per_step:.2f} s of fp64 oracle work, rate = work/seconds")
+              f"about {per_step:.2f} s of fp64 oracle work, rate = work/seconds; ms_per_step is the "
+              f"sample's wall time, ms_per_full_step_extrapolated the whole workload at that rate")
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(walls),
+        "ms_per_full_step_extrapolated": (1e3 * full_units / (value / metric_scale)) if value > 0 else None,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wname},
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
