@@ -148,3 +148,13 @@ def test_million_token_context(la):
     num_pages = sum(-(-L // 16) for L in lens) + 3
     dd = workloads.make_decode(lens, 8, 1, 128, num_pages=num_pages, seed=2110)
     check(la, dd)
+
+
+def test_peaked_softmax(la):
+    """q and the K cache times 8 (exact in bf16): score spreads near +-100,
+    most exponentials underflow and the split partials' lse differ by tens
+    of octaves, so the combine weights span many orders of magnitude."""
+    dd = workloads.make_decode([3000, 17, 800, 4096, 1], 8, 2, 128, num_pages=700, seed=2200,
+                               nan_fill_unused=True, max_pages=256)
+    dd = dataclasses.replace(dd, q=dd.q * 8, k_cache=dd.k_cache * 8)
+    check(la, dd)

@@ -74,6 +74,25 @@ def test_score_ladder_all_rows(la, cfg):
     check_all_rows(la, workloads.score_ladder(p))
 
 
+# Peaked rows: q and k times 8 (exact in bf16) put the scores' spread near
+# +-100 in natural units, so each row's probability mass sits on a few keys and
+# the exponentials of most keys underflow to zero; whole tiles contribute
+# nothing after the first, and the running max jumps by tens of octaves.
+PEAKED = [
+    (1, 4, 2, 300, 1100, 128, False),
+    (1, 4, 2, 300, 1100, 128, True),
+    (2, 4, 1, 260, 700, 64, True),
+]
+
+
+@pytest.mark.parametrize("cfg", PEAKED, ids=lambda c: "B{}_Hq{}_Hkv{}_Nq{}_Nk{}_d{}_{}".format(*c[:6], "c" if c[6] else "n"))
+def test_peaked_softmax_all_rows(la, cfg):
+    B, Hq, Hkv, Nq, Nk, d, causal = cfg
+    p = workloads.make_prefill(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=41 + Nk + d)
+    p = dataclasses.replace(p, q=p.q * 8, k=p.k * 8)
+    check_all_rows(la, p)
+
+
 VARLEN = [
     ([5, 300, 0, 129, 1000, 1], [5, 300, 17, 700, 1000, 1], 128, True),
     ([256, 3, 600], [100, 3, 2000], 128, True),     # a sequence with Nq > Nk
