@@ -202,6 +202,15 @@ def test_tiny_all_rows(la, causal):
     check_fp8(la, p)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_peaked_softmax_all_rows(la, causal):
+    """q and k times 8 (the codes are unchanged, the tile scales grow 8x):
+    score spreads near +-100, most exponentials underflow and the reference
+    max jumps by tens of octaves, with the per-tile score coefficients."""
+    p = workloads.make_prefill(1, 4, 2, 300, 1100, 128, causal=causal, seed=43 + causal)
+    check_fp8(la, dataclasses.replace(p, q=p.q * 8, k=p.k * 8))
+
+
 # (B, Hq, Hkv, Nq, Nk, causal)
 SMALL = [
     (2, 4, 4, 300, 300, True),
