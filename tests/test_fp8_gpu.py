@@ -206,9 +206,11 @@ def test_tiny_all_rows(la, causal):
 def test_peaked_softmax_all_rows(la, causal):
     """q and k times 8 (the codes are unchanged, the tile scales grow 8x):
     score spreads near +-100, most exponentials underflow and the reference
-    max jumps by tens of octaves, with the per-tile score coefficients."""
+    max jumps by tens of octaves, with the per-tile score coefficients.  V
+    times 1/4 keeps |O| where the 1e-2 absolute bound is above a bf16
+    output's rounding (O is a few single V rows here, not an average)."""
     p = workloads.make_prefill(1, 4, 2, 300, 1100, 128, causal=causal, seed=43 + causal)
-    check_fp8(la, dataclasses.replace(p, q=p.q * 8, k=p.k * 8))
+    check_fp8(la, dataclasses.replace(p, q=p.q * 8, k=p.k * 8, v=p.v * 0.25))
 
 
 # (B, Hq, Hkv, Nq, Nk, causal)
