@@ -153,8 +153,10 @@ def test_million_token_context(la):
 def test_peaked_softmax(la):
     """q and the K cache times 8 (exact in bf16): score spreads near +-100,
     most exponentials underflow and the split partials' lse differ by tens
-    of octaves, so the combine weights span many orders of magnitude."""
+    of octaves, so the combine weights span many orders of magnitude.  The
+    V cache times 1/4: O is then a few single V rows, and at |O| >= 2.56 a
+    bf16 output's half step alone exceeds the 1e-2 bound."""
     dd = workloads.make_decode([3000, 17, 800, 4096, 1], 8, 2, 128, num_pages=700, seed=2200,
                                nan_fill_unused=True, max_pages=256)
-    dd = dataclasses.replace(dd, q=dd.q * 8, k_cache=dd.k_cache * 8)
+    dd = dataclasses.replace(dd, q=dd.q * 8, k_cache=dd.k_cache * 8, v_cache=dd.v_cache * 0.25)
     check(la, dd)
