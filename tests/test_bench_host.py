@@ -104,6 +104,10 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the arm's own step time (each step is one bounded sample of ~0.3 s) and the
+    # whole workload's time at the measured rate
+    assert 0.1e3 < line["ms_per_step"] < 60e3
+    assert line["ms_per_full_step_extrapolated"] > 0
 
 
 def test_clock_summary_windows_and_reasons():
