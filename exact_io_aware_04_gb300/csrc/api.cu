@@ -90,6 +90,13 @@ attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const 
 
 attn_status encode_tma(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
                        const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128) {
+    return encode_tma_swizzle(map, dtype, base, rank, dims, strides_bytes, box,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+attn_status encode_tma_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                               CUtensorMapSwizzle swizzle) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -110,8 +117,7 @@ attn_status encode_tma(CUtensorMap* map, CUtensorMapDataType dtype, const void* 
         if (i + 1 < rank) gstride[i] = strides_bytes[i];
     }
     CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
-                          gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d, rank %d)", (int)r, rank);
     return ATTN_OK;
@@ -296,7 +302,7 @@ attn_status attn_fwd_fp8_window(const void* q8, const void* k8, const void* v8, 
         (reinterpret_cast<uintptr_t>(q_scale) & 3u) != 0 || (reinterpret_cast<uintptr_t>(k_scale) & 3u) != 0 ||
         (reinterpret_cast<uintptr_t>(v_scale) & 3u) != 0)
         return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_fp8: misaligned pointer");
-    if (d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8: head_dim %d (built: 128)", d);
+    if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8: head_dim %d (built: 64, 128)", d);
     const bool varlen = cu_seqlens_q != nullptr;
     if (!varlen && (static_cast<long long>(B) * Nq > INT32_MAX || static_cast<long long>(B) * Nk > INT32_MAX))
         return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8: more than 2^31 tokens");

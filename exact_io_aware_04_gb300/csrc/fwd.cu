@@ -70,13 +70,17 @@ constexpr int kChunks = kThreads;            // packed mode: sequences scanned i
 // F8: the 8-bit forward (E4M3 Q, K, V with per-tile scales).
 template <int HD, bool F8 = false>
 struct Cfg {
-    // Q and K tiles: 128-byte column panels (64 bf16 or 128 E4M3 values wide)
-    static constexpr int kPanels = F8 ? HD / 128 : HD / 64;
-    static constexpr int kPanelBytes = kBM * 128;    // 128 rows x 128 bytes
+    // Q and K tiles: 128-byte column panels (64 bf16 or 128 E4M3 values
+    // wide, 128-byte swizzle), or for the 8-bit tiles at d = 64 one panel of
+    // 64-byte rows (64-byte swizzle)
+    static constexpr int kRowBytes = (F8 && HD < 128) ? HD : 128;
+    static constexpr int kPanels = F8 ? (HD + 127) / 128 : HD / 64;
+    static constexpr int kPanelBytes = kBM * kRowBytes;
     static constexpr int kTileBytes = kPanels * kPanelBytes;
     // the V tile as the PV product reads it: 16-bit values (bf16, or f16
-    // converted from E4M3), 64-element panels
-    static constexpr int kVBytes = (HD / 64) * kPanelBytes;
+    // converted from E4M3), 64-element (128-byte) panels
+    static constexpr int kVPanelBytes = kBM * 128;
+    static constexpr int kVBytes = (HD / 64) * kVPanelBytes;
     // K/V ring: slot u of an item holds V_{u-1} and K_u (what one step of
     // the MMA issuer consumes), so each step needs one wait and one release
     static constexpr int kStages = HD == 128 ? 2 : 4;
@@ -414,7 +418,7 @@ struct Widen {
         for (int par = 0; par < 2; ++par) {
             const int ph = r0 + 4 * par;  // row % 8 for rows 4 i + r0 with i % 2 == par
             src_off[par] = r0 * 128 + ((kc ^ ph) << 4);
-            const uint32_t prow = (kc >> 2) * C::kPanelBytes + r0 * 128;
+            const uint32_t prow = (kc >> 2) * C::kVPanelBytes + r0 * 128;
             dst_off[par][0] = prow + (((2 * (kc & 3)) ^ ph) << 4);
             dst_off[par][1] = prow + (((2 * (kc & 3) + 1) ^ ph) << 4);
         }
@@ -441,6 +445,48 @@ struct Widen {
                          "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
                          : "memory");
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off[par][1] + i * 512),
+                         "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+    }
+};
+
+// d = 64: the staged E4M3 rows are 64 bytes, unswizzled; the f16 tile is one
+// 128-byte-swizzled panel.  Lane l converts code chunk kc = l % 4 (values
+// 16 kc .. 16 kc + 15) of key rows 8 i + l / 4 into f16 chunks 2 kc and
+// 2 kc + 1 of the same rows; a lane's rows all have the swizzle phase l / 4.
+// A warp request reads 512 contiguous bytes (eight rows).
+template <>
+struct Widen<64> {
+    uint32_t src_off, dst_off0, dst_off1;
+
+    __device__ __forceinline__ explicit Widen(int lane) {
+        const int kc = lane & 3, r0 = lane >> 2;
+        src_off = r0 * 64 + kc * 16;
+        dst_off0 = r0 * 128 + (((2 * kc) ^ r0) << 4);
+        dst_off1 = r0 * 128 + (((2 * kc + 1) ^ r0) << 4);
+    }
+
+    // Key rows 64 half .. 64 half + 63 (row groups 8 half .. 8 half + 7).
+    __device__ __forceinline__ void run(uint32_t src0, uint32_t dst0, int half) const {
+#pragma unroll
+        for (int i2 = 0; i2 < 8; ++i2) {
+            const int i = half * 8 + i2;
+            uint32_t w0, w1, w2, w3;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                         : "r"(src0 + src_off + i * 512)
+                         : "memory");
+            uint32_t h[8];
+            e4m3x4_to_f16x2x2(w0, h[0], h[1]);
+            e4m3x4_to_f16x2x2(w1, h[2], h[3]);
+            e4m3x4_to_f16x2x2(w2, h[4], h[5]);
+            e4m3x4_to_f16x2x2(w3, h[6], h[7]);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off0 + i * 1024),
+                         "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                         : "memory");
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst0 + dst_off1 + i * 1024),
                          "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
                          : "memory");
         }
@@ -585,6 +631,24 @@ __device__ __noinline__ void role_producer_f8(const FwdParams& p, const Schedule
 }
 
 // ---------------------------------------------------------------- MMA warp (one thread)
+// Shared-memory descriptor of a K-major Q or K tile: 128-byte rows with the
+// 128-byte swizzle (8-row groups 1024 bytes apart), or, for the 8-bit tiles
+// at d = 64, 64-byte rows with the 64-byte swizzle (groups 512 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t desc = 0;
+    desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    desc |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    desc |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    desc |= 1ull << 46;  // descriptor version for tcgen05
+    desc |= 4ull << 61;  // 64-byte swizzle
+    return desc;
+}
+template <int HD, bool F8>
+__device__ __forceinline__ uint64_t qk_desc(uint32_t saddr) {
+    if constexpr (Cfg<HD, F8>::kRowBytes == 64) return smem_desc_sw64(saddr, 16, 512);
+    else return smem_desc_sw128(saddr, 16, 1024);
+}
+
 // Descriptors are built once per kernel; each K-step adds a compile-time
 // offset (the 14-bit start-address field never overflows: shared memory is
 // below 256 KB).  The tensor pipe's input queue is shallow, so issue is
@@ -639,9 +703,9 @@ __device__ __noinline__ void role_mma(const FwdParams& p, const Schedule& sc, ui
     using BI = BarIdx<C::kStages, F8, C::kV8Stages>;
     constexpr int S = C::kStages;
     const uint32_t ring0 = smem0 + 2 * C::kTileBytes;
-    const uint64_t dq = smem_desc_sw128(smem0 + t * C::kTileBytes, 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(ring0, 16, 1024);                              // K part of slot 0
-    const uint64_t dv0 = smem_desc_sw128(ring0 + C::kTileBytes, C::kPanelBytes, 1024);  // V part of slot 0
+    const uint64_t dq = qk_desc<HD, F8>(smem0 + t * C::kTileBytes);
+    const uint64_t dk0 = qk_desc<HD, F8>(ring0);                                         // K part of slot 0
+    const uint64_t dv0 = smem_desc_sw128(ring0 + C::kTileBytes, C::kVPanelBytes, 1024);  // V part of slot 0
     constexpr uint64_t kSlotDesc = C::kSlotBytes >> 4;  // descriptor step between ring slots
     const uint32_t ts = tmem + C::col_s(t);
     const uint32_t to = tmem + C::col_o(t);
@@ -1120,23 +1184,27 @@ attn_status launch_typed(const FwdArgs& a, const DeviceInfo& dev, cudaStream_t s
     // encodable, so they get one row.
     uint64_t t_k = varlen ? static_cast<uint64_t>(a.Nk) : static_cast<uint64_t>(a.B) * a.Nk;
     if (t_k == 0) t_k = 1;
-    // boxes of 128 bytes x 128 rows: 64 bf16 or 128 E4M3 values wide
+    // boxes of 128 bytes x 128 rows (64 bf16 or 128 E4M3 values wide,
+    // 128-byte swizzle); the 8-bit tiles at d = 64 are 64 bytes wide (Q and K
+    // with the 64-byte swizzle, V staged unswizzled for the widening warps)
     constexpr uint64_t kElem = F8 ? 1 : 2;
     const CUtensorMapDataType dtype = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const uint32_t box[2] = {static_cast<uint32_t>(128 / kElem), kBM};
+    const uint32_t box[2] = {static_cast<uint32_t>(C::kRowBytes / kElem), kBM};
+    const CUtensorMapSwizzle sw_qk = C::kRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapSwizzle sw_v = C::kRowBytes == 64 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(a.Hq) * HD, t_q};
         const uint64_t strides[1] = {static_cast<uint64_t>(a.Hq) * HD * kElem};
-        attn_status st = encode_tma(&p.tm_q, dtype, a.q, 2, dims, strides, box, true);
+        attn_status st = encode_tma_swizzle(&p.tm_q, dtype, a.q, 2, dims, strides, box, sw_qk);
         if (st != ATTN_OK) return st;
     }
     {
         // with no keys the maps point at q (one row, never read)
         const uint64_t dims[2] = {static_cast<uint64_t>(a.Hkv) * HD, t_k};
         const uint64_t strides[1] = {static_cast<uint64_t>(a.Hkv) * HD * kElem};
-        attn_status st = encode_tma(&p.tm_k, dtype, a.k, 2, dims, strides, box, true);
+        attn_status st = encode_tma_swizzle(&p.tm_k, dtype, a.k, 2, dims, strides, box, sw_qk);
         if (st != ATTN_OK) return st;
-        st = encode_tma(&p.tm_v, dtype, a.v, 2, dims, strides, box, true);
+        st = encode_tma_swizzle(&p.tm_v, dtype, a.v, 2, dims, strides, box, sw_v);
         if (st != ATTN_OK) return st;
     }
     if constexpr (F8) {
@@ -1228,6 +1296,7 @@ attn_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
     attn_status st = current_device_info(&dev);
     if (st != ATTN_OK) return st;
     if (a.d == 128) return launch_typed<128, true>(a, dev, stream);
+    if (a.d == 64) return launch_typed<64, true>(a, dev, stream);
     return ATTN_ERR_UNSUPPORTED;
 }
 

@@ -36,6 +36,10 @@ attn_status encode_tma_bf16(CUtensorMap* map, const void* base, int rank, const 
 // The same for any element type (8-bit codes use CU_TENSOR_MAP_DATA_TYPE_UINT8).
 attn_status encode_tma(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank, const uint64_t* dims,
                        const uint64_t* strides_bytes, const uint32_t* box, bool swizzle128);
+// The same with any swizzle mode (the 8-bit tiles at d = 64 use the 64-byte one).
+attn_status encode_tma_swizzle(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                               const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                               CUtensorMapSwizzle swizzle);
 
 bool validation_enabled();
 // With validation on: checks packed offsets cu[0..B] (start 0, nondecreasing,

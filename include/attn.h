@@ -210,7 +210,7 @@ attn_status attn_quantize_fp8_qkv(const void *q, const void *k, const void *v,
  * [Hq, attn_fp8_scale_count(B, T_q)], k_scale and v_scale [Hkv,
  * attn_fp8_scale_count(B, T_k)], fp32, tiles as attn_quantize_fp8 cuts them
  * (from the same B, N or cu_seqlens).  out, lse, B, Hq, Hkv, Nq, Nk, scale,
- * causal and the cu_seqlens as attn_fwd.  d == 128 only (others:
+ * causal and the cu_seqlens as attn_fwd.  d in {64, 128} (others:
  * ATTN_ERR_UNSUPPORTED).
  * Rejects (ATTN_ERR_INVALID_ARG): attn_fwd's cases, NULL or misaligned
  * (4-byte) scale pointers.  k8, v8, k_scale, v_scale may be NULL only when

@@ -156,7 +156,7 @@ def test_fp8_host_rejections(lib):
     assert f(Hq=5) == -1
     assert f(causal=3) == -1
     assert f(cq=FAKE) == -1
-    assert f(d=64) == -2                               # the 8-bit forward is built for d = 128
+    assert f(d=96) == -2                               # the 8-bit forward is built for d = 64 and 128
     assert f(B=0) == 0
     # scale entries: T // 128 + B per head
     assert lib.attn_fp8_scale_count(2, 512) == 6 and lib.attn_fp8_scale_count(16, 8192) == 80
@@ -166,7 +166,7 @@ def test_fp8_host_rejections(lib):
         return lib.attn_fwd_fp8_window(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, 4, 2, 8, 8, d, 0.1, 0,
                                        left, right, None, None, None)
     assert w(-2, 5) == -1 and w(5, -3) == -1          # window sides below -1
-    assert w(5, 5, d=64) == -2
+    assert w(5, 5, d=96) == -2
     assert w(5, 5, B=0) == 0 and w(-1, -1, B=0) == 0
 
 

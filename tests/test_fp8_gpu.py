@@ -196,9 +196,11 @@ def check_fp8(la, p, rows=None):
     return assert_close(p.name + " fp8", go, gl, ref_o, ref_lse)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_tiny_all_rows(la, causal):
-    p = workloads.make_prefill(1, 2, 2, 256, 256, 128, causal=causal, seed=1000, name="tiny_d128")
+def test_tiny_all_rows(la, causal, d):
+    """The tiny configuration (B1, H2, N256; d = 64 as configured, and d = 128)."""
+    p = workloads.make_prefill(1, 2, 2, 256, 256, d, causal=causal, seed=1000, name=f"tiny_d{d}")
     check_fp8(la, p)
 
 
@@ -226,10 +228,11 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: "B{}_Hq{}_Hkv{}_Nq{}_Nk{}_{}".format(*c[:5], "c" if c[5] else "n"))
-def test_small_problems(la, cfg):
+def test_small_problems(la, cfg, d):
     B, Hq, Hkv, Nq, Nk, causal = cfg
-    check_fp8(la, workloads.make_prefill(B, Hq, Hkv, Nq, Nk, 128, causal=causal, seed=sum(cfg[:5]) + 7))
+    check_fp8(la, workloads.make_prefill(B, Hq, Hkv, Nq, Nk, d, causal=causal, seed=sum(cfg[:5]) + 7 + d))
 
 
 @pytest.mark.parametrize("q_lens,k_lens", [
@@ -239,6 +242,11 @@ def test_small_problems(la, cfg):
 ])
 def test_varlen(la, q_lens, k_lens):
     check_fp8(la, workloads.make_varlen(q_lens, k_lens, 4, 2, 128, causal=True, seed=len(q_lens) + 60))
+
+
+def test_varlen_d64(la):
+    check_fp8(la, workloads.make_varlen([5, 1, 33, 0, 130, 300], [5, 9, 200, 4, 130, 1000], 4, 2, 64, causal=True,
+                                        seed=161))
 
 
 def test_no_keys_gives_zero_rows(la):
@@ -255,11 +263,12 @@ def test_score_ladder_all_rows(la, causal):
     check_fp8(la, p)
 
 
-def test_one_hot_attended_keys(la):
+@pytest.mark.parametrize("d", [64, 128])
+def test_one_hot_attended_keys(la, d):
     """Q = 0 (every allowed key weighs 1/|A_i|), V one-hot by key index over a
     window of d keys: the nonzero pattern of O is the allowed set exactly,
     its magnitude names the K/V head, and exp(lse) is the allowed count."""
-    p = workloads.make_varlen([3, 130, 200], [70, 300, 128], 4, 2, 128, causal=True, seed=66)
+    p = workloads.make_varlen([3, 130, 200], [70, 300, 128], 4, 2, d, causal=True, seed=66)
     for base in (0, 60, 200):
         ph = workloads.one_hot_values(p, base)
         args, kw, qz = fp8_inputs(ph)
@@ -277,10 +286,11 @@ def test_one_hot_attended_keys(la):
         assert np.array_equal(np.rint(np.exp(gl[fin])), cnt[fin])
 
 
-def test_quantize_then_forward_end_to_end(la):
+@pytest.mark.parametrize("d", [64, 128])
+def test_quantize_then_forward_end_to_end(la, d):
     """The GPU's own quantization feeds the GPU forward; the oracle quantizes
     the same bf16 inputs itself."""
-    p = workloads.make_varlen([300, 77], [900, 77], 8, 2, 128, causal=True, seed=67)
+    p = workloads.make_varlen([300, 77], [900, 77], 8, 2, d, causal=True, seed=67)
     g = p.to("cuda")
     (q8, qs), (k8, ks), (v8, vs) = la.attn_quantize_fp8_qkv(g.q, g.k, g.v, cu_seqlens_q=g.cu_q, cu_seqlens_k=g.cu_k)
     out, lse = la.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, causal=True, scale=p.scale, cu_seqlens_q=g.cu_q,
@@ -417,8 +427,9 @@ def test_window_dense(la, window, causal):
     check_fp8(la, workloads.make_prefill(1, 4, 2, 400, 700, 128, causal=causal, seed=1950, window=window))
 
 
-def test_window_varlen(la):
-    check_fp8(la, workloads.make_varlen([200, 5, 300, 0], [700, 5, 300, 9], 4, 2, 128, causal=False, seed=1951,
+@pytest.mark.parametrize("d", [64, 128])
+def test_window_varlen(la, d):
+    check_fp8(la, workloads.make_varlen([200, 5, 300, 0], [700, 5, 300, 9], 4, 2, d, causal=False, seed=1951,
                                         window=(90, 40)))
 
 

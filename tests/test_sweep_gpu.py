@@ -46,7 +46,7 @@ def window(r):
 def prefill_case(i, fp8=False, bwd=False):
     r = np.random.RandomState(7100 + 97 * i + (5000 if fp8 else 0) + (9000 if bwd else 0))
     Hq, Hkv = heads(r, 8 if bwd else 16)
-    d = 128 if fp8 else int(r.choice([64, 128]))
+    d = int(r.choice([64, 128]))
     causal = bool(r.rand() < 0.6)
     win = window(r)
     if win is not None and causal:
