@@ -276,9 +276,10 @@ def attn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: 
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                  window: Optional[tuple] = None, stream=None):
     """Prefill forward on per-tile E4M3 q8, k8, v8 (uint8 codes, shaped as
-    attn_fwd's q, k, v) with their fp32 tile scales from attn_quantize_fp8.
-    window = (left, right) selects the local band mask (attn_fwd_fp8_window).
-    Returns (out bf16 shaped like q8, lse) as attn_fwd."""
+    attn_fwd's q, k, v; d = 64 or 128) with their fp32 tile scales from
+    attn_quantize_fp8 or attn_quantize_fp8_qkv.  window = (left, right)
+    selects the local band mask (attn_fwd_fp8_window).  Returns (out bf16
+    shaped like q8, lse) as attn_fwd."""
     for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
         _need(t, n, torch.uint8)
     for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
